@@ -1,0 +1,113 @@
+"""Seeded synthetic workloads for Longformer sparse attention.
+
+This module only describes problem shapes and draws random inputs; it holds
+none of the attention arithmetic, so both the CUDA path's tests/bench and the
+CPU oracle can take their inputs from it without sharing any of the method.
+
+Input recipe (the same for every configuration):
+  * ``g = torch.Generator('cpu').manual_seed(seed)``;
+  * ``q, k, v = torch.randn((B, H, L, D), generator=g, dtype=torch.float32)``,
+    drawn in that order (iid N(0, 1));
+  * the arithmetic inputs are those values rounded to bf16 (round to nearest
+    even).  Configurations with fp32 inputs keep the fp32 tensors for the
+    call, and both sides round them to bf16 before any product.
+
+The window size w is one-sided (2w+1 keys including the query itself), the
+dilation is per head, and the global token positions are a sorted list.
+Scale is 1/sqrt(D) for every configuration.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    L: int
+    D: int
+    w: int
+    dilation: tuple          # per head, len H
+    global_idx: tuple        # sorted, strictly increasing
+    seed: int
+    in_dtype: str            # "fp32" or "bf16"
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def n_global(self) -> int:
+        return len(self.global_idx)
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name, "B": self.B, "H": self.H, "L": self.L,
+            "D": self.D, "w": self.w, "dilation": list(self.dilation),
+            "n_global": self.n_global, "in_dtype": self.in_dtype,
+            "seed": self.seed,
+        }
+
+
+def _long_globals(L: int = 65536, n: int = 16, seed: int = 4) -> tuple:
+    """16 distinct positions drawn uniformly from [0, L) with a fresh generator."""
+    g = torch.Generator().manual_seed(seed)
+    return tuple(sorted(torch.randperm(L, generator=g)[:n].tolist()))
+
+
+# The five synthetic configurations (tiny is the one the oracle finishes in
+# well under a second; base is the L=4096 headline workload).
+CONFIGS = {
+    "tiny": Workload("tiny", 1, 2, 512, 64, 32, (1, 1), (0, 1), 0, "fp32"),
+    "base": Workload("base", 2, 12, 4096, 64, 256, (1,) * 12, (0,), 1, "bf16"),
+    "dilated": Workload("dilated", 1, 12, 8192, 64, 128, (1,) * 8 + (2,) * 4,
+                        (0,), 2, "bf16"),
+    "qa": Workload("qa", 4, 16, 4096, 64, 256, (1,) * 16, tuple(range(64)), 3,
+                   "bf16"),
+    "long": Workload("long", 1, 16, 65536, 128, 512, (1,) * 16,
+                     _long_globals(), 4, "bf16"),
+}
+
+CONFIG_ORDER = ["tiny", "base", "dilated", "qa", "long"]
+
+
+def custom(name: str, B: int, H: int, L: int, D: int, w: int,
+           dilation: Sequence[int], global_idx: Sequence[int], seed: int,
+           in_dtype: str = "bf16") -> Workload:
+    return Workload(name, B, H, L, D, w, tuple(int(x) for x in dilation),
+                    tuple(int(x) for x in global_idx), seed, in_dtype)
+
+
+def make_qkv(wl: Workload, generator_device: str = "cpu"):
+    """Draw q, k, v for a workload.
+
+    Returns (q, k, v) as CPU tensors of the call dtype: bf16 for bf16
+    workloads, fp32 for fp32 ones.  Use :func:`bf16_round_f64` to get the
+    exact values the arithmetic sees.
+    """
+    g = torch.Generator(generator_device).manual_seed(wl.seed)
+    shape = (wl.B, wl.H, wl.L, wl.D)
+    out = []
+    for _ in range(3):
+        t = torch.randn(shape, generator=g, dtype=torch.float32)
+        if wl.in_dtype == "bf16":
+            t = t.to(torch.bfloat16)
+        out.append(t)
+    return tuple(out)
+
+
+def bf16_round_f64(t: torch.Tensor):
+    """The bf16-rounded values of ``t`` as a float64 numpy array."""
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def random_globals(L: int, n: int, seed: int) -> tuple:
+    g = torch.Generator().manual_seed(seed)
+    n = min(n, L)
+    return tuple(sorted(torch.randperm(L, generator=g)[:n].tolist()))

@@ -1,0 +1,5 @@
+"""CPU oracle (test infrastructure only): see ``oracle.lf_oracle``."""
+from .lf_oracle import (  # noqa: F401
+    attention, attention_row_bruteforce, band_offsets, key_lists, key_set,
+    mask_rows, pair_count, total_pairs, useful_flops,
+)

@@ -1,0 +1,248 @@
+"""Plain fp64 CPU oracle for Longformer sparse self-attention (forward).
+
+TEST INFRASTRUCTURE.  Only the test-suite, the smoke check and the bench's
+CPU-baseline / reference leg may import or run this module.  It shares no code
+with the CUDA library and imports nothing from it.
+
+Sources (web pages; cited by title and section):
+  [LF-explained]  "基于自注意力机制的长文本建模算法：Longformer详解"
+                  (Longformer explained), sections 2-4.
+  [LF-blocksparse] "基于Block-Sparse Attention的Longformer：降低长序列计算复杂度
+                  至O(n)的实现" (block-sparse Longformer), sections 2-4.
+  [Reformer-hash] "Reformer哈希", section "核心原理" (the attention formula).
+  [Eff-survey]    the commentary on "Efficient Transformers: A Survey",
+                  section 2.1 (where the cost of dense attention comes from).
+
+What is computed (the plain definition; readings of open points are listed
+in the repository's design notes and repeated at each function):
+
+  For head h with dilation d = dilation[h], one-sided window w, sequence
+  length L and the sorted global positions G:
+    band(i) = { i + d*t : |t| <= w, 0 <= i + d*t < L }
+                  ([LF-explained] §2 sliding window; §2 dilated window)
+    K(i)    = [0, L)          if i in G      ([LF-explained] §2 global attention)
+            = band(i) ∪ G     otherwise      (the union, each key once)
+    s_ij    = scale * <q_i, k_j>             ([Reformer-hash] 核心原理 formula)
+    p_ij    = exp(s_ij - max_{K(i)} s) / sum_{j' in K(i)} exp(s_ij' - max)
+    out_i   = sum_{j in K(i)} p_ij v_j       (one softmax over all of K(i):
+                  [LF-explained] §4, the three patterns combined)
+
+All arithmetic is float64 on whatever values are passed in (callers pass the
+bf16-rounded inputs).  The dense-masked form below builds full [rows, L] score
+blocks and sets every key outside K(i) to -inf, which is exactly the
+definition above: exp(-inf) = 0 removes those keys from both sums.
+
+Parity status: every function here is pinned by tests in
+``tests/test_oracle.py`` against values the pages print, closed forms,
+library routines and brute force; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# Key sets
+# --------------------------------------------------------------------------
+
+def band_offsets(i: int, L: int, w: int, d: int) -> List[int]:
+    """band(i): the dilated sliding window of query i, clipped to [0, L).
+
+    [LF-explained] §2: each token attends to a fixed number of neighbours on
+    each side (one-sided width w); with dilation d the attended positions are
+    i-d*w, ..., i-d, i, i+d, ..., i+d*w.  Positions outside the sequence are
+    dropped (no wrap-around, no padding).
+    """
+    keys = []
+    for t in range(-w, w + 1):
+        j = i + d * t
+        if 0 <= j < L:
+            keys.append(j)
+    return keys
+
+
+def key_set(i: int, L: int, w: int, d: int, G: Sequence[int]) -> List[int]:
+    """K(i) as a sorted list (see the module docstring)."""
+    Gs = set(int(g) for g in G)
+    if i in Gs:
+        # [LF-explained] §2 global attention: a global token sees the whole
+        # sequence.
+        return list(range(L))
+    # Every token also attends to the global tokens ([LF-blocksparse] §4).
+    return sorted(set(band_offsets(i, L, w, d)) | Gs)
+
+
+def mask_rows(rows: np.ndarray, L: int, w: int, d: int,
+              G: Sequence[int]) -> np.ndarray:
+    """Boolean [len(rows), L] mask, True where key j is in K(row).
+
+    Vectorised form of :func:`key_set`: j is in band(i) iff |i-j| <= d*w and
+    d divides i-j (then i-j = d*t with |t| <= w).
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    j = np.arange(L, dtype=np.int64)[None, :]
+    i = rows[:, None]
+    diff = j - i
+    m = (np.abs(diff) <= d * w) & (diff % d == 0)
+    G = np.asarray(G, dtype=np.int64)
+    if G.size:
+        m[:, G] = True
+        is_g = np.isin(rows, G)
+        m[is_g, :] = True
+    return m
+
+
+def pair_count(L: int, w: int, d: int, G: Sequence[int]) -> int:
+    """Number of attended (query, key) pairs of one head, in closed form.
+
+    Sliding window: sum_i |band(i)| = L + 2 * sum_{t=1..w} max(0, L - t*d)
+    (each offset +-t*d is valid for exactly L - t*d queries).  This is the
+    exact, edge-clipped form of the O(n*w) count ([LF-explained] §2,
+    [LF-blocksparse] §3).  Global rows add n_g*L ([LF-blocksparse] §4, the
+    O(n*g) term); each non-global query gains the globals outside its band.
+    """
+    G = sorted(set(int(g) for g in G))
+    band_total = L + 2 * sum(max(0, L - t * d) for t in range(1, w + 1))
+    if not G:
+        return band_total
+    Gset = set(G)
+    total = len(G) * L
+    # Non-global rows: |band(i)| + |G \ band(i)|.
+    band_nonglobal = band_total - sum(_band_size(g, L, w, d) for g in G)
+    extra = 0
+    for g in G:
+        # Number of non-global queries i whose band does NOT contain g:
+        # (L - n_g) minus the non-global i with g in band(i).  By symmetry
+        # of the relation, g in band(i) iff i in band(g).
+        in_band_of_g = [i for i in _band_members(g, L, w, d) if i not in Gset]
+        extra += (L - len(G)) - len(in_band_of_g)
+    return total + band_nonglobal + extra
+
+
+def _band_size(i: int, L: int, w: int, d: int) -> int:
+    return 1 + min(w, i // d) + min(w, (L - 1 - i) // d)
+
+
+def _band_members(i: int, L: int, w: int, d: int) -> List[int]:
+    lo = max(-w, -(i // d))
+    hi = min(w, (L - 1 - i) // d)
+    return [i + d * t for t in range(lo, hi + 1)]
+
+
+def key_lists(L: int, w: int, dilation: Sequence[int], G: Sequence[int],
+              rows: Optional[Iterable[Tuple[int, int]]] = None):
+    """Per-(head, query) sorted key lists in CSR form.
+
+    Without ``rows`` every (h, i) row in head-major order is listed and the
+    result is (row_ptr int64 [H*L+1], col_idx int32 [total]).  With ``rows``
+    (an iterable of (h, i)) only those rows are listed, in that order.
+    """
+    H = len(dilation)
+    if rows is None:
+        rows = [(h, i) for h in range(H) for i in range(L)]
+    rows = list(rows)
+    G = np.asarray(sorted(int(g) for g in G), dtype=np.int64)
+    Gset = set(G.tolist())
+    ptr = [0]
+    cols: List[np.ndarray] = []
+    for (h, i) in rows:
+        d = int(dilation[h])
+        if i in Gset:
+            c = np.arange(L, dtype=np.int64)
+        else:
+            lo = max(-w, -(i // d))
+            hi = min(w, (L - 1 - i) // d)
+            band = i + d * np.arange(lo, hi + 1, dtype=np.int64)
+            c = np.union1d(band, G)
+        cols.append(c)
+        ptr.append(ptr[-1] + c.size)
+    col = (np.concatenate(cols) if cols else np.zeros(0, np.int64))
+    return np.asarray(ptr, dtype=np.int64), col.astype(np.int32)
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
+              dilation: Sequence[int], G: Sequence[int], scale: float,
+              rows: Optional[Sequence[int]] = None,
+              chunk: int = 256) -> np.ndarray:
+    """Longformer sparse self-attention forward, dense-masked, float64.
+
+    q, k, v: arrays [B, H, L, D] (any float type; promoted to float64).
+    Returns out [B, H, L, D] float64, or [B, H, len(rows), D] when ``rows``
+    (a list of query positions shared by all heads) is given.
+
+    For each (b, h) and each chunk of query rows: scores = scale * Q K^T over
+    all L keys ([Reformer-hash] 核心原理), keys outside K(i) set to -inf
+    (exact exclusion: the reading of "attends only to" in [LF-explained] §2),
+    one row softmax ([LF-explained] §4: the patterns share one normalisation),
+    then the product with V.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, L, D = q.shape
+    if rows is None:
+        rows_arr = np.arange(L, dtype=np.int64)
+    else:
+        rows_arr = np.asarray(rows, dtype=np.int64)
+    out = np.empty((B, H, rows_arr.size, D), dtype=np.float64)
+    for h in range(H):
+        d = int(dilation[h])
+        for c0 in range(0, rows_arr.size, chunk):
+            r = rows_arr[c0:c0 + chunk]
+            m = mask_rows(r, L, w, d, G)
+            for b in range(B):
+                s = (q[b, h, r, :] @ k[b, h].T) * scale
+                s = np.where(m, s, -np.inf)
+                s = s - s.max(axis=1, keepdims=True)
+                p = np.exp(s)
+                p /= p.sum(axis=1, keepdims=True)
+                out[b, h, c0:c0 + r.size, :] = p @ v[b, h]
+    return out
+
+
+def attention_row_bruteforce(q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                             b: int, h: int, i: int, w: int, d: int,
+                             G: Sequence[int], scale: float) -> List[float]:
+    """One output row with scalar Python loops over K(i) (tiny inputs only).
+
+    Written directly from the definition with math.exp and math.fsum, as an
+    independent check of the dense-masked form.
+    """
+    L = q.shape[2]
+    D = q.shape[3]
+    keys = key_set(i, L, w, d, G)
+    s = []
+    for j in keys:
+        acc = math.fsum(float(q[b, h, i, e]) * float(k[b, h, j, e])
+                        for e in range(D))
+        s.append(scale * acc)
+    mx = max(s)
+    e = [math.exp(x - mx) for x in s]
+    z = math.fsum(e)
+    return [math.fsum(e[n] * float(v[b, h, j, c]) for n, j in enumerate(keys)) / z
+            for c in range(D)]
+
+
+def useful_flops(B: int, H: int, D: int, pairs_all_heads: int) -> int:
+    """Useful FLOPs of the forward: 2*D for q.k plus 2*D for p*v per pair."""
+    return 4 * B * D * pairs_all_heads
+
+
+def total_pairs(L: int, w: int, dilation: Sequence[int],
+                G: Sequence[int]) -> int:
+    """Attended pairs summed over heads (batch-independent)."""
+    cache = {}
+    tot = 0
+    for d in dilation:
+        d = int(d)
+        if d not in cache:
+            cache[d] = pair_count(L, w, d, G)
+        tot += cache[d]
+    return tot
