@@ -1,0 +1,167 @@
+/*
+ * lfattn — Longformer sparse self-attention (forward) on one B300 GPU.
+ *
+ * The operation (sources are web pages, cited by title and section):
+ *   "基于自注意力机制的长文本建模算法：Longformer详解" (Longformer explained)
+ *       §2 sliding window, dilated sliding window and global attention;
+ *       §4 the patterns combined under one attention.
+ *   "基于Block-Sparse Attention的Longformer" (block-sparse Longformer)
+ *       §3 sliding-window attention, §4 global attention.
+ *   "Reformer哈希" §核心原理: Attention(Q,K,V) = softmax(QK^T/sqrt(d)) V.
+ *
+ * For head h with dilation d = dilation[h], one-sided window w, sequence
+ * length L and sorted global positions G (n_global of them):
+ *   band(i) = { i + d*t : |t| <= w, 0 <= i + d*t < L }
+ *   K(i)    = [0, L)          if i is in G (global tokens see every key)
+ *           = band(i) ∪ G     otherwise (every token sees the globals; each
+ *                             key counted once)
+ *   out_i   = sum_{j in K(i)} softmax_j(scale * q_i . k_j) v_j
+ * with one softmax per query row over all of K(i).
+ *
+ * Conventions shared by every call:
+ *   - Tensors are contiguous [B, H, L, D] (heads already split), row-major.
+ *   - Tensor pointers are DEVICE pointers owned by the caller, unless the
+ *     function says otherwise; they must be 16-byte aligned.
+ *   - dilation[] and global_idx[] are HOST arrays read during the call.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream); only lf_attn_get_status,
+ *     lf_attn_pairs (which returns a count) and lf_attn_fwd_host block.
+ *   - Library-owned state: a cache of per-shape plans (device work lists and
+ *     the global-position table) and per-call scratch taken from the
+ *     stream-ordered allocator (cudaMallocAsync / cudaFreeAsync).
+ *   - No C++ exception crosses this interface.  A non-OK status leaves a
+ *     message for lf_last_error() in the calling thread.
+ *   - Device-side waits are bounded; a wait that runs out records a timeout
+ *     that lf_attn_get_status reports (the kernel then returns cleanly and
+ *     the outputs of that call are undefined).
+ */
+#ifndef LFATTN_H
+#define LFATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LF_OK = 0,
+  LF_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment, index list or scale */
+  LF_ERR_UNSUPPORTED = 2,   /* valid but not implemented (see each call) */
+  LF_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  LF_ERR_NOMEM = 4,         /* device allocation failed */
+  LF_ERR_TIMEOUT = 5        /* a device-side wait ran out (lf_attn_get_status) */
+} lf_status;
+
+typedef void* lf_stream_t; /* cudaStream_t */
+
+#if defined(__GNUC__)
+#define LF_API __attribute__((visibility("default")))
+#else
+#define LF_API
+#endif
+
+/*
+ * lf_attn_fwd — sparse attention forward, bf16 in / bf16 out.
+ *
+ *   q, k, v   device, bf16 [B,H,L,D], read only.
+ *   out       device, bf16 [B,H,L,D], written (every element).
+ *   B, H, L   >= 1.  D in {64, 128}.  w >= 0 (one-sided window).
+ *   dilation  host int32[H], each >= 1.  For d > 1, L % d must be 0
+ *             (else LF_ERR_UNSUPPORTED).  At most 8 distinct values.
+ *   global_idx host int32[n_global], strictly increasing, in [0, L);
+ *             may be NULL when n_global == 0.  0 <= n_global <= L.
+ *   scale     finite, > 0 (the configurations use 1/sqrt(D)).
+ *   stream    cudaStream_t.
+ *
+ * Arithmetic: products in bf16 on the tensor cores with fp32 accumulation,
+ * softmax in fp32, probabilities rounded to bf16 before the product with V,
+ * output rounded to bf16 (round to nearest even).
+ */
+LF_API lf_status lf_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int H,
+                      int L, int D, int w, const int32_t* dilation, const int32_t* global_idx,
+                      int n_global, float scale, lf_stream_t stream);
+
+/*
+ * lf_attn_fwd_f32 — same operation with fp32 q/k/v/out.  q, k and v are
+ * rounded to bf16 (nearest even) on the device first; the output is written
+ * in fp32 without the final bf16 rounding.  Same arguments and errors as
+ * lf_attn_fwd, all tensors fp32.
+ */
+LF_API lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, int H,
+                          int L, int D, int w, const int32_t* dilation,
+                          const int32_t* global_idx, int n_global, float scale,
+                          lf_stream_t stream);
+
+/*
+ * lf_attn_fwd_host — lf_attn_fwd (is_f32 == 0) or lf_attn_fwd_f32
+ * (is_f32 != 0) on HOST buffers: copies q, k, v to device memory it
+ * allocates on `stream`, runs the forward, copies the result into the host
+ * buffer `out` and synchronises the stream before returning.  Pinned host
+ * memory gives asynchronous copies; pageable memory works too.
+ */
+LF_API lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, void* out, int is_f32,
+                           int B, int H, int L, int D, int w, const int32_t* dilation,
+                           const int32_t* global_idx, int n_global, float scale,
+                           lf_stream_t stream);
+
+/*
+ * lf_attn_pairs — the attended key lists, per (head, query), in CSR form.
+ * Batch-independent (the pattern does not depend on b).
+ *
+ *   row_ptr   device int64[H*L + 1]: row (h, i) is index h*L + i; its keys
+ *             are col_idx[row_ptr[r] .. row_ptr[r+1]) in increasing order.
+ *             Always written.
+ *   col_idx   device int32[cap], or NULL to only count.
+ *   cap       capacity of col_idx in elements.
+ *   total     host int64*, receives the number of pairs (row_ptr[H*L]).
+ *
+ * Blocks until the count is known.  Returns LF_ERR_INVALID_ARG (with *total
+ * set) when col_idx is non-NULL and cap < total.  Same pattern arguments
+ * and errors as lf_attn_fwd (L % d need not be 0 here).  The enumerator
+ * uses the same key-set predicates as the attention kernel.
+ */
+LF_API lf_status lf_attn_pairs(int H, int L, int w, const int32_t* dilation, const int32_t* global_idx,
+                        int n_global, int64_t* row_ptr, int32_t* col_idx, int64_t cap,
+                        int64_t* total, lf_stream_t stream);
+
+/* Message for the last non-OK status returned in this thread ("" if none).
+ * The pointer stays valid until the thread's next lfattn call. */
+LF_API const char* lf_last_error(void);
+
+/*
+ * Synchronises `stream`, then reports LF_ERR_TIMEOUT if a device-side wait
+ * of any call on the current device ran out since the last check (and
+ * clears that record), LF_ERR_CUDA if the stream holds an error, else LF_OK.
+ */
+LF_API lf_status lf_attn_get_status(lf_stream_t stream);
+
+/* Frees every cached plan (synchronises the device). */
+LF_API void lf_plan_cache_clear(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads).  Lets callers count the kernels a region of work ran. */
+LF_API uint64_t lf_launch_count(void);
+
+/*
+ * Per-kernel device-time tracing.  While enabled, every kernel launch of the
+ * library is bracketed by two CUDA events recorded on the launch's stream.
+ * lf_profile_query synchronises on those events and returns the summed
+ * device time (ms) and number of launches of the kernels whose name
+ * contains `name` (NULL or "" = all) since the last lf_profile_reset.
+ * Kernel names: "attn_main", "gather_globals", "combine_globals",
+ * "cast_f32_bf16", "pairs_count", "pairs_scan", "pairs_fill".
+ * Tracing adds two event records per launch; it is off by default.
+ */
+LF_API void lf_profile_enable(int on);
+LF_API void lf_profile_reset(void);
+LF_API lf_status lf_profile_query(const char* name, double* total_ms, uint64_t* launches);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+LF_API int lf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LFATTN_H */

@@ -1,0 +1,726 @@
+// C ABI of the Longformer sparse attention library: argument validation,
+// per-shape plans (work lists, global-position tables), tensor-map setup and
+// the launch sequence
+//     [cast f32->bf16] -> [gather global rows] -> attention -> [combine]
+// on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/lfattn.h"
+#include "lf_attn_kernel.cuh"
+#include "lf_aux_kernels.cuh"
+#include "lf_common.cuh"
+
+namespace {
+
+using lf::MainParams;
+using lf::WorkItem;
+
+__device__ unsigned g_status_word;
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+// ---- per-kernel device-time tracing (events around each library launch)
+struct TraceRec {
+  const char* name;
+  cudaEvent_t e0, e1;
+};
+std::atomic<int> g_trace_on{0};
+std::mutex g_trace_mu;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t trace_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Runs `launch` (one kernel launch on `s`) and counts it; while tracing is
+// on, brackets it with two events recorded on the same stream.
+template <class F>
+void traced(const char* name, cudaStream_t s, F&& launch) {
+  if (g_trace_on.load(std::memory_order_relaxed)) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    TraceRec r{name, trace_event(), trace_event()};
+    cudaEventRecord(r.e0, s);
+    launch();
+    cudaEventRecord(r.e1, s);
+    g_trace.push_back(r);
+  } else {
+    launch();
+  }
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+}
+
+lf_status fail(lf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+#define LF_CUDA(call)                                                                   \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess) {                                                            \
+      if (e_ == cudaErrorMemoryAllocation)                                              \
+        return fail(LF_ERR_NOMEM, "%s: %s", #call, cudaGetErrorString(e_));             \
+      return fail(LF_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_));                \
+    }                                                                                   \
+  } while (0)
+
+// ------------------------------------------------------------ device state
+
+struct DevState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+std::mutex g_mu;
+std::vector<DevState> g_dev;
+
+unsigned long long wait_timeout_ns() {
+  static unsigned long long v = [] {
+    const char* s = std::getenv("LF_WAIT_TIMEOUT_MS");
+    double ms = s ? std::atof(s) : 4000.0;
+    if (!(ms >= 0)) ms = 4000.0;
+    return static_cast<unsigned long long>(ms * 1e6);
+  }();
+  return v;
+}
+
+lf_status get_dev(DevState** out, int* dev_out) {
+  int dev = 0;
+  LF_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+  DevState& ds = g_dev[dev];
+  if (!ds.ready) {
+    int major = 0, minor = 0;
+    LF_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    LF_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    if (major != 10 || minor != 3)
+      return fail(LF_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                  dev, major, minor);
+    LF_CUDA(cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev));
+    LF_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&ds.status), g_status_word));
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    LF_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q));
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    ds.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<64>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)lf::KCfg<64>::SMEM_BYTES));
+    LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)lf::KCfg<128>::SMEM_BYTES));
+    ds.ready = true;
+  }
+  *out = &ds;
+  *dev_out = dev;
+  return LF_OK;
+}
+
+// ------------------------------------------------------------- validation
+
+lf_status check_pattern(int H, int L, int w, const int32_t* dilation, const int32_t* gidx,
+                        int n_g) {
+  if (H < 1 || L < 1) return fail(LF_ERR_INVALID_ARG, "H=%d and L=%d must be >= 1", H, L);
+  if (w < 0) return fail(LF_ERR_INVALID_ARG, "window w=%d must be >= 0", w);
+  if (dilation == nullptr) return fail(LF_ERR_INVALID_ARG, "dilation is NULL");
+  for (int h = 0; h < H; ++h)
+    if (dilation[h] < 1) return fail(LF_ERR_INVALID_ARG, "dilation[%d]=%d < 1", h, dilation[h]);
+  if (n_g < 0 || n_g > L) return fail(LF_ERR_INVALID_ARG, "n_global=%d not in [0, L]", n_g);
+  if (n_g > 0 && gidx == nullptr) return fail(LF_ERR_INVALID_ARG, "global_idx is NULL");
+  for (int g = 0; g < n_g; ++g) {
+    if (gidx[g] < 0 || gidx[g] >= L)
+      return fail(LF_ERR_INVALID_ARG, "global_idx[%d]=%d out of [0, %d)", g, gidx[g], L);
+    if (g > 0 && gidx[g] <= gidx[g - 1])
+      return fail(LF_ERR_INVALID_ARG, "global_idx not strictly increasing at %d", g);
+  }
+  // products such as d*w and H*L must stay inside int32 arithmetic
+  for (int h = 0; h < H; ++h)
+    if ((long long)dilation[h] * w > (1LL << 30))
+      return fail(LF_ERR_UNSUPPORTED, "dilation[%d]*w too large", h);
+  if ((long long)H * L > (1LL << 31) - 2) return fail(LF_ERR_UNSUPPORTED, "H*L too large");
+  return LF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ plans
+
+struct Pattern {
+  int H = 0, L = 0, w = 0, n_g = 0;
+  std::vector<int32_t> dil, G;
+  int32_t* d_G = nullptr;
+  uint8_t* d_isg = nullptr;
+  int32_t* d_dil = nullptr;
+  std::vector<uint8_t> isg;
+};
+
+struct Plan {
+  std::shared_ptr<Pattern> pat;
+  int B = 0, D = 0;
+  int n_slots = 0;
+  int slot_dil[lf::kMaxDilSlots] = {0};
+  std::vector<int> head_slot;
+  int NGB = 16, NGQ = 0, n_gblk = 0, n_chunks = 0;
+  std::vector<WorkItem> items;
+  WorkItem* d_items = nullptr;
+};
+
+using PatKey = std::tuple<int, int, int, int, std::vector<int32_t>, std::vector<int32_t>>;
+using PlanKey = std::tuple<int, int, int, PatKey>;   // dev, B, D, pattern
+std::map<PatKey, std::shared_ptr<Pattern>> g_patterns;
+std::map<PlanKey, std::unique_ptr<Plan>> g_plans;
+
+lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const int32_t* gidx,
+                      int n_g, std::shared_ptr<Pattern>* out) {
+  PatKey key{dev, H, L, w, std::vector<int32_t>(dil, dil + H),
+             std::vector<int32_t>(gidx ? gidx : dil, gidx ? gidx + n_g : dil)};
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_patterns.find(key);
+  if (it != g_patterns.end()) {
+    *out = it->second;
+    return LF_OK;
+  }
+  auto pat = std::make_shared<Pattern>();
+  pat->H = H;
+  pat->L = L;
+  pat->w = w;
+  pat->n_g = n_g;
+  pat->dil.assign(dil, dil + H);
+  if (n_g) pat->G.assign(gidx, gidx + n_g);
+  pat->isg.assign(L, 0);
+  for (int g : pat->G) pat->isg[g] = 1;
+  LF_CUDA(cudaMalloc(&pat->d_isg, L));
+  LF_CUDA(cudaMemcpy(pat->d_isg, pat->isg.data(), L, cudaMemcpyHostToDevice));
+  LF_CUDA(cudaMalloc(&pat->d_dil, sizeof(int32_t) * H));
+  LF_CUDA(cudaMemcpy(pat->d_dil, dil, sizeof(int32_t) * H, cudaMemcpyHostToDevice));
+  LF_CUDA(cudaMalloc(&pat->d_G, sizeof(int32_t) * std::max(n_g, 1)));
+  if (n_g) LF_CUDA(cudaMemcpy(pat->d_G, gidx, sizeof(int32_t) * n_g, cudaMemcpyHostToDevice));
+  g_patterns[key] = pat;
+  *out = pat;
+  return LF_OK;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+void build_items(Plan& pl, int num_sms) {
+  const Pattern& pt = *pl.pat;
+  const int H = pt.H, L = pt.L, w = pt.w, n_g = pt.n_g;
+  (void)num_sms;
+  // global key blocks folded into every band tile
+  if (n_g > 0) {
+    pl.NGB = n_g <= lf::kBN ? ((n_g + 15) / 16) * 16 : lf::kBN;
+    pl.n_gblk = ceil_div(n_g, pl.NGB);
+    pl.NGQ = ceil_div(n_g, lf::kBM) * lf::kBM;
+  } else {
+    pl.NGB = 16;
+    pl.n_gblk = 0;
+    pl.NGQ = 0;
+  }
+  std::vector<WorkItem>& items = pl.items;
+  items.clear();
+  for (int b = 0; b < pl.B; ++b) {
+    for (int h = 0; h < H; ++h) {
+      const int bh = b * H + h;
+      const int d = pt.dil[h];
+      for (int r = 0; r < d; ++r) {
+        const int Lr = lf::residue_len(L, d, r);
+        for (int t0 = 0; t0 < Lr; t0 += lf::kBM) {
+          const int tlast = std::min(t0 + lf::kBM - 1, Lr - 1);
+          bool all_global = n_g > 0;
+          for (int t = t0; t <= tlast && all_global; ++t) all_global = pt.isg[r + d * t] != 0;
+          if (all_global) continue;
+          const int lo = std::max(t0 - w, 0);
+          const int hi = std::min(tlast + w, Lr - 1);
+          WorkItem wi;
+          wi.bh = bh;
+          wi.kind = 0;
+          wi.r = r;
+          wi.t0 = t0;
+          wi.kb0 = lo;
+          wi.nkb = ceil_div(hi - lo + 1, lf::kBN);
+          wi.ngb = pl.n_gblk;
+          wi.slot = pl.head_slot[h];
+          items.push_back(wi);
+        }
+      }
+    }
+  }
+  if (n_g > 0) {
+    const int nblocks = ceil_div(L, lf::kBN);
+    const int band_cost = std::min(nblocks, ceil_div(lf::kBM + 2 * w, lf::kBN)) + pl.n_gblk;
+    const int CB = std::max(1, std::min(nblocks, band_cost));
+    pl.n_chunks = ceil_div(nblocks, CB);
+    for (int b = 0; b < pl.B; ++b)
+      for (int h = 0; h < H; ++h)
+        for (int gt = 0; gt < pl.NGQ / lf::kBM; ++gt)
+          for (int c = 0; c < pl.n_chunks; ++c) {
+            WorkItem wi;
+            wi.bh = b * H + h;
+            wi.kind = 1;
+            wi.r = gt;
+            wi.t0 = 0;
+            wi.kb0 = c * CB * lf::kBN;
+            wi.nkb = std::min(CB, nblocks - c * CB);
+            wi.ngb = 0;
+            wi.slot = c;
+            items.push_back(wi);
+          }
+  } else {
+    pl.n_chunks = 0;
+  }
+  // longest first (stable: neighbouring tiles stay together for L2 reuse)
+  std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) {
+    return a.nkb + a.ngb > b.nkb + b.ngb;
+  });
+}
+
+lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pattern>& pat,
+                   Plan** out) {
+  PatKey pk{dev, pat->H, pat->L, pat->w, pat->dil, pat->G};
+  PlanKey key{dev, B, D, pk};
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_plans.find(key);
+  if (it != g_plans.end()) {
+    *out = it->second.get();
+    return LF_OK;
+  }
+  auto pl = std::make_unique<Plan>();
+  pl->pat = pat;
+  pl->B = B;
+  pl->D = D;
+  pl->head_slot.resize(pat->H);
+  for (int h = 0; h < pat->H; ++h) {
+    int s = 0;
+    while (s < pl->n_slots && pl->slot_dil[s] != pat->dil[h]) ++s;
+    if (s == pl->n_slots) {
+      if (pl->n_slots == lf::kMaxDilSlots)
+        return fail(LF_ERR_UNSUPPORTED, "more than %d distinct dilation values",
+                    lf::kMaxDilSlots);
+      pl->slot_dil[pl->n_slots++] = pat->dil[h];
+    }
+    pl->head_slot[h] = s;
+  }
+  build_items(*pl, num_sms);
+  if (!pl->items.empty()) {
+    LF_CUDA(cudaMalloc(&pl->d_items, sizeof(WorkItem) * pl->items.size()));
+    LF_CUDA(cudaMemcpy(pl->d_items, pl->items.data(), sizeof(WorkItem) * pl->items.size(),
+                       cudaMemcpyHostToDevice));
+  }
+  *out = pl.get();
+  g_plans[key] = std::move(pl);
+  return LF_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+lf_status encode(DevState* ds, CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = ds->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd,
+                          gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return LF_OK;
+}
+
+// 4-D residue view {D, d, L/d, BH} of a [BH, L, D] bf16 tensor
+lf_status map_residue(DevState* ds, CUtensorMap* m, const void* base, int D, int L, int d,
+                      int BH) {
+  const uint64_t dims[4] = {(uint64_t)D, (uint64_t)d, (uint64_t)(L / d), (uint64_t)BH};
+  const uint64_t st[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * d, (uint64_t)D * 2 * L};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  return encode(ds, m, base, 4, dims, st, box);
+}
+
+// 3-D view {D, rows, BH} with a box of `box_rows` rows
+lf_status map_rows(DevState* ds, CUtensorMap* m, const void* base, int D, int rows, int BH,
+                   int box_rows) {
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)rows, (uint64_t)BH};
+  const uint64_t st[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * rows};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+  return encode(ds, m, base, 3, dims, st, box);
+}
+
+// ------------------------------------------------------------------ forward
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool f32, int B, int H,
+                   int L, int D, int w, const int32_t* dilation, const int32_t* gidx, int n_g,
+                   float scale, cudaStream_t stream) {
+  t_last_error.clear();
+  if (B < 1) return fail(LF_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  if (!q || !k || !v || !out) return fail(LF_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LF_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(LF_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (D != 64 && D != 128) return fail(LF_ERR_UNSUPPORTED, "D=%d (supported: 64, 128)", D);
+  for (int h = 0; h < H; ++h)
+    if (dilation[h] > 1 && L % dilation[h] != 0)
+      return fail(LF_ERR_UNSUPPORTED, "L=%d is not a multiple of dilation[%d]=%d", L, h,
+                  dilation[h]);
+  if ((long long)B * H > (1LL << 30)) return fail(LF_ERR_UNSUPPORTED, "B*H too large");
+
+  DevState* ds = nullptr;
+  int dev = 0;
+  if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
+  std::shared_ptr<Pattern> pat;
+  if ((s = get_pattern(dev, H, L, w, dilation, gidx, n_g, &pat)) != LF_OK) return s;
+  Plan* pl = nullptr;
+  if ((s = get_plan(dev, ds->num_sms, B, D, pat, &pl)) != LF_OK) return s;
+
+  const int BH = B * H;
+  const size_t elems = (size_t)BH * L * D;
+  // scratch layout
+  size_t off = 0;
+  const size_t off_cast = off;
+  if (f32) off += align_up(3 * elems * 2, 256);
+  const size_t off_g = off;
+  const size_t g_elems = (size_t)BH * pl->NGQ * D;
+  if (n_g > 0) off += align_up(3 * g_elems * 2, 256);
+  const size_t off_po = off;
+  const size_t n_part = (size_t)BH * pl->NGQ * pl->n_chunks;
+  if (n_g > 0) off += align_up(n_part * D * 4, 256);
+  const size_t off_pm = off;
+  if (n_g > 0) off += align_up(n_part * 2 * 4, 256);
+  uint8_t* ws = nullptr;
+  if (off > 0) LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&ws), off, stream));
+
+  struct Freer {
+    uint8_t* p;
+    cudaStream_t s;
+    ~Freer() {
+      if (p) cudaFreeAsync(p, s);
+    }
+  } freer{ws, stream};
+
+  const void *qb = q, *kb = k, *vb = v;
+  if (f32) {
+    uint16_t* cq = reinterpret_cast<uint16_t*>(ws + off_cast);
+    const size_t n4 = elems / 4;
+    const int threads = 256;
+    const int blocks = (int)std::min<size_t>((n4 + threads - 1) / threads, (size_t)ds->num_sms * 8);
+    const void* src[3] = {q, k, v};
+    for (int x = 0; x < 3; ++x) {
+      traced("cast_f32_bf16", stream, [&] {
+        lf::lf_cast_f32_bf16_kernel<<<blocks, threads, 0, stream>>>(
+            reinterpret_cast<const float4*>(src[x]), reinterpret_cast<uint2*>(cq + x * elems), n4);
+      });
+    }
+    qb = cq;
+    kb = cq + elems;
+    vb = cq + 2 * elems;
+  }
+
+  MainParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  for (int sl = 0; sl < pl->n_slots; ++sl) {
+    const int d = pl->slot_dil[sl];
+    prm.dil[sl] = d;
+    if ((s = map_residue(ds, &prm.tmQ[sl], qb, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &prm.tmK[sl], kb, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &prm.tmV[sl], vb, D, L, d, BH)) != LF_OK) return s;
+  }
+  uint16_t* qg = reinterpret_cast<uint16_t*>(ws + off_g);
+  uint16_t* kg = qg + g_elems;
+  uint16_t* vg = kg + g_elems;
+  if (n_g > 0) {
+    if ((s = map_rows(ds, &prm.tmKp, kb, D, L, BH, lf::kBN)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmVp, vb, D, L, BH, lf::kBN)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmQg, qg, D, pl->NGQ, BH, lf::kBM)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmKg, kg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmVg, vg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+  }
+  prm.items = pl->d_items;
+  prm.n_items = (int)pl->items.size();
+  prm.gidx = pat->d_G;
+  prm.is_glob = pat->d_isg;
+  prm.n_g = n_g;
+  prm.NGB = pl->NGB;
+  prm.NGQ = pl->NGQ;
+  prm.n_chunks = pl->n_chunks;
+  prm.out = out;
+  prm.out_f32 = f32 ? 1 : 0;
+  prm.part_o = reinterpret_cast<float*>(ws + off_po);
+  prm.part_ml = reinterpret_cast<float*>(ws + off_pm);
+  prm.H = H;
+  prm.L = L;
+  prm.w = w;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.status = ds->status;
+  prm.timeout_ns = wait_timeout_ns();
+
+  if (n_g > 0) {
+    const size_t total = (size_t)BH * pl->NGQ * (D / 8);
+    const int threads = 256;
+    const int blocks = (int)std::max<size_t>(1, std::min<size_t>((total + threads - 1) / threads,
+                                                                 (size_t)ds->num_sms * 8));
+    traced("gather_globals", stream, [&] {
+      lf::lf_gather_globals_kernel<<<blocks, threads, 0, stream>>>(
+          reinterpret_cast<const uint4*>(qb), reinterpret_cast<const uint4*>(kb),
+          reinterpret_cast<const uint4*>(vb), reinterpret_cast<uint4*>(qg),
+          reinterpret_cast<uint4*>(kg), reinterpret_cast<uint4*>(vg), pat->d_G, n_g, pl->NGQ, L,
+          D, BH);
+    });
+  }
+  if (prm.n_items > 0) {
+    const int grid = std::min(prm.n_items, ds->num_sms);
+    traced("attn_main", stream, [&] {
+      if (D == 64)
+        lf::lf_attn_main_kernel<64><<<grid, 192, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
+      else
+        lf::lf_attn_main_kernel<128><<<grid, 192, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
+    });
+  }
+  if (n_g > 0) {
+    const int threads = 256;
+    const long long warps = (long long)BH * n_g;
+    const int blocks = (int)((warps + threads / 32 - 1) / (threads / 32));
+    traced("combine_globals", stream, [&] {
+      if (D == 64)
+        lf::lf_combine_globals_kernel<64><<<blocks, threads, 0, stream>>>(
+            prm.part_o, prm.part_ml, pat->d_G, out, prm.out_f32, n_g, pl->NGQ, pl->n_chunks, L,
+            BH);
+      else
+        lf::lf_combine_globals_kernel<128><<<blocks, threads, 0, stream>>>(
+            prm.part_o, prm.part_ml, pat->d_G, out, prm.out_f32, n_g, pl->NGQ, pl->n_chunks, L,
+            BH);
+    });
+  }
+  LF_CUDA(cudaGetLastError());
+  return LF_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+lf_status lf_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int H,
+                      int L, int D, int w, const int32_t* dilation, const int32_t* global_idx,
+                      int n_global, float scale, lf_stream_t stream) {
+  try {
+    return fwd_impl(q, k, v, out, false, B, H, L, D, w, dilation, global_idx, n_global, scale,
+                    static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, int H,
+                          int L, int D, int w, const int32_t* dilation,
+                          const int32_t* global_idx, int n_global, float scale,
+                          lf_stream_t stream) {
+  try {
+    return fwd_impl(q, k, v, out, true, B, H, L, D, w, dilation, global_idx, n_global, scale,
+                    static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, void* out, int is_f32,
+                           int B, int H, int L, int D, int w, const int32_t* dilation,
+                           const int32_t* global_idx, int n_global, float scale,
+                           lf_stream_t stream) {
+  try {
+    t_last_error.clear();
+    if (!q || !k || !v || !out) return fail(LF_ERR_INVALID_ARG, "a host pointer is NULL");
+    if (B < 1 || H < 1 || L < 1 || (D != 64 && D != 128))
+      return fail(LF_ERR_INVALID_ARG, "bad shape B=%d H=%d L=%d D=%d", B, H, L, D);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)B * H * L * D * (is_f32 ? 4 : 2);
+    uint8_t* buf = nullptr;
+    LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&buf), 4 * align_up(bytes, 256), st));
+    uint8_t* dq = buf;
+    uint8_t* dk = dq + align_up(bytes, 256);
+    uint8_t* dv = dk + align_up(bytes, 256);
+    uint8_t* dout = dv + align_up(bytes, 256);
+    cudaError_t e = cudaSuccess;
+    lf_status s = LF_OK;
+    if ((e = cudaMemcpyAsync(dq, q, bytes, cudaMemcpyHostToDevice, st)) == cudaSuccess &&
+        (e = cudaMemcpyAsync(dk, k, bytes, cudaMemcpyHostToDevice, st)) == cudaSuccess &&
+        (e = cudaMemcpyAsync(dv, v, bytes, cudaMemcpyHostToDevice, st)) == cudaSuccess) {
+      s = fwd_impl(dq, dk, dv, dout, is_f32 != 0, B, H, L, D, w, dilation, global_idx, n_global,
+                   scale, st);
+      if (s == LF_OK) e = cudaMemcpyAsync(out, dout, bytes, cudaMemcpyDeviceToHost, st);
+    }
+    cudaFreeAsync(buf, st);
+    cudaError_t e2 = cudaStreamSynchronize(st);
+    if (s != LF_OK) return s;
+    if (e != cudaSuccess) return fail(LF_ERR_CUDA, "copy failed: %s", cudaGetErrorString(e));
+    if (e2 != cudaSuccess) return fail(LF_ERR_CUDA, "stream: %s", cudaGetErrorString(e2));
+    return LF_OK;
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_pairs(int H, int L, int w, const int32_t* dilation, const int32_t* global_idx,
+                        int n_global, int64_t* row_ptr, int32_t* col_idx, int64_t cap,
+                        int64_t* total, lf_stream_t stream) {
+  try {
+    t_last_error.clear();
+    lf_status s = check_pattern(H, L, w, dilation, global_idx, n_global);
+    if (s != LF_OK) return s;
+    if (row_ptr == nullptr || total == nullptr)
+      return fail(LF_ERR_INVALID_ARG, "row_ptr and total must not be NULL");
+    if (col_idx != nullptr && cap < 0) return fail(LF_ERR_INVALID_ARG, "cap < 0");
+    DevState* ds = nullptr;
+    int dev = 0;
+    if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
+    std::shared_ptr<Pattern> pat;
+    if ((s = get_pattern(dev, H, L, w, dilation, global_idx, n_global, &pat)) != LF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long n = (long long)H * L;
+    const int threads = 256;
+    const int blocks = (int)std::min<long long>((n + threads - 1) / threads, ds->num_sms * 16LL);
+    // counts are written into row_ptr and scanned in place
+    traced("pairs_count", st, [&] {
+      lf::lf_pairs_count_kernel<<<blocks, threads, 0, st>>>(pat->d_dil, pat->d_G, pat->d_isg,
+                                                           n_global, H, L, w, row_ptr);
+    });
+    traced("pairs_scan", st, [&] { lf::lf_pairs_scan_kernel<<<1, 1024, 0, st>>>(row_ptr, row_ptr, n); });
+    LF_CUDA(cudaGetLastError());
+    int64_t tot = 0;
+    LF_CUDA(cudaMemcpyAsync(&tot, row_ptr + n, sizeof(int64_t), cudaMemcpyDeviceToHost, st));
+    LF_CUDA(cudaStreamSynchronize(st));
+    *total = tot;
+    if (col_idx == nullptr) return LF_OK;
+    if (cap < tot)
+      return fail(LF_ERR_INVALID_ARG, "col_idx capacity %lld < %lld pairs", (long long)cap,
+                  (long long)tot);
+    traced("pairs_fill", st, [&] {
+      lf::lf_pairs_fill_kernel<<<blocks, threads, 0, st>>>(pat->d_dil, pat->d_G, pat->d_isg,
+                                                          n_global, H, L, w, row_ptr, col_idx);
+    });
+    LF_CUDA(cudaGetLastError());
+    return LF_OK;
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+const char* lf_last_error(void) { return t_last_error.c_str(); }
+
+lf_status lf_attn_get_status(lf_stream_t stream) {
+  t_last_error.clear();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(LF_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+  unsigned word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word));
+  if (e != cudaSuccess) return fail(LF_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    unsigned zero = 0;
+    cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+    if (word & lf::kStatusTimeout)
+      return fail(LF_ERR_TIMEOUT, "a device-side wait ran out (status word 0x%x)", word);
+    return fail(LF_ERR_CUDA, "device status word 0x%x", word);
+  }
+  return LF_OK;
+}
+
+void lf_plan_cache_clear(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaDeviceSynchronize();
+  for (auto& kv : g_plans)
+    if (kv.second->d_items) cudaFree(kv.second->d_items);
+  g_plans.clear();
+  for (auto& kv : g_patterns) {
+    cudaFree(kv.second->d_G);
+    cudaFree(kv.second->d_isg);
+    cudaFree(kv.second->d_dil);
+  }
+  g_patterns.clear();
+}
+
+uint64_t lf_launch_count(void) { return g_launches.load(); }
+
+void lf_profile_enable(int on) { g_trace_on.store(on ? 1 : 0); }
+
+void lf_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (auto& r : g_trace) {
+    cudaEventSynchronize(r.e1);
+    g_event_pool.push_back(r.e0);
+    g_event_pool.push_back(r.e1);
+  }
+  g_trace.clear();
+}
+
+lf_status lf_profile_query(const char* name, double* total_ms, uint64_t* launches) {
+  t_last_error.clear();
+  if (total_ms == nullptr || launches == nullptr)
+    return fail(LF_ERR_INVALID_ARG, "total_ms and launches must not be NULL");
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  double ms = 0.0;
+  uint64_t n = 0;
+  for (auto& r : g_trace) {
+    if (name != nullptr && name[0] != 0 && std::strstr(r.name, name) == nullptr) continue;
+    cudaError_t e = cudaEventSynchronize(r.e1);
+    if (e != cudaSuccess) return fail(LF_ERR_CUDA, "event: %s", cudaGetErrorString(e));
+    float x = 0.f;
+    e = cudaEventElapsedTime(&x, r.e0, r.e1);
+    if (e != cudaSuccess) return fail(LF_ERR_CUDA, "elapsed: %s", cudaGetErrorString(e));
+    ms += x;
+    ++n;
+  }
+  *total_ms = ms;
+  *launches = n;
+  return LF_OK;
+}
+
+int lf_version(void) { return 100; }
+
+}  // extern "C"
