@@ -1,0 +1,421 @@
+"""Benchmark of the Longformer sparse attention forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config base]
+
+One step = one call of the whole forward (lf_attn_fwd: gather of global rows,
+the band + global attention kernel, the global-row combine) on one batch of
+the workload.  The default workload is "base" (B=2, H=12, L=4096, D=64,
+one-sided window 256, no dilation, one global token at 0), the L=4096
+configuration the headline metric is quoted on.  Inputs are seeded
+synthetic N(0,1) values rounded to bf16 (see workloads.py).
+
+Timing: W untimed warm-up steps; then K steps, each preceded by an L2 flush
+(a 256 MiB device memset outside the timed events), each timed with CUDA
+events on the launching stream; barrier + synchronize on both sides; the
+maximum over ranks.  Under torchrun every rank runs its own replica of the
+workload on its own GPU (the problem shards into independent (b, h) heads,
+so there is no exchange on the data path): scaling is weak.
+
+Metric: useful TFLOP/s = 4 * B * H * D * (attended pairs) / time, the pairs
+counted by the library's own key-list enumerator (lf_attn_pairs).
+
+--impl reference times the fp64 CPU oracle (the plain dense-masked
+definition) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from long_sequence_sparse_lf_b300 import workloads as W  # noqa: E402
+
+METRIC = "banded+global attention fwd useful TFLOP/s & % of BF16 tensor peak (1 B300)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["lf_attn_kernel.cuh", "lf_ptx.cuh", "lf_common.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "long_sequence_sparse_lf_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of attn_main from a committed ncu summary, if it
+    was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"attn_main_{workload}_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    return d.get("traffic_bytes_per_launch")
+
+
+def useful_work(wl, pairs_all_heads: int):
+    """pairs_all_heads: attended pairs summed over the H heads of one batch
+    element (the pattern does not depend on b)."""
+    flops = 4 * wl.B * wl.D * pairs_all_heads
+    elt = 2  # bf16
+    compulsory = 4 * wl.B * wl.H * wl.L * wl.D * elt   # q, k, v read + out write
+    return flops, compulsory
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        loaded = [r for r in rows if num(r[4]) >= 50] or rows
+        sm = [num(r[1]) for r in loaded if not math.isnan(num(r[1]))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(num(r[2]) for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, q, k, v, budget_s: float, max_heads=None):
+    """Runs the oracle over whole (b, h) heads until the time budget is spent.
+    Returns (seconds, useful flops of the heads done, heads done, threads)."""
+    from oracle import lf_oracle as O
+    qf = q.to(torch.bfloat16).double().numpy()
+    kf = k.to(torch.bfloat16).double().numpy()
+    vf = v.to(torch.bfloat16).double().numpy()
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    if max_heads is not None:
+        heads = heads[:max_heads]
+    done, flops = 0, 0
+    t0 = time.perf_counter()
+    for (b, h) in heads:
+        O.attention(qf[b:b + 1, h:h + 1], kf[b:b + 1, h:h + 1], vf[b:b + 1, h:h + 1],
+                    wl.w, [wl.dilation[h]], wl.global_idx, wl.scale)
+        done += 1
+        flops += 4 * wl.D * O.pair_count(wl.L, wl.w, wl.dilation[h], wl.global_idx)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return time.perf_counter() - t0, flops, done
+
+
+def oracle_rows_step(wl, qf, kf, vf, rows, b, h):
+    from oracle import lf_oracle as O
+    O.attention(qf[b:b + 1, h:h + 1], kf[b:b + 1, h:h + 1], vf[b:b + 1, h:h + 1], wl.w,
+                [wl.dilation[h]], wl.global_idx, wl.scale, rows=rows)
+    pairs = 0
+    for i in rows:
+        pairs += len(O.key_set(int(i), wl.L, wl.w, wl.dilation[h], wl.global_idx))
+    return 4 * wl.D * pairs
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ arms
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, wl):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = W.make_qkv(wl)
+    qf = q.to(torch.bfloat16).double().numpy()
+    kf = k.to(torch.bfloat16).double().numpy()
+    vf = v.to(torch.bfloat16).double().numpy()
+    # size one step so that all steps end within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    t0 = time.perf_counter()
+    oracle_rows_step(wl, qf, kf, vf, list(range(64)), 0, 0)
+    per_row = (time.perf_counter() - t0) / 64
+    n_rows = int(max(16, min(wl.L, budget / max(per_row, 1e-9))))
+    rng = np.random.default_rng(0)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+
+    def one_step(s):
+        b, h = heads[s % len(heads)]
+        r0 = int(rng.integers(0, max(1, wl.L - n_rows + 1)))
+        return oracle_rows_step(wl, qf, kf, vf, list(range(r0, r0 + n_rows)), b, h)
+
+    for s in range(args.warmup):
+        one_step(s)
+    t0 = time.perf_counter()
+    flops = 0
+    for s in range(args.steps):
+        flops += one_step(s)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"fp64 dense-masked oracle, {args.steps} steps of {n_rows} consecutive query rows "
+              f"of one (b,h) head each (heads in turn) of the {wl.name} workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.describe(), parallelism="host cores"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    import long_sequence_sparse_lf_b300 as lf
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    lf.load_library()
+
+    q, k, v = W.make_qkv(wl)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # attended pairs from the library's enumerator (one count, not timed)
+    _, _, pairs = lf.lf_attn_pairs(wl.H, wl.L, wl.w, wl.dilation, wl.global_idx,
+                                   count_only=True, device=dev)
+    flops, comp_bytes = useful_work(wl, pairs)
+
+    def step():
+        lf.lf_attn_fwd(qd, kd, vd, out, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if lf.lf_attn_get_status(stream) != 0:
+        raise SystemExit("device status error after warm-up: " + lf.lf_last_error())
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    lf.lf_profile_reset()
+    lf.lf_profile_enable(True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    launches0 = lf.lf_launch_count()
+    for s in range(args.steps):
+        flush.zero_()
+        evs[s][0].record(stream)
+        step()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = lf.lf_launch_count() - launches0
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop() if sampler else None
+    lf.lf_profile_enable(False)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = float(sum(step_ms))
+    main_ms, main_n = lf.lf_profile_query("attn_main")
+    lf.lf_profile_reset()
+    if lf.lf_attn_get_status(stream) != 0:
+        raise SystemExit("device status error in timed region: " + lf.lf_last_error())
+    if pg:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    n_units = ws * args.steps
+    value = flops * n_units / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end through the host-buffer entry point (pinned memory)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    qh, kh, vh = (t.contiguous().pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lf.lf_attn_fwd_host(qh, kh, vh, oh, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        lf.lf_attn_fwd_host(qh, kh, vh, oh, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+    e2e_s = time.perf_counter() - t0
+    if pg:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = flops * ws * e2e_steps / e2e_s / 1e12
+    io_bytes = qh.numel() * qh.element_size()
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (attn_main)
+    peaks, peak_src = load_peaks()
+    main_avg_s = main_ms / max(main_n, 1) * 1e-3
+    ai = flops / comp_bytes
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_achieved = flops / main_avg_s / 1e12
+    hbm_achieved = comp_bytes / main_avg_s / 1e9
+    traffic = recorded_traffic(wl.name)
+    if ai < ridge:
+        roof = {"bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": hbm_achieved / peaks["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tensor_achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": tensor_achieved / peaks["bf16_tflops"]}
+    roof.update({"traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+                 if peak_src == "measured" else "fallback",
+                 "kernel": "attn_main", "kernel_ms": main_avg_s * 1e3,
+                 "algorithmic_bytes": comp_bytes, "useful_flops": flops,
+                 "arithmetic_intensity": ai, "ridge": ridge,
+                 "tensor_achieved_tflops": tensor_achieved,
+                 "tensor_frac": tensor_achieved / peaks["bf16_tflops"]})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": dict(wl.describe(), parallelism=f"replica x{ws}",
+                       l2="flushed between timed steps (256 MiB memset)",
+                       pairs=pairs * wl.B),
+        "peak_frac_bf16": value / peaks["bf16_tflops"],
+        "roofline": roof,
+        "gpu_launches": launches,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 3 * io_bytes,
+                "d2h_bytes_per_step": io_bytes, "steps": e2e_steps,
+                "api": "lf_attn_fwd_host (pinned host buffers)"},
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        secs, cflops, heads = oracle_sample(wl, q, k, v, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": cflops / secs / 1e12, "unit": UNIT, "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 dense-masked oracle over {heads} whole (b,h) heads of the "
+                      f"{wl.name} workload (time-bounded to ~{args.cpu_budget:.0f} s)"}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="base", choices=W.CONFIG_ORDER)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    wl = W.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,8 +1,13 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
 
-Tolerance (for every output comparison): max |gpu - oracle| <= 1e-2 and
-||gpu - oracle||_2 / ||oracle||_2 <= 5e-3, compared in float64 on the same
-bf16-rounded inputs.  Key lists are compared bit-exactly.
+Tolerance (for every output comparison), in float64 on the same
+bf16-rounded inputs:
+  * max |gpu - oracle| <= 1e-2 beyond the output format's own rounding:
+    a bf16 output cannot be closer to the exact value than half a bf16 ulp
+    (2^-8 relative), so each element may differ by 1e-2 + 2^-8 * |oracle|
+    (fp32 outputs get no allowance);
+  * ||gpu - oracle||_2 / ||oracle||_2 <= 5e-3.
+Key lists are compared bit-exactly.
 """
 import math
 
@@ -29,14 +34,19 @@ def lf():
     return lf
 
 
-def _errors(got, ref):
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def _errors(got, ref, out_bf16=True):
     d = np.abs(got - ref)
+    if out_bf16:
+        d = d - BF16_HALF_ULP * np.abs(ref)
     rel = float(np.linalg.norm((got - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))
     return float(d.max()), rel
 
 
-def _assert_close(got, ref, what=""):
-    mx, rel = _errors(got, ref)
+def _assert_close(got, ref, what="", out_bf16=True):
+    mx, rel = _errors(got, ref, out_bf16)
     assert mx <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs={mx:.3e} rel_l2={rel:.3e}"
     return mx, rel
 
@@ -65,7 +75,7 @@ def test_tiny_config_full_parity(lf):
     q, k, v = W.make_qkv(wl)
     got = _run(lf, q, k, v, wl.w, wl.dilation, wl.global_idx, wl.scale)
     ref = O.attention(_f64(q), _f64(k), _f64(v), wl.w, wl.dilation, wl.global_idx, wl.scale)
-    _assert_close(got, ref, "tiny")
+    _assert_close(got, ref, "tiny", out_bf16=False)
 
 
 # ------------------------------------------------ closed-form special cases
@@ -129,14 +139,14 @@ def test_random_shapes_parity(lf, shape):
     _assert_close(got, ref, str(shape[:5]))
 
 
-def test_fp32_path_matches_bf16_path_inputs(lf):
+def test_fp32_path_matches_oracle_on_rounded_inputs(lf):
     """fp32 inputs are rounded to bf16 first, so they match the oracle on the
     rounded values (fp32 output, no final rounding)."""
     B, H, L, D, w = 1, 2, 500, 64, 30
     q, k, v = _inputs((B, H, L, D), 11, dtype=torch.float32)
-    got = _run(lf, q, k, v, w, [1, 2] if L % 2 == 0 else [1, 1], (0, 1), 0.125)
+    got = _run(lf, q, k, v, w, [1, 2], (0, 1), 0.125)
     ref = O.attention(_f64(q), _f64(k), _f64(v), w, [1, 2], (0, 1), 0.125)
-    _assert_close(got, ref, "fp32 path")
+    _assert_close(got, ref, "fp32 path", out_bf16=False)
 
 
 def test_repeat_calls_are_deterministic(lf):
