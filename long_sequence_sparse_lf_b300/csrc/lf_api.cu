@@ -138,6 +138,17 @@ lf_status get_dev(DevState** out, int* dev_out) {
     if (q != cudaDriverEntryPointSuccess || fn == nullptr)
       return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
     ds.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    // The attention kernel hands registers between its warpgroups
+    // (setmaxnreg); the split assumes the launch allocation kRegsLaunch.
+    for (const void* fn : {reinterpret_cast<const void*>(lf::lf_attn_main_kernel<64>),
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128>)}) {
+      cudaFuncAttributes fa;
+      LF_CUDA(cudaFuncGetAttributes(&fa, fn));
+      if (fa.numRegs != (int)lf::kRegsLaunch)
+        return fail(LF_ERR_UNSUPPORTED,
+                    "attention kernel built with %d registers per thread, expected %u",
+                    fa.numRegs, lf::kRegsLaunch);
+    }
     LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<64>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)lf::KCfg<64>::SMEM_BYTES));
@@ -170,9 +181,10 @@ lf_status check_pattern(int H, int L, int w, const int32_t* dilation, const int3
   }
   // products such as d*w and H*L must stay inside int32 arithmetic
   for (int h = 0; h < H; ++h)
-    if ((long long)dilation[h] * w > (1LL << 30))
+    if ((long long)dilation[h] * w > (1LL << 28))
       return fail(LF_ERR_UNSUPPORTED, "dilation[%d]*w too large", h);
   if ((long long)H * L > (1LL << 31) - 2) return fail(LF_ERR_UNSUPPORTED, "H*L too large");
+  if (L > (1 << 28)) return fail(LF_ERR_UNSUPPORTED, "L=%d too large", L);
   return LF_OK;
 }
 
@@ -237,6 +249,9 @@ lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const in
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Work list of the attention kernel (see WorkItem): band pairs of
+// neighbouring 128-query tiles per (b, h, residue class), then the
+// global-row chunks; longest first.
 void build_items(Plan& pl, int num_sms) {
   const Pattern& pt = *pl.pat;
   const int H = pt.H, L = pt.L, w = pt.w, n_g = pt.n_g;
@@ -253,43 +268,68 @@ void build_items(Plan& pl, int num_sms) {
   }
   std::vector<WorkItem>& items = pl.items;
   items.clear();
+  int pair_cost = 0;
   for (int b = 0; b < pl.B; ++b) {
     for (int h = 0; h < H; ++h) {
       const int bh = b * H + h;
       const int d = pt.dil[h];
       for (int r = 0; r < d; ++r) {
         const int Lr = lf::residue_len(L, d, r);
-        for (int t0 = 0; t0 < Lr; t0 += lf::kBM) {
-          const int tlast = std::min(t0 + lf::kBM - 1, Lr - 1);
-          bool all_global = n_g > 0;
-          for (int t = t0; t <= tlast && all_global; ++t) all_global = pt.isg[r + d * t] != 0;
-          if (all_global) continue;
-          const int lo = std::max(t0 - w, 0);
-          const int hi = std::min(tlast + w, Lr - 1);
-          WorkItem wi;
+        for (int t0 = 0; t0 < Lr; t0 += 2 * lf::kBM) {
+          // key range [lo, hi] (residue space) of each slot; absent slots have lo > hi
+          int lo[2], hi[2];
+          bool present[2];
+          for (int X = 0; X < 2; ++X) {
+            const int ta = t0 + X * lf::kBM;
+            const int tb = std::min(ta + lf::kBM - 1, Lr - 1);
+            present[X] = ta < Lr;
+            if (present[X] && n_g > 0) {
+              bool all_global = true;
+              for (int t = ta; t <= tb && all_global; ++t) all_global = pt.isg[r + d * t] != 0;
+              present[X] = !all_global;
+            }
+            lo[X] = std::max(ta - w, 0);
+            hi[X] = std::min(tb + w, Lr - 1);
+          }
+          if (!present[0] && !present[1]) continue;
+          const int plo = present[0] ? lo[0] : lo[1];
+          const int phi = present[1] ? hi[1] : hi[0];
+          WorkItem wi{};
           wi.bh = bh;
           wi.kind = 0;
           wi.r = r;
           wi.t0 = t0;
-          wi.kb0 = lo;
-          wi.nkb = ceil_div(hi - lo + 1, lf::kBN);
+          wi.kb0 = plo;
+          wi.nkb = ceil_div(phi - plo + 1, lf::kBN);
           wi.ngb = pl.n_gblk;
           wi.slot = pl.head_slot[h];
+          for (int X = 0; X < 2; ++X) {
+            if (present[X]) {
+              wi.jlo[X] = (lo[X] - plo) / lf::kBN;
+              wi.jhi[X] = (hi[X] - plo) / lf::kBN;
+            } else {
+              wi.jlo[X] = 1;
+              wi.jhi[X] = 0;
+            }
+          }
+          pair_cost = std::max(pair_cost, lf::blk_count(wi, 0) + lf::blk_count(wi, 1));
           items.push_back(wi);
         }
       }
     }
   }
   if (n_g > 0) {
+    // chunks of CB key blocks, about one band pair's worth of blocks each
     const int nblocks = ceil_div(L, lf::kBN);
-    const int band_cost = std::min(nblocks, ceil_div(lf::kBM + 2 * w, lf::kBN)) + pl.n_gblk;
-    const int CB = std::max(1, std::min(nblocks, band_cost));
-    pl.n_chunks = ceil_div(nblocks, CB);
+    int CB = std::max(2, std::min(nblocks, pair_cost > 0 ? pair_cost : nblocks));
+    const int n_items1 = ceil_div(nblocks, CB);
+    CB = ceil_div(nblocks, n_items1);   // even out the chunks
+    pl.n_chunks = 2 * n_items1;
     for (int b = 0; b < pl.B; ++b)
       for (int h = 0; h < H; ++h)
         for (int gt = 0; gt < pl.NGQ / lf::kBM; ++gt)
-          for (int c = 0; c < pl.n_chunks; ++c) {
-            WorkItem wi;
+          for (int c = 0; c < n_items1; ++c) {
+            WorkItem wi{};
             wi.bh = b * H + h;
             wi.kind = 1;
             wi.r = gt;
@@ -298,6 +338,8 @@ void build_items(Plan& pl, int num_sms) {
             wi.nkb = std::min(CB, nblocks - c * CB);
             wi.ngb = 0;
             wi.slot = c;
+            wi.jlo[0] = wi.jlo[1] = 0;
+            wi.jhi[0] = wi.jhi[1] = -1;
             items.push_back(wi);
           }
   } else {
@@ -305,8 +347,19 @@ void build_items(Plan& pl, int num_sms) {
   }
   // longest first (stable: neighbouring tiles stay together for L2 reuse)
   std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) {
-    return a.nkb + a.ngb > b.nkb + b.ngb;
+    return lf::blk_count(a, 0) + lf::blk_count(a, 1) > lf::blk_count(b, 0) + lf::blk_count(b, 1);
   });
+}
+
+// Every block of an item must have a user: the kernel releases a K/V stage
+// after its users' products (checked once per plan).
+bool items_consistent(const Plan& pl) {
+  for (const WorkItem& wi : pl.items) {
+    for (int j = 0; j < wi.nkb + wi.ngb; ++j)
+      if (!lf::blk_uses(wi, 0, j) && !lf::blk_uses(wi, 1, j)) return false;
+    if (wi.nkb < 1) return false;
+  }
+  return true;
 }
 
 lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pattern>& pat,
@@ -336,6 +389,7 @@ lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pat
     pl->head_slot[h] = s;
   }
   build_items(*pl, num_sms);
+  if (!items_consistent(*pl)) return fail(LF_ERR_INVALID_ARG, "internal: inconsistent work list");
   if (!pl->items.empty()) {
     LF_CUDA(cudaMalloc(&pl->d_items, sizeof(WorkItem) * pl->items.size()));
     LF_CUDA(cudaMemcpy(pl->d_items, pl->items.data(), sizeof(WorkItem) * pl->items.size(),
@@ -513,9 +567,9 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
     const int grid = std::min(prm.n_items, ds->num_sms);
     traced("attn_main", stream, [&] {
       if (D == 64)
-        lf::lf_attn_main_kernel<64><<<grid, 192, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
+        lf::lf_attn_main_kernel<64><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
       else
-        lf::lf_attn_main_kernel<128><<<grid, 192, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
+        lf::lf_attn_main_kernel<128><<<grid, lf::KCfg<128>::THREADS, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
     });
   }
   if (n_g > 0) {

@@ -1,29 +1,51 @@
 // Persistent band + global attention kernel (forward) for sm_103a.
 //
-// What one CTA does, per work item (see WorkItem):
-//   * band tile (kind 0): 128 consecutive queries of one residue class of a
-//     head (all of a head when d = 1).  It visits only the key blocks the
-//     tile's windows touch (block-sparse realisation of the sliding window:
-//     "Block-Sparse Attention Longformer", §2-3), masks the window edges and
-//     the sequence ends inside the boundary blocks, then folds in the
-//     gathered global keys as extra blocks, masking globals already in the
-//     row's window (the union of Longformer explained §2's patterns under one
-//     softmax, §4).  Rows of global tokens are computed but not stored.
-//   * global-row tile (kind 1): up to 128 gathered global queries of a head
-//     against one chunk of all L keys (Longformer explained §2, global
-//     attention); writes un-normalised partials (O, m, l) that a combine
-//     kernel merges.
+// Each CTA owns one SM and walks its share of the work list.  A work item
+// (see WorkItem) carries two 128-row query tiles, "slots" 0 and 1, that run
+// side by side over one shared stream of 128-key blocks:
+//   * band pair (kind 0): two neighbouring query tiles of one residue class
+//     of a head.  The stream holds only the key blocks their windows touch
+//     (the block-sparse realisation of the sliding window: "Block-Sparse
+//     Attention Longformer", §2-3), each tile using the contiguous run it
+//     needs, then the gathered global keys as extra blocks (the union of
+//     Longformer explained §2's patterns under one softmax, §4).  Window
+//     edges and sequence ends are masked inside the boundary blocks; globals
+//     already inside a row's window are masked in the gathered block.  Rows
+//     of global tokens are computed but not stored.
+//   * global rows (kind 1): the gathered global queries of a head against
+//     one chunk of all L keys (Longformer explained §2, global attention),
+//     the two slots taking alternate blocks; each slot writes un-normalised
+//     partials (O, m, l) that the combine kernel merges.
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: Q tile, then K/V blocks into a ring of stages
-//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma):
-//               S = Q K^T into TMEM, then O += P V with P read from TMEM
-//   warps 2..5  softmax + epilogue; thread = query row = TMEM lane
+// Roles (384 threads = three warpgroups, one CTA per SM):
+//   warps 0..3  softmax + epilogue of slot 0 (thread = query row = TMEM lane)
+//   warps 4..7  softmax + epilogue of slot 1
+//   warp 8      TMA producer: Q tiles of both slots, then the K/V blocks into
+//               a ring of shared-memory stages
+//   warp 9      TMEM owner and single-thread MMA issuer (tcgen05.mma):
+//               S_X = Q_X K^T into TMEM, then O_X += P_X V with P_X read from
+//               TMEM, interleaving the two slots
+//   warps 10-11 idle
+// While one slot's softmax warps exponentiate, the tensor core works on the
+// other slot, and each SM sub-partition holds one softmax warp of each slot.
+// The launch gives every thread kRegsLaunch registers; the third warpgroup
+// hands most of its share to the two softmax warpgroups (setmaxnreg), which
+// hold a whole 128-score row each.
 //
-// Softmax is the online form with fp32 running max m (in log2 units) and sum
-// l per row.  O is only rescaled when the max grows by more than 2^8, since
-// any common reference point gives the same O/l; this keeps the rescale (a
-// TMEM round trip) off the common path.
+// TMEM (512 columns): S_0, S_1 (128 fp32 columns each), P_0, P_1 (bf16 pairs,
+// 64 columns each; for D = 128 they alias the first half of S_X, written
+// only after S_X has been read, and the MMA warp issues S_X(next) after
+// PV_X(prev), so the in-order tensor pipe never overwrites a live P), O_0,
+// O_1 (D columns each).
+//
+// Softmax is the online form with fp32 running max m (log2 units) and sum l
+// per row.  O is only rescaled when the max grows by more than 2^8: any
+// common reference point gives the same O / l, and this keeps the rescale (a
+// TMEM round trip) off the common path.  Warps find, per 16-key chunk of a
+// block, whether all of their 32 rows see the chunk fully, not at all, or in
+// part: chunks no row sees are skipped (P = 0), and only partial chunks are
+// masked element by element.  A fixed share of the exponentials runs on the
+// FMA pipe (exp2_poly2) to relieve the special-function unit.
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // kStatusTimeout in the device status word, all roles leave their loops,
@@ -34,9 +56,25 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <type_traits>
 
 #include "lf_common.cuh"
 #include "lf_ptx.cuh"
+
+#ifndef LF_EMU16_D64
+#define LF_EMU16_D64 0     // exponentials per 16 columns done on the FMA pipe (D = 64)
+#endif
+#ifndef LF_REGS_SM64
+#define LF_REGS_SM64 216   // register split, softmax / other warpgroups (D = 64)
+#define LF_REGS_OT64 72
+#endif
+#ifndef LF_REGS_SM128
+#define LF_REGS_SM128 200  // (D = 128)
+#define LF_REGS_OT128 104
+#endif
+#ifndef LF_EMU16_D128
+#define LF_EMU16_D128 0    // (D = 128)
+#endif
 
 namespace lf {
 
@@ -46,14 +84,41 @@ struct KCfg {
   static constexpr uint32_t HALF = 128u * 128u;     // one [128 rows][64] bf16 atom column
   static constexpr uint32_t QB = NH * HALF;         // Q tile bytes
   static constexpr uint32_t KVB = NH * HALF;        // K (or V) block bytes
-  static constexpr int NQ = 2;                      // Q tile buffers
+  static constexpr int NQ = (D == 64) ? 2 : 1;      // Q buffers per slot
   static constexpr int NST = (D == 64) ? 4 : 2;     // K/V stages
-  // TMEM columns (512 allocated): two S buffers, two P buffers, O.
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_P0 = 256, TM_P1 = 320, TM_O = 384;
-  static constexpr int NBAR = 2 * NQ + 2 * NST + 2 + 2 + 2 + 2 + 1 + 1;
-  static constexpr uint32_t TILE_BYTES = NQ * QB + 2u * NST * KVB;
+  static constexpr bool P_ALIAS = (D != 64);        // P_X lives in S_X's columns
+  static constexpr int EMU16 = (D == 64) ? LF_EMU16_D64 : LF_EMU16_D128;
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
+  static constexpr uint32_t TM_P0 = P_ALIAS ? 0 : 256, TM_P1 = P_ALIAS ? 128 : 320;
+  static constexpr uint32_t TM_O0 = P_ALIAS ? 256 : 384, TM_O1 = P_ALIAS ? 384 : 448;
+  // barrier index map
+  static constexpr int B_QF = 0;                    // [X * NQ + b] Q buffer full
+  static constexpr int B_QE = B_QF + 2 * NQ;        // [X * NQ + b] Q buffer free
+  static constexpr int B_KF = B_QE + 2 * NQ;        // [stage] K/V full
+  static constexpr int B_KE = B_KF + NST;           // [stage] K/V free
+  static constexpr int B_SF = B_KE + NST;           // [X] S_X written
+  static constexpr int B_SR = B_SF + 2;             // [X] S_X read (free)
+  static constexpr int B_PF = B_SR + 2;             // [X] P_X written
+  static constexpr int B_PV = B_PF + 2;             // [X] O_X += P_X V done
+  static constexpr int B_OE = B_PV + 2;             // [X] O_X read by the epilogue
+  static constexpr int B_DR = B_OE + 2;             // drain
+  static constexpr int NBAR = B_DR + 1;
+  static constexpr uint32_t TILE_BYTES = 2u * NQ * QB + 2u * NST * KVB;
   static constexpr uint32_t SMEM_BYTES = TILE_BYTES + NBAR * 8 + 64 + 1024;
+  static constexpr int THREADS = 384;
+  // per-thread registers of the softmax warpgroups / the third warpgroup
+  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? LF_REGS_SM64 : LF_REGS_SM128;
+  static constexpr uint32_t REGS_OTHER = (D == 64) ? LF_REGS_OT64 : LF_REGS_OT128;
 };
+
+// Register split (per thread): at launch, after the hand-over.  The launch
+// pool is THREADS * kRegsLaunch; the split must not exceed it (the host
+// checks the kernel's launch register count against kRegsLaunch).
+constexpr uint32_t kRegsLaunch = 168;
+static_assert(8 * KCfg<64>::REGS_SOFTMAX + 4 * KCfg<64>::REGS_OTHER <= 12 * kRegsLaunch,
+              "register split (D = 64)");
+static_assert(8 * KCfg<128>::REGS_SOFTMAX + 4 * KCfg<128>::REGS_OTHER <= 12 * kRegsLaunch,
+              "register split (D = 128)");
 
 struct Waiter {
   volatile int* abort;
@@ -61,7 +126,7 @@ struct Waiter {
   unsigned long long timeout_ns;
 };
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
                                        bool honour_abort) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -82,22 +147,53 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const Waite
   return wait_slow(bar, parity, w, true);
 }
 
+// Issue state of one tile slot in the MMA warp: its position in the CTA's
+// item list and block stream, counters of issued products, and the (at most
+// two) blocks whose O += P V is still to be issued, oldest first.  A pending
+// word packs: bits 0-2 stage, 3-6 keys/16, 7 first block of the item (O is
+// overwritten), 8 block shared with the other slot, 9 parity of the item's
+// predecessor, 10 the slot had a previous item (whose O must be read first).
+struct MmaSlot {
+  int it;          // current item (index into the work list)
+  uint32_t base;   // stream position of block 0 of the current item
+  int nbt;         // blocks of the current item
+  int kind, nkb, ngb, jlo, jhi;   // the item as this slot sees it
+  int olo, ohi;    // the other slot's band range in the item
+  int j;           // next block for S (-1: the slot is done)
+  int seen, cnt;   // blocks issued / used in the current item
+  uint32_t kS, kP; // S and PV products issued
+  uint32_t qn;     // Q buffers consumed
+  uint32_t items;  // items started
+  int lastpv;      // stream position of the last PV issued
+  int npend;       // pending PVs (0..2)
+  uint32_t pw0, pw1;
+  int pn0, pn1;    // their stream positions
+  __device__ __forceinline__ void init(int first_item) {
+    it = first_item;
+    base = 0;
+    nbt = 0;
+    j = -1;
+    seen = cnt = 0;
+    kS = kP = qn = items = 0;
+    lastpv = -1;
+    npend = 0;
+    pw0 = pw1 = 0;
+    pn0 = pn1 = 0;
+  }
+};
+
 template <int D>
-__global__ void __launch_bounds__(192, 1) lf_attn_main_kernel(const __grid_constant__ MainParams p) {
+__global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_constant__ MainParams p) {
   using C = KCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK = sQ + C::NQ * C::QB;
-  const uint32_t sV = sK + C::NST * C::KVB;
+  const uint32_t sQ = smem_u32(smem);                 // [X][NQ] Q tiles
+  const uint32_t sK = sQ + 2 * C::NQ * C::QB;         // [NST] K blocks
+  const uint32_t sV = sK + C::NST * C::KVB;           // [NST] V blocks
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE_BYTES);
   const uint32_t b0 = smem_u32(bars);
   auto BAR = [&](int idx) -> uint32_t { return b0 + 8u * idx; };
-  // barrier index map
-  const int iQF = 0, iQE = C::NQ, iKF = 2 * C::NQ, iKE = 2 * C::NQ + C::NST;
-  const int iSF = 2 * C::NQ + 2 * C::NST, iSR = iSF + 2, iPF = iSR + 2, iPV = iPF + 2;
-  const int iOF = iPV + 2, iDR = iOF + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::TILE_BYTES + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -105,26 +201,26 @@ __global__ void __launch_bounds__(192, 1) lf_attn_main_kernel(const __grid_const
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int q = 0; q < C::NQ; ++q) {
-      mbar_init(BAR(iQF + q), 1);
-      mbar_init(BAR(iQE + q), 1);
+    for (int q = 0; q < 2 * C::NQ; ++q) {
+      mbar_init(BAR(C::B_QF + q), 1);
+      mbar_init(BAR(C::B_QE + q), 1);
     }
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(BAR(iKF + s), 1);
-      mbar_init(BAR(iKE + s), 1);
+      mbar_init(BAR(C::B_KF + s), 1);
+      mbar_init(BAR(C::B_KE + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(BAR(iSF + b), 1);
-      mbar_init(BAR(iSR + b), 128);
-      mbar_init(BAR(iPF + b), 128);
-      mbar_init(BAR(iPV + b), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(BAR(C::B_SF + x), 1);
+      mbar_init(BAR(C::B_SR + x), 128);
+      mbar_init(BAR(C::B_PF + x), 128);
+      mbar_init(BAR(C::B_PV + x), 1);
+      mbar_init(BAR(C::B_OE + x), 128);
     }
-    mbar_init(BAR(iOF), 128);
-    mbar_init(BAR(iDR), 1);
+    mbar_init(BAR(C::B_DR), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     for (int s = 0; s < kMaxDilSlots; ++s) {
       if (p.dil[s] > 0) {
         tma_prefetch_desc(&p.tmQ[s]);
@@ -140,7 +236,7 @@ __global__ void __launch_bounds__(192, 1) lf_attn_main_kernel(const __grid_const
       tma_prefetch_desc(&p.tmVp);
     }
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -151,352 +247,579 @@ __global__ void __launch_bounds__(192, 1) lf_attn_main_kernel(const __grid_const
 
   Waiter W{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == 0) {
+  if (warp >= 8) {
+    regs_dec<C::REGS_OTHER>();
+    if (warp == 8 && lane == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t nb = 0;   // K/V loads armed
-      uint32_t nq = 0;   // Q loads armed
+    {
+      uint32_t nb = 0;                 // K/V blocks armed
+      uint32_t qn[2] = {0u, 0u};       // Q loads armed per slot
       bool ok = true;
       for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
         const WorkItem wi = p.items[it];
-        const int qb = nq % C::NQ;
-        const uint32_t qu = nq / C::NQ;
-        if (qu > 0 && !bwait(BAR(iQE + qb), (qu - 1) & 1, W)) { ok = false; break; }
-        mbar_arrive_expect_tx(BAR(iQF + qb), C::QB);
-        const uint32_t qdst = sQ + qb * C::QB;
 #pragma unroll
-        for (int hh = 0; hh < C::NH; ++hh) {
-          if (wi.kind == 0)
-            tma_load_4d(qdst + hh * C::HALF, &p.tmQ[wi.slot], BAR(iQF + qb), 64 * hh, wi.r, wi.t0,
-                        wi.bh);
-          else
-            tma_load_3d(qdst + hh * C::HALF, &p.tmQg, BAR(iQF + qb), 64 * hh, wi.r * kBM, wi.bh);
+        for (int X = 0; X < 2; ++X) {
+          if (!ok || blk_count(wi, X) == 0) continue;
+          const int qb = qn[X] % C::NQ;
+          const uint32_t qu = qn[X] / C::NQ;
+          const int bi = X * C::NQ + qb;
+          if (qu > 0 && !bwait(BAR(C::B_QE + bi), (qu - 1) & 1, W)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(C::B_QF + bi), C::QB);
+          const uint32_t qdst = sQ + bi * C::QB;
+#pragma unroll
+          for (int hh = 0; hh < C::NH; ++hh) {
+            if (wi.kind == 0)
+              tma_load_4d(qdst + hh * C::HALF, &p.tmQ[wi.slot], BAR(C::B_QF + bi), 64 * hh, wi.r,
+                          wi.t0 + kBM * X, wi.bh);
+            else
+              tma_load_3d(qdst + hh * C::HALF, &p.tmQg, BAR(C::B_QF + bi), 64 * hh, wi.r * kBM,
+                          wi.bh);
+          }
+          ++qn[X];
         }
-        ++nq;
+        if (!ok) break;
         const int nbt = wi.nkb + wi.ngb;
         for (int j = 0; j < nbt; ++j) {
           const int st = nb % C::NST;
           const uint32_t su = nb / C::NST;
-          if (su > 0 && !bwait(BAR(iKE + st), (su - 1) & 1, W)) { ok = false; break; }
+          if (su > 0 && !bwait(BAR(C::B_KE + st), (su - 1) & 1, W)) { ok = false; break; }
           const uint32_t kd = sK + st * C::KVB, vd = sV + st * C::KVB;
           if (j < wi.nkb) {
             const int kpos = wi.kb0 + kBN * j;
-            mbar_arrive_expect_tx(BAR(iKF + st), 2u * C::KVB);
+            mbar_arrive_expect_tx(BAR(C::B_KF + st), 2u * C::KVB);
 #pragma unroll
             for (int hh = 0; hh < C::NH; ++hh) {
               if (wi.kind == 0) {
-                tma_load_4d(kd + hh * C::HALF, &p.tmK[wi.slot], BAR(iKF + st), 64 * hh, wi.r, kpos,
-                            wi.bh);
-                tma_load_4d(vd + hh * C::HALF, &p.tmV[wi.slot], BAR(iKF + st), 64 * hh, wi.r, kpos,
-                            wi.bh);
+                tma_load_4d(kd + hh * C::HALF, &p.tmK[wi.slot], BAR(C::B_KF + st), 64 * hh, wi.r,
+                            kpos, wi.bh);
+                tma_load_4d(vd + hh * C::HALF, &p.tmV[wi.slot], BAR(C::B_KF + st), 64 * hh, wi.r,
+                            kpos, wi.bh);
               } else {
-                tma_load_3d(kd + hh * C::HALF, &p.tmKp, BAR(iKF + st), 64 * hh, kpos, wi.bh);
-                tma_load_3d(vd + hh * C::HALF, &p.tmVp, BAR(iKF + st), 64 * hh, kpos, wi.bh);
+                tma_load_3d(kd + hh * C::HALF, &p.tmKp, BAR(C::B_KF + st), 64 * hh, kpos, wi.bh);
+                tma_load_3d(vd + hh * C::HALF, &p.tmVp, BAR(C::B_KF + st), 64 * hh, kpos, wi.bh);
               }
             }
           } else {
             const int gb = j - wi.nkb;
-            mbar_arrive_expect_tx(BAR(iKF + st), 2u * C::NH * p.NGB * 128u);
+            mbar_arrive_expect_tx(BAR(C::B_KF + st), 2u * C::NH * p.NGB * 128u);
 #pragma unroll
             for (int hh = 0; hh < C::NH; ++hh) {
-              tma_load_3d(kd + hh * C::HALF, &p.tmKg, BAR(iKF + st), 64 * hh, gb * p.NGB, wi.bh);
-              tma_load_3d(vd + hh * C::HALF, &p.tmVg, BAR(iKF + st), 64 * hh, gb * p.NGB, wi.bh);
+              tma_load_3d(kd + hh * C::HALF, &p.tmKg, BAR(C::B_KF + st), 64 * hh, gb * p.NGB, wi.bh);
+              tma_load_3d(vd + hh * C::HALF, &p.tmVg, BAR(C::B_KF + st), 64 * hh, gb * p.NGB, wi.bh);
             }
           }
           ++nb;
         }
       }
       if (!ok) {
-        // drain: the last load armed on every stage completes before the CTA exits
+        // drain: the last load armed on every buffer completes before the CTA exits
         for (uint32_t n = (nb > (uint32_t)C::NST ? nb - C::NST : 0u); n < nb; ++n)
-          wait_slow(BAR(iKF + n % C::NST), (n / C::NST) & 1, W, false);
-        for (uint32_t t = (nq > (uint32_t)C::NQ ? nq - C::NQ : 0u); t < nq; ++t)
-          wait_slow(BAR(iQF + t % C::NQ), (t / C::NQ) & 1, W, false);
+          wait_slow(BAR(C::B_KF + n % C::NST), (n / C::NST) & 1, W, false);
+        for (int X = 0; X < 2; ++X)
+          for (uint32_t t = (qn[X] > (uint32_t)C::NQ ? qn[X] - C::NQ : 0u); t < qn[X]; ++t)
+            wait_slow(BAR(C::B_QF + X * C::NQ + t % C::NQ), (t / C::NQ) & 1, W, false);
       }
     }
-  } else if (warp == 1) {
+    } else if (warp == 9 && lane == 0) {
     // -------------------------------------------------------------- MMA
-    if (lane == 0) {
+    // The two slots advance independently: each has an ordered stream of
+    // S_X(b) (one per block it uses) and PV_X(b) products, and the loop
+    // issues whichever next product of either slot has its inputs ready
+    // (non-blocking barrier tests), so that neither slot waits on the other.
+    {
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_g = idesc_bf16(128, p.NGB, false);
       const uint32_t id_pv = idesc_bf16(128, D, true);
-      uint32_t nb = 0, nt = 0;
+      MmaSlot sl[2];
       bool ok = true;
-      for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++nt) {
-        const WorkItem wi = p.items[it];
-        const int qb = nt % C::NQ;
-        if (!bwait(BAR(iQF + qb), (nt / C::NQ) & 1, W)) { ok = false; break; }
-        tc_fence_after();
-        const int nbt = wi.nkb + wi.ngb;
-        auto issue_pv = [&](uint32_t n, int jj) -> bool {
-          const int st = n % C::NST;
-          const int sb = n & 1;
-          if (jj == 0 && nt > 0 && !bwait(BAR(iOF), (nt - 1) & 1, W)) return false;
-          if (!bwait(BAR(iPF + sb), (n >> 1) & 1, W)) return false;
-          tc_fence_after();
-          const int kext = (jj >= wi.nkb) ? p.NGB : kBN;
-          const uint32_t pt = tmem + (sb ? C::TM_P1 : C::TM_P0);
-          for (int kk = 0; kk < kext / 16; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(sV + st * C::KVB + kk * 2048u, C::HALF, 1024);
-            mma_ts(tmem + C::TM_O, pt + kk * 8, bdesc, id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+      using I0 = std::integral_constant<int, 0>;
+      using I1 = std::integral_constant<int, 1>;
+
+      // next item of the CTA's list in which slot X has blocks (from s.it on)
+      auto load_item = [&](auto XC) {
+        constexpr int X = decltype(XC)::value;
+        MmaSlot& s = sl[X];
+        while (s.it < p.n_items) {
+          const WorkItem wi = p.items[s.it];
+          const SlotBlocks sb(wi, X);
+          s.nbt = wi.nkb + wi.ngb;
+          s.cnt = sb.count();
+          if (s.cnt > 0) {
+            s.kind = wi.kind;
+            s.nkb = wi.nkb;
+            s.ngb = wi.ngb;
+            s.jlo = sb.jlo;
+            s.jhi = sb.jhi;
+            s.olo = X ? wi.jlo[0] : wi.jlo[1];
+            s.ohi = X ? wi.jhi[0] : wi.jhi[1];
+            s.j = sb.first();
+            s.seen = 0;
+            return;
           }
-          mma_commit(BAR(iKE + st));
-          mma_commit(BAR(iPV + sb));
-          return true;
-        };
-        for (int j = 0; j < nbt; ++j) {
-          const uint32_t n = nb + j;
-          const int st = n % C::NST;
-          const int sb = n & 1;
-          if (!bwait(BAR(iKF + st), (n / C::NST) & 1, W)) { ok = false; break; }
-          if (n >= 2 && !bwait(BAR(iSR + sb), ((n >> 1) - 1) & 1, W)) { ok = false; break; }
-          tc_fence_after();
-          const bool gblk = j >= wi.nkb;
-          const uint32_t ds = tmem + (sb ? C::TM_S1 : C::TM_S0);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32u;
-            const uint64_t ad = sdesc_sw128(sQ + qb * C::QB + off, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sK + st * C::KVB + off, 16, 1024);
-            mma_ss(ds, ad, bd, gblk ? id_g : id_s, k > 0 ? 1u : 0u);
-          }
-          mma_commit(BAR(iSF + sb));
-          if (j == nbt - 1) mma_commit(BAR(iQE + qb));
-          if (j > 0 && !issue_pv(n - 1, j - 1)) { ok = false; break; }
+          s.base += s.nbt;
+          s.it += gridDim.x;
         }
-        if (!ok) break;
-        if (!issue_pv(nb + nbt - 1, nbt - 1)) { ok = false; break; }
-        nb += nbt;
+        s.j = -1;
+      };
+
+      // O_X += P_X V of the oldest pending block, if its P is written
+      auto try_pv = [&](auto XC) -> bool {
+        constexpr int X = decltype(XC)::value;
+        MmaSlot& s = sl[X];
+        if (s.npend == 0) return false;
+        const uint32_t w = s.pw0;
+        const int stage = w & 7, kext = ((w >> 3) & 15) * 16;
+        const bool first = (w >> 7) & 1, shared = (w >> 8) & 1;
+        if (first && ((w >> 10) & 1) && !mbar_test_wait(BAR(C::B_OE + X), (w >> 9) & 1))
+          return false;
+        if (!mbar_test_wait(BAR(C::B_PF + X), s.kP & 1)) return false;
+        tc_fence_after();
+        const uint32_t to = tmem + (X ? C::TM_O1 : C::TM_O0);
+        const uint32_t tp = tmem + (X ? C::TM_P1 : C::TM_P0);
+        const uint32_t vb = sV + stage * C::KVB;
+        for (int kk = 0; kk < kext / 16; ++kk)
+          mma_ts(to, tp + kk * 8, sdesc_sw128(vb + kk * 2048u, C::HALF, 1024), id_pv,
+                 (!first || kk > 0) ? 1u : 0u);
+        mma_commit(BAR(C::B_PV + X));
+        // the stage is free once every slot using the block has its PV
+        if (!shared || sl[X ^ 1].lastpv >= s.pn0) mma_commit(BAR(C::B_KE + stage));
+        s.lastpv = s.pn0;
+        ++s.kP;
+        s.pw0 = s.pw1;
+        s.pn0 = s.pn1;
+        --s.npend;
+        return true;
+      };
+
+      // S_X = Q_X K^T of the slot's next block, if its inputs are ready
+      auto try_s = [&](auto XC) -> bool {
+        constexpr int X = decltype(XC)::value;
+        MmaSlot& s = sl[X];
+        if (s.j < 0) return false;
+        if (C::P_ALIAS ? s.npend > 0 : s.npend > 1) return false;
+        if (!C::P_ALIAS && s.kS > 0 && !mbar_test_wait(BAR(C::B_SR + X), (s.kS - 1) & 1))
+          return false;
+        const int bi = X * C::NQ + s.qn % C::NQ;
+        if (s.seen == 0 && !mbar_test_wait(BAR(C::B_QF + bi), (s.qn / C::NQ) & 1)) return false;
+        const uint32_t nb = s.base + s.j;
+        const int st = nb % C::NST;
+        if (!mbar_test_wait(BAR(C::B_KF + st), (nb / C::NST) & 1)) return false;
+        tc_fence_after();
+        const bool gblk = s.j >= s.nkb;
+        const uint32_t ds = tmem + (X ? C::TM_S1 : C::TM_S0);
+        const uint32_t qa = sQ + bi * C::QB, ka = sK + st * C::KVB;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32u;
+          mma_ss(ds, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 gblk ? id_g : id_s, k > 0 ? 1u : 0u);
+        }
+        mma_commit(BAR(C::B_SF + X));
+        if (s.seen == 0) ++s.items;
+        if (s.seen == s.cnt - 1) {
+          mma_commit(BAR(C::B_QE + bi));
+          ++s.qn;
+        }
+        // does the other slot use this block too?
+        bool shared;
+        if (s.kind == 0) shared = s.olo <= s.ohi && (gblk || (s.j >= s.olo && s.j <= s.ohi));
+        else shared = false;
+        const uint32_t item = s.items - 1;
+        const uint32_t w = (uint32_t)st | ((uint32_t)((gblk ? p.NGB : kBN) / 16) << 3) |
+                           ((s.seen == 0 ? 1u : 0u) << 7) | ((shared ? 1u : 0u) << 8) |
+                           ((item > 0 ? (item - 1) & 1 : 0u) << 9) | ((item > 0 ? 1u : 0u) << 10);
+        if (s.npend == 0) {
+          s.pw0 = w;
+          s.pn0 = (int)nb;
+        } else {
+          s.pw1 = w;
+          s.pn1 = (int)nb;
+        }
+        ++s.npend;
+        ++s.kS;
+        ++s.seen;
+        // advance to the slot's next block (possibly in a later item)
+        const SlotBlocks sb{s.kind, s.nkb, s.ngb, s.jlo, s.jhi, X};
+        s.j = sb.next(s.j);
+        if (s.j < 0) {
+          s.base += s.nbt;
+          s.it += gridDim.x;
+          load_item(XC);
+        }
+        return true;
+      };
+
+      sl[0].init(blockIdx.x);
+      sl[1].init(blockIdx.x);
+      load_item(I0{});
+      load_item(I1{});
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (sl[0].j >= 0 || sl[0].npend > 0 || sl[1].j >= 0 || sl[1].npend > 0) {
+        bool prog = try_pv(I0{});
+        prog |= try_pv(I1{});
+        prog |= try_s(I0{});
+        prog |= try_s(I1{});
+        if (prog) {
+          idle = 0;
+          continue;
+        }
+        __nanosleep(20);   // nothing ready: leave the issue slots to the softmax warps
+        if ((++idle & 31u) == 0) {
+          const uint64_t now = globaltimer_ns();
+          if (idle == 32) t_idle = now;
+          if (*abort_flag) { ok = false; break; }
+          if (now - t_idle > p.timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(p.status, kStatusTimeout);
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) {
-        mma_commit(BAR(iDR));
-        wait_slow(BAR(iDR), 0, W, false);
+        mma_commit(BAR(C::B_DR));
+        wait_slow(BAR(C::B_DR), 0, W, false);
       }
     }
+    }
+    // teardown (this warpgroup): all TMEM traffic of the CTA is done after the barrier
+    __syncwarp();
+    tc_fence_before();
+    cta_bar_sync();
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
   } else {
+    regs_inc<C::REGS_SOFTMAX>();
     // -------------------------------------------------- softmax + epilogue
+    const int X = warp >> 2;
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const uint32_t tS = tl + (X ? C::TM_S1 : C::TM_S0);
+    const uint32_t tP = tl + (X ? C::TM_P1 : C::TM_P0);
+    const uint32_t tO = tl + (X ? C::TM_O1 : C::TM_O0);
     const float sl2 = p.sl2;
     const float NEG_INF = -__int_as_float(0x7f800000);
-    uint32_t nb = 0, nt = 0;
+    const unsigned FULL = 0xffffffffu;
+    uint32_t k = 0;   // blocks processed by this slot
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++nt) {
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
       const WorkItem wi = p.items[it];
       const bool band = wi.kind == 0;
-      const int nbt = wi.nkb + wi.ngb;
-      int d = 1, Lr = p.L, t = 0, i = 0, wlo = 0, whi = 0;
-      if (band) {
-        d = p.dil[wi.slot];
-        Lr = residue_len(p.L, d, wi.r);
-        t = wi.t0 + row;
-        i = wi.r + d * t;
-        band_window(t, p.w, Lr, wlo, whi);
-      }
-      float m_ref = NEG_INF, l = 0.f;
-      for (int j = 0; j < nbt; ++j) {
-        const uint32_t n = nb + j;
-        const int sb = n & 1;
-        ok = bwait(BAR(iSF + sb), (n >> 1) & 1, W);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        const bool gblk = j >= wi.nkb;
-        const int nch = gblk ? (p.NGB >> 4) : 8;   // 16-column chunks in this block
-        float s[128];
-        const uint32_t sadr = tl + (sb ? C::TM_S1 : C::TM_S0);
-        if (!gblk) {
+      const SlotBlocks sb(wi, X);
+      if (sb.count() == 0) {
+        if (!band) {
+          // the slot had no block of this chunk: an empty partial
+          const int gi = wi.r * kBM + row;
+          if (gi < p.n_g) {
+            const size_t pidx = (static_cast<size_t>(wi.bh) * p.NGQ + gi) * p.n_chunks +
+                                (2 * wi.slot + X);
+            float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t r[32];
-            tmem_ld32(sadr + c4 * 32, r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[c4 * 32 + e] = __uint_as_float(r[e]);
-          }
-        } else {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            if (ch < nch) {
-              uint32_t r[16];
-              tmem_ld16(sadr + ch * 16, r);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) s[ch * 16 + e] = __uint_as_float(r[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) s[ch * 16 + e] = NEG_INF;
-            }
+            for (int c = 0; c < D; c += 4) dst[c >> 2] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.part_ml[pidx * 2 + 0] = NEG_INF;
+            p.part_ml[pidx * 2 + 1] = 0.f;
           }
         }
-        tc_fence_before();
-        mbar_arrive(BAR(iSR + sb));
-
-        // ---- masks
-        if (!gblk) {
+        continue;
+      }
+      int d = 1, i = 0, wlo = 0, whi = p.L - 1, gi = 0;
+      bool rowvalid;
+      if (band) {
+        d = p.dil[wi.slot];
+        const int Lr = residue_len(p.L, d, wi.r);
+        const int t = wi.t0 + kBM * X + row;
+        i = wi.r + d * t;
+        rowvalid = t < Lr;
+        band_window(t, p.w, Lr, wlo, whi);
+      } else {
+        gi = wi.r * kBM + row;
+        rowvalid = gi < p.n_g;
+      }
+      const bool active = __any_sync(FULL, rowvalid);
+      // globals inside the row's window: G[ga .. gz) (band items only); for
+      // dilated heads only those on the row's residue class are in band(i)
+      int ga = 0, gz = 0;
+      if (band && wi.ngb > 0) {
+        ga = sorted_lower(p.gidx, p.n_g, i - d * p.w);
+        gz = sorted_lower(p.gidx, p.n_g, i + d * p.w + 1);
+      }
+      float m_ref = NEG_INF, l = 0.f;
+      bool firstblk = true;
+      for (int j = sb.first(); j >= 0; j = sb.next(j), ++k) {
+        ok = bwait(BAR(C::B_SF + X), k & 1, W);
+        if (!__all_sync(FULL, ok)) { ok = false; break; }
+        tc_fence_after();
+        if (!active) {
+          // no row of this warp is a real query: keep the barrier phases only
+          tc_fence_before();
+          if (!C::P_ALIAS) mbar_arrive(BAR(C::B_SR + X));
+          if (k > 0) {
+            ok = bwait(BAR(C::B_PV + X), (k - 1) & 1, W);
+            if (!__all_sync(FULL, ok)) { ok = false; break; }
+          }
+          mbar_arrive(BAR(C::B_PF + X));
+          continue;
+        }
+        // ---- this row's visible columns of the block, as four 32-bit words
+        uint32_t v0, v1, v2, v3;
+        if (j < wi.nkb) {
+          // band block / key chunk: the columns [clo, chi]
           const int kpos0 = wi.kb0 + kBN * j;
-          int clo, chi;
-          if (band) {
-            clo = wlo - kpos0;
-            chi = whi - kpos0;
-          } else {
-            clo = -kpos0;
-            chi = p.L - 1 - kpos0;
-          }
-          if (clo > 0 || chi < kBN - 1) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = (c >= clo && c <= chi) ? s[c] : NEG_INF;
-          }
+          const int clo = wlo - kpos0, chi1 = whi - kpos0 + 1;
+          v0 = range_bits(clo, chi1, 0);
+          v1 = range_bits(clo, chi1, 32);
+          v2 = range_bits(clo, chi1, 64);
+          v3 = range_bits(clo, chi1, 96);
         } else {
-          const int gb = j - wi.nkb;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            if (ch < nch) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int gi = gb * p.NGB + ch * 16 + e;
-                bool valid = gi < p.n_g;
-                if (valid) valid = !in_band_abs(i, __ldg(p.gidx + gi), d, p.w);
-                s[ch * 16 + e] = valid ? s[ch * 16 + e] : NEG_INF;
+          // gathered globals G[gbase + c]: not the padding, and not a global
+          // already in the row's window (columns [c_lo, c_hi) hold G[ga .. gz);
+          // for dilated heads only those on the row's residue class are in
+          // band(i): the off bits mark the others)
+          const int gbase = (j - wi.nkb) * p.NGB;
+          const int c_lo = ga - gbase, c_hi = gz - gbase, nvalid = p.n_g - gbase;
+          uint32_t off0 = 0, off1 = 0, off2 = 0, off3 = 0;
+          if (d > 1) {
+            const int cb = c_lo > 0 ? c_lo : 0, ce = c_hi < p.NGB ? c_hi : p.NGB;
+            for (int c = cb; c < ce; ++c) {
+              const int diff = __ldg(p.gidx + gbase + c) - i;
+              if (diff % d != 0) {
+                const uint32_t bit = 1u << (c & 31);
+                const int wsel = c >> 5;
+                off0 |= wsel == 0 ? bit : 0u;
+                off1 |= wsel == 1 ? bit : 0u;
+                off2 |= wsel == 2 ? bit : 0u;
+                off3 |= wsel == 3 ? bit : 0u;
               }
             }
           }
+          v0 = range_bits(0, nvalid, 0) & ~(range_bits(c_lo, c_hi, 0) & ~off0);
+          v1 = range_bits(0, nvalid, 32) & ~(range_bits(c_lo, c_hi, 32) & ~off1);
+          v2 = range_bits(0, nvalid, 64) & ~(range_bits(c_lo, c_hi, 64) & ~off2);
+          v3 = range_bits(0, nvalid, 96) & ~(range_bits(c_lo, c_hi, 96) & ~off3);
+        }
+        // warp-wide: which halves any row sees (S_X is read up to the last one)
+        const bool live0 = __any_sync(FULL, (v0 | v1) != 0u);
+        const bool live1 = __any_sync(FULL, (v2 | v3) != 0u);
+
+        // P_X (and O_X) are free once the previous O += P V of this slot has
+        // completed; that is awaited just before the first write (for
+        // D = 128, S_X(k) was issued after PV_X(k-1), so it already has)
+        bool pfree = C::P_ALIAS || k == 0;
+        auto await_pfree = [&]() -> bool {
+          if (pfree) return true;
+          const bool w_ok = bwait(BAR(C::B_PV + X), (k - 1) & 1, W);
+          pfree = true;
+          if (!__all_sync(FULL, w_ok)) return false;
+          tc_fence_after();
+          return true;
+        };
+        if (!C::P_ALIAS && !live0 && !live1) {
+          tc_fence_before();
+          mbar_arrive(BAR(C::B_SR + X));
         }
 
-        // ---- running max (log2 units), rare rescale of O
-        float mx = NEG_INF;
+        // ---- two halves of 64 keys: load, mask, max, exp, store P
+        const float2 sl2v = make_float2(sl2, sl2);
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t va = hf ? v2 : v0, vb = hf ? v3 : v1;
+          const uint32_t tPh = tP + 32 * hf;
+          if (!(hf ? live1 : live0)) {
+            if (!await_pfree()) { ok = false; break; }
+            uint32_t z[16];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float mxs = mx * sl2;
-        if (j == 0) {
-          m_ref = mxs;
-        } else {
-          // per-row decision; the TMEM round trip below is warp-collective
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+            tmem_st16(tPh, z);
+            tmem_st16(tPh + 16, z);
+            continue;
+          }
+          float s[64];
+          {
+            uint32_t r[64];
+            tmem_ld64(tS + 64 * hf, r);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
+          }
+          if (!C::P_ALIAS && (hf == 1 || !live1)) {
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_SR + X));
+          }
+          // chunk classes of the warp: seen by no row / by every row / partly
+          const uint32_t ora = __reduce_or_sync(FULL, va), orb = __reduce_or_sync(FULL, vb);
+          const uint32_t anda = __reduce_and_sync(FULL, va), andb = __reduce_and_sync(FULL, vb);
+          uint32_t vis = 0, full = 0;   // bit c4: chunk c4 (16 keys) of this half
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const uint32_t o = ((c4 < 2 ? ora : orb) >> (16 * (c4 & 1))) & 0xffffu;
+            const uint32_t n = ((c4 < 2 ? anda : andb) >> (16 * (c4 & 1))) & 0xffffu;
+            vis |= (o != 0u ? 1u : 0u) << c4;
+            full |= (n == 0xffffu ? 1u : 0u) << c4;
+          }
+          // masks of the partial chunks; running max over the visible ones
+          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            if (!(vis & (1u << c4))) continue;
+            if (!(full & (1u << c4))) {
+              const uint32_t vw = c4 < 2 ? va : vb;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int bit = 16 * (c4 & 1) + e;
+                s[16 * c4 + e] = (vw & (1u << bit)) ? s[16 * c4 + e] : NEG_INF;
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e += 2)
+              m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[16 * c4 + e], s[16 * c4 + e + 1]);
+          }
+
+          // running max (log2 units); a rare rescale of O (and of P's first
+          // half) when it grows by more than 2^8
+          const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
           const bool need = mxs > m_ref + 8.0f;
           const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
-          if (__any_sync(0xffffffffu, need && m_ref != NEG_INF)) {
-            const uint32_t np = n - 1;
-            ok = bwait(BAR(iPV + (np & 1)), (np >> 1) & 1, W);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
+          if (__any_sync(FULL, need && m_ref != NEG_INF)) {
+            if (!await_pfree()) { ok = false; break; }
+            if (!firstblk) {
+#pragma unroll 1
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + c0, r);
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                tmem_st32(tO + c0, r);
+              }
+            }
+            if (hf == 1 && live0) {
               uint32_t r[32];
-              tmem_ld32(tl + C::TM_O + c0, r);
+              tmem_st_wait();
+              tmem_ld32(tP, r);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(tl + C::TM_O + c0, r);
+              for (int e = 0; e < 32; ++e) {
+                const float lo = __uint_as_float(r[e] << 16), hi = __uint_as_float(r[e] & 0xffff0000u);
+                r[e] = pack_bf16x2(lo * alpha, hi * alpha);
+              }
+              tmem_st32(tP, r);
             }
             tmem_st_wait();
           }
           l *= alpha;
           if (need) m_ref = mxs;
-        }
-        const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+          const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+          const float2 nmu = make_float2(-mu, -mu);
 
-        // ---- P = exp2(s*sl2 - m), row sum, pack to bf16 pairs
-        uint32_t pk[64];
+          // P = 2^(s*sl2 - m) and its row sum, bf16 pairs 32 keys at a time
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          if (ch < nch) {
+          for (int g2 = 0; g2 < 2; ++g2) {
+            if (g2 == 0 && !await_pfree()) { ok = false; break; }
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = ch * 16; c < ch * 16 + 16; c += 2) {
-              const float p0 = ex2_approx(fmaf(s[c], sl2, -mu));
-              const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -mu));
-              l += p0 + p1;
-              pk[c >> 1] = pack_bf16x2(p0, p1);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int c4 = 2 * g2 + h2;
+              if (!(vis & (1u << c4))) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pk[h2 * 8 + e] = 0u;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                  const int c = 16 * c4 + e;
+                  const float2 x = fma2(make_float2(s[c], s[c + 1]), sl2v, nmu);
+                  float2 pv;
+                  if (e < C::EMU16) {
+                    pv = exp2_poly2(x);
+                  } else {
+                    pv.x = ex2_approx(x.x);
+                    pv.y = ex2_approx(x.y);
+                  }
+                  acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+                  pk[h2 * 8 + (e >> 1)] = pack_bf16x2(pv.x, pv.y);
+                }
+              }
             }
-          } else {
-#pragma unroll
-            for (int c = ch * 16; c < ch * 16 + 16; c += 2) pk[c >> 1] = 0u;
+            tmem_st16(tPh + 16 * g2, pk);
           }
+          if (!ok) break;
+          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
         }
-        // P buffer sb was last read by PV(n-2)
-        if (n >= 2) {
-          ok = bwait(BAR(iPV + sb), ((n >> 1) - 1) & 1, W);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-        }
-        const uint32_t padr = tl + (sb ? C::TM_P1 : C::TM_P0);
-        if (!gblk) {
-          uint32_t a[32], b[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) { a[e] = pk[e]; b[e] = pk[32 + e]; }
-          tmem_st32(padr, a);
-          tmem_st32(padr + 32, b);
-        } else {
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (2 * ch < nch) {   // 16 packed columns hold 32 keys (unused ones are 0)
-              uint32_t a[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) a[e] = pk[ch * 16 + e];
-              tmem_st16(padr + ch * 16, a);
-            }
-          }
-        }
+        if (!ok) break;
+        firstblk = false;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(BAR(iPF + sb));
+        mbar_arrive(BAR(C::B_PF + X));
       }
       if (!ok) break;
 
-      // ---- epilogue
-      const uint32_t nl = nb + nbt - 1;
-      ok = bwait(BAR(iPV + (nl & 1)), (nl >> 1) & 1, W);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // ---- epilogue: O_X of the item is final once its last PV completed
+      ok = bwait(BAR(C::B_PV + X), (k - 1) & 1, W);
+      if (!__all_sync(FULL, ok)) { ok = false; break; }
       tc_fence_after();
-      float o[D];
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_O + c0, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[c0 + e] = __uint_as_float(r[e]);
+      if (!active) {
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_OE + X));
+        continue;
       }
-      tc_fence_before();
-      mbar_arrive(BAR(iOF));
-
+      // O is read 32 columns at a time and written straight out
       if (band) {
-        const bool store = (t < Lr) && (p.is_glob[i] == 0);
-        if (store) {
-          const float inv = l > 0.f ? 1.0f / l : 0.f;
-          const size_t base = (static_cast<size_t>(wi.bh) * p.L + i) * D;
-          if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base);
+        const bool store = rowvalid && p.is_glob[i] == 0;
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        const size_t base = (static_cast<size_t>(wi.bh) * p.L + i) * D;
 #pragma unroll
-            for (int c = 0; c < D; c += 4)
-              dst[c >> 2] = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + base);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tO + c0, r);
+          if (store) {
+            if (p.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base + c0);
 #pragma unroll
-            for (int c = 0; c < D; c += 8)
-              dst[c >> 3] = make_uint4(pack_bf16x2(o[c] * inv, o[c + 1] * inv),
-                                       pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv),
-                                       pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv),
-                                       pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv));
+              for (int c = 0; c < 32; c += 4)
+                dst[c >> 2] = make_float4(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv,
+                                          __uint_as_float(r[c + 2]) * inv,
+                                          __uint_as_float(r[c + 3]) * inv);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + base + c0);
+#pragma unroll
+              for (int c = 0; c < 32; c += 8)
+                dst[c >> 3] = make_uint4(
+                    pack_bf16x2(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv),
+                    pack_bf16x2(__uint_as_float(r[c + 2]) * inv, __uint_as_float(r[c + 3]) * inv),
+                    pack_bf16x2(__uint_as_float(r[c + 4]) * inv, __uint_as_float(r[c + 5]) * inv),
+                    pack_bf16x2(__uint_as_float(r[c + 6]) * inv, __uint_as_float(r[c + 7]) * inv));
+            }
           }
         }
       } else {
-        const int gi = wi.r * kBM + row;
-        if (gi < p.n_g) {
-          const size_t pidx =
-              (static_cast<size_t>(wi.bh) * p.NGQ + gi) * p.n_chunks + wi.slot;
-          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D);
+        const size_t pidx = (static_cast<size_t>(wi.bh) * p.NGQ + gi) * p.n_chunks +
+                            (2 * wi.slot + X);
 #pragma unroll
-          for (int c = 0; c < D; c += 4) dst[c >> 2] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tO + c0, r);
+          if (rowvalid) {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + c0);
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              dst[c >> 2] = make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                        __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+          }
+        }
+        if (rowvalid) {
           p.part_ml[pidx * 2 + 0] = m_ref;
           p.part_ml[pidx * 2 + 1] = l;
         }
       }
-      nb += nbt;
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_OE + X));
     }
-  }
-
-  // ---------------------------------------------------------------- teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    // teardown (this warpgroup)
+    __syncwarp();
+    tc_fence_before();
+    cta_bar_sync();
   }
 }
 

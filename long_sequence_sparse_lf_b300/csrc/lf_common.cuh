@@ -22,18 +22,88 @@ constexpr int kBN = 128;            // keys per band block (MMA N)
 
 enum : uint32_t { kStatusTimeout = 1u, kStatusBadItem = 2u };
 
-// One unit of work of the persistent attention kernel.
+// One unit of work of the persistent attention kernel.  A CTA runs two
+// 128-row query tiles side by side (tile slots X = 0 and X = 1) over one
+// shared stream of 128-key blocks; each block names which slots use it.
+//   kind 0 (band pair): slot X holds queries t0 + 128*X .. +127 of residue
+//     class r of head bh (residue space, see above).  Block j < nkb holds keys
+//     kb0 + 128*j .. +127 (residue space); slot X uses blocks jlo[X]..jhi[X]
+//     (empty when jlo > jhi: the slot is absent) and, when present, the ngb
+//     gathered global-key blocks j = nkb .. nkb+ngb-1.
+//   kind 1 (global rows): both slots hold the gathered global queries
+//     r*128 .. r*128+127 of head bh; block j < nkb holds absolute keys
+//     kb0 + 128*j .. +127; slot 0 uses the even blocks, slot 1 the odd ones,
+//     and slot X writes its partial (O, m, l) as key chunk 2*slot + X.
 struct WorkItem {
   int bh;        // b*H + h
-  int kind;      // 0: band tile of a head; 1: global-row tile over a key chunk
-  int r;         // band: residue (i mod d); global: global-row tile index
-  int t0;        // band: first query of the tile in residue space
-  int kb0;       // first key of the first key block (residue space for band,
-                 // absolute position for global rows); may be negative
+  int kind;      // 0: band pair; 1: global rows over a key chunk
+  int r;         // band: residue (i mod d); global: gathered-row tile index
+  int t0;        // band: first query of slot 0 in residue space
+  int kb0;       // first key of block 0 (residue space / absolute position)
   int nkb;       // number of 128-key blocks
-  int ngb;       // band: number of gathered global key blocks; global: 0
-  int slot;      // band: dilation slot; global: key-chunk index
+  int ngb;       // band: gathered global key blocks; global: 0
+  int slot;      // band: dilation slot; global: chunk-pair index
+  int jlo[2];    // band: first block used by each tile slot
+  int jhi[2];    // band: last band block used by each tile slot (inclusive)
 };
+
+// The blocks one tile slot uses in an item, with the slot fixed (its range
+// is taken out of the item once, so that walking it needs no indexing).
+struct SlotBlocks {
+  int kind, nkb, ngb, jlo, jhi, X;
+  __host__ __device__ __forceinline__ SlotBlocks(int kind_, int nkb_, int ngb_, int jlo_, int jhi_,
+                                                 int x)
+      : kind(kind_), nkb(nkb_), ngb(ngb_), jlo(jlo_), jhi(jhi_), X(x) {}
+  __host__ __device__ __forceinline__ SlotBlocks(const WorkItem& wi, int x)
+      : kind(wi.kind), nkb(wi.nkb), ngb(wi.ngb), jlo(x ? wi.jlo[1] : wi.jlo[0]),
+        jhi(x ? wi.jhi[1] : wi.jhi[0]), X(x) {}
+  __host__ __device__ __forceinline__ int count() const {
+    if (kind == 0) return jlo <= jhi ? jhi - jlo + 1 + ngb : 0;
+    return nkb > X ? (nkb - X + 1) / 2 : 0;
+  }
+  __host__ __device__ __forceinline__ int first() const {
+    if (kind == 0) return jlo <= jhi ? jlo : -1;
+    return nkb > X ? X : -1;
+  }
+  __host__ __device__ __forceinline__ int next(int j) const {
+    if (kind == 0) {
+      if (j < jhi) return j + 1;
+      if (j < nkb) return ngb > 0 ? nkb : -1;
+      return j + 1 < nkb + ngb ? j + 1 : -1;
+    }
+    return j + 2 < nkb ? j + 2 : -1;
+  }
+};
+
+// Blocks of item `wi` used by tile slot X.
+__host__ __device__ __forceinline__ bool blk_uses(const WorkItem& wi, int X, int j) {
+  if (wi.kind == 0) {
+    const bool present = wi.jlo[X] <= wi.jhi[X];
+    return present && (j >= wi.nkb || (j >= wi.jlo[X] && j <= wi.jhi[X]));
+  }
+  return j < wi.nkb && (j & 1) == X;
+}
+
+__host__ __device__ __forceinline__ int blk_count(const WorkItem& wi, int X) {
+  if (wi.kind == 0) return wi.jlo[X] <= wi.jhi[X] ? wi.jhi[X] - wi.jlo[X] + 1 + wi.ngb : 0;
+  return wi.nkb > X ? (wi.nkb - X + 1) / 2 : 0;
+}
+
+// first block used by slot X, or -1
+__host__ __device__ __forceinline__ int blk_first(const WorkItem& wi, int X) {
+  if (wi.kind == 0) return wi.jlo[X] <= wi.jhi[X] ? wi.jlo[X] : -1;
+  return wi.nkb > X ? X : -1;
+}
+
+// next block used by slot X after block j, or -1
+__host__ __device__ __forceinline__ int blk_next(const WorkItem& wi, int X, int j) {
+  if (wi.kind == 0) {
+    if (j < wi.jhi[X]) return j + 1;
+    if (j < wi.nkb) return wi.ngb > 0 ? wi.nkb : -1;
+    return j + 1 < wi.nkb + wi.ngb ? j + 1 : -1;
+  }
+  return j + 2 < wi.nkb ? j + 2 : -1;
+}
 
 struct MainParams {
   CUtensorMap tmQ[kMaxDilSlots];   // 4-D views {D, d, L/d, B*H} per dilation slot
@@ -76,6 +146,26 @@ __host__ __device__ __forceinline__ bool in_band_abs(int i, int j, int d, int w)
   int diff = j - i;
   int ad = diff < 0 ? -diff : diff;
   return ad <= d * w && (diff % d) == 0;
+}
+
+// Number of entries of the sorted array G[0..n) that are < x.
+__host__ __device__ __forceinline__ int sorted_lower(const int32_t* G, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (G[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Bits of the columns base .. base+31 that lie in [lo, hi) (bit c - base).
+__host__ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
+  int a = lo - base, b = hi - base;
+  a = a < 0 ? 0 : a;
+  b = b > 32 ? 32 : b;
+  if (b <= a) return 0u;
+  const uint32_t upto_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+  return upto_b & ~((1u << a) - 1u);
 }
 
 // Number of positions p in [0, L) with p mod d == r.

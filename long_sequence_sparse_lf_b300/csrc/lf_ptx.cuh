@@ -45,6 +45,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// non-blocking: true if the phase with the given parity has completed
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -90,6 +103,23 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+// Barrier 0 over the whole CTA, callable from the separate role branches of
+// a warp-specialised kernel (each warp arrives once, converged).
+__device__ __forceinline__ void cta_bar_sync() {
+  asm volatile("bar.sync 0;" ::: "memory");
+}
+
+// Resize this warpgroup's per-thread register allocation (all four warps of
+// the warpgroup execute it).  The counts are immediates, multiples of 8.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -183,6 +213,40 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 64 consecutive columns starting at taddr; waits for completion.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : LF_R8(0), LF_R8(8), LF_R8(16), LF_R8(24), LF_R8(32), LF_R8(40), LF_R8(48), LF_R8(56)
+      : "r"(taddr)
+      : "memory");
+}
+
+// 128 consecutive columns starting at taddr; waits for completion.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, "
+      "%79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
+      "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, "
+      "%111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, "
+      "%125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : LF_R8(0), LF_R8(8), LF_R8(16), LF_R8(24), LF_R8(32), LF_R8(40), LF_R8(48), LF_R8(56),
+        LF_R8(64), LF_R8(72), LF_R8(80), LF_R8(88), LF_R8(96), LF_R8(104), LF_R8(112),
+        LF_R8(120)
+      : "r"(taddr)
+      : "memory");
+}
+
 #undef LF_R8
 
 #define LF_W8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), \
@@ -193,6 +257,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
       "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
       LF_W8(0), LF_W8(8)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      LF_W8(0)
       : "memory");
 }
 
@@ -223,6 +294,68 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// max(a, b, c) in one instruction (three-input form, sm_100 family)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed pair arithmetic on the FMA pipe (one instruction for two fp32
+// lanes; sm_100 family).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// 2^x for a pair of arguments x <= 8 on the FMA pipe instead of the
+// special-function unit (the software-exp2 idea of FlashAttention-4):
+// split x = n + f with n = round(x) (the 1.5 * 2^23 rounding constant puts n
+// in the low mantissa bits), evaluate 2^f on [-1/2, 1/2] with a cubic and
+// add n to the exponent field.  The cubic is our own relative-error minimax
+// fit (Remez exchange; csrc/fit_exp2_poly.py reproduces it): max relative
+// error 7.5e-5, below the bf16 rounding the result then goes through.
+// Arguments are clamped at -125 so that the exponent never underflows; the
+// result there (2^-125) stands in for 0 and is negligible in every sum.
+namespace exp2poly {
+constexpr float C0 = 0.9999280571937561f;
+constexpr float C1 = 0.6932609677314758f;
+constexpr float C2 = 0.2426111251115799f;
+constexpr float C3 = 0.0551716685295105f;
+constexpr float RND = 12582912.0f;   // 1.5 * 2^23
+}  // namespace exp2poly
+
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  using namespace exp2poly;
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 t = add2(x, make_float2(RND, RND));             // n in the low bits
+  const float2 n = add2(t, make_float2(-RND, -RND));           // n as a float
+  const float2 f = add2(x, make_float2(-n.x, -n.y));           // x - n in [-1/2, 1/2]
+  float2 q = fma2(f, make_float2(C3, C3), make_float2(C2, C2));
+  q = fma2(q, f, make_float2(C1, C1));
+  q = fma2(q, f, make_float2(C0, C0));
+  float2 r;
+  r.x = __int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23));
+  r.y = __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23));
   return r;
 }
 
