@@ -22,10 +22,10 @@
 //   warps 4..7  softmax + epilogue of slot 1
 //   warp 8      TMA producer: Q tiles of both slots, then the K/V blocks into
 //               a ring of shared-memory stages
-//   warp 9      TMEM owner and single-thread MMA issuer (tcgen05.mma):
-//               S_X = Q_X K^T into TMEM, then O_X += P_X V with P_X read from
-//               TMEM, interleaving the two slots
-//   warps 10-11 idle
+//   warp 9      TMEM owner; MMA issuer of slot 0 (tcgen05.mma): S_0 = Q_0 K^T
+//               into TMEM, then O_0 += P_0 V with P_0 read from TMEM
+//   warp 10     MMA issuer of slot 1
+//   warp 11     idle
 // While one slot's softmax warps exponentiate, the tensor core works on the
 // other slot, and each SM sub-partition holds one softmax warp of each slot.
 // The launch gives every thread kRegsLaunch registers; the third warpgroup
@@ -61,6 +61,9 @@
 #include "lf_common.cuh"
 #include "lf_ptx.cuh"
 
+#ifndef LF_FULLROW
+#define LF_FULLROW 0       // 1: softmax over the whole 128-key block at once
+#endif
 #ifndef LF_EMU16_D64
 #define LF_EMU16_D64 0     // exponentials per 16 columns done on the FMA pipe (D = 64)
 #endif
@@ -101,8 +104,8 @@ struct KCfg {
   static constexpr int B_PF = B_SR + 2;             // [X] P_X written
   static constexpr int B_PV = B_PF + 2;             // [X] O_X += P_X V done
   static constexpr int B_OE = B_PV + 2;             // [X] O_X read by the epilogue
-  static constexpr int B_DR = B_OE + 2;             // drain
-  static constexpr int NBAR = B_DR + 1;
+  static constexpr int B_DR = B_OE + 2;             // [X] drain
+  static constexpr int NBAR = B_DR + 2;
   static constexpr uint32_t TILE_BYTES = 2u * NQ * QB + 2u * NST * KVB;
   static constexpr uint32_t SMEM_BYTES = TILE_BYTES + NBAR * 8 + 64 + 1024;
   static constexpr int THREADS = 384;
@@ -147,41 +150,6 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const Waite
   return wait_slow(bar, parity, w, true);
 }
 
-// Issue state of one tile slot in the MMA warp: its position in the CTA's
-// item list and block stream, counters of issued products, and the (at most
-// two) blocks whose O += P V is still to be issued, oldest first.  A pending
-// word packs: bits 0-2 stage, 3-6 keys/16, 7 first block of the item (O is
-// overwritten), 8 block shared with the other slot, 9 parity of the item's
-// predecessor, 10 the slot had a previous item (whose O must be read first).
-struct MmaSlot {
-  int it;          // current item (index into the work list)
-  uint32_t base;   // stream position of block 0 of the current item
-  int nbt;         // blocks of the current item
-  int kind, nkb, ngb, jlo, jhi;   // the item as this slot sees it
-  int olo, ohi;    // the other slot's band range in the item
-  int j;           // next block for S (-1: the slot is done)
-  int seen, cnt;   // blocks issued / used in the current item
-  uint32_t kS, kP; // S and PV products issued
-  uint32_t qn;     // Q buffers consumed
-  uint32_t items;  // items started
-  int lastpv;      // stream position of the last PV issued
-  int npend;       // pending PVs (0..2)
-  uint32_t pw0, pw1;
-  int pn0, pn1;    // their stream positions
-  __device__ __forceinline__ void init(int first_item) {
-    it = first_item;
-    base = 0;
-    nbt = 0;
-    j = -1;
-    seen = cnt = 0;
-    kS = kP = qn = items = 0;
-    lastpv = -1;
-    npend = 0;
-    pw0 = pw1 = 0;
-    pn0 = pn1 = 0;
-  }
-};
-
 template <int D>
 __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_constant__ MainParams p) {
   using C = KCfg<D>;
@@ -207,7 +175,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
     }
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(BAR(C::B_KF + s), 1);
-      mbar_init(BAR(C::B_KE + s), 1);
+      mbar_init(BAR(C::B_KE + s), 2);   // one arrival per slot
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(BAR(C::B_SF + x), 1);
@@ -217,6 +185,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       mbar_init(BAR(C::B_OE + x), 128);
     }
     mbar_init(BAR(C::B_DR), 1);
+    mbar_init(BAR(C::B_DR + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -320,168 +289,108 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             wait_slow(BAR(C::B_QF + X * C::NQ + t % C::NQ), (t / C::NQ) & 1, W, false);
       }
     }
-    } else if (warp == 9 && lane == 0) {
-    // -------------------------------------------------------------- MMA
-    // The two slots advance independently: each has an ordered stream of
-    // S_X(b) (one per block it uses) and PV_X(b) products, and the loop
-    // issues whichever next product of either slot has its inputs ready
-    // (non-blocking barrier tests), so that neither slot waits on the other.
-    {
+    } else if ((warp == 9 || warp == 10) && lane == 0) {
+    // ------------------------------------------------------- MMA issuers
+    // One thread per slot (warp 9: slot 0, warp 10: slot 1) walks the CTA's
+    // block stream in order: S_X(b) = Q_X K_b^T for each block the slot
+    // uses and O_X += P_X V_b after its softmax wrote P_X.  Two issuing
+    // threads keep the tensor core fed (issuing one tcgen05.mma costs its
+    // thread tens of cycles, more than a 128x64x16 product takes).
+    // K/V stage b is released by one arrival per slot: the slot's PV commit
+    // if it uses the block, else a plain arrival once the block is loaded.
+    auto issuer = [&](auto XC) {
+      constexpr int X = decltype(XC)::value;
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_g = idesc_bf16(128, p.NGB, false);
       const uint32_t id_pv = idesc_bf16(128, D, true);
-      MmaSlot sl[2];
+      const uint32_t ds = tmem + (X ? C::TM_S1 : C::TM_S0);
+      const uint32_t to = tmem + (X ? C::TM_O1 : C::TM_O0);
+      const uint32_t tp = tmem + (X ? C::TM_P1 : C::TM_P0);
+      uint32_t nb = 0, kS = 0, kP = 0, qn = 0, items = 0;
+      bool pend = false, p_first = false;
+      int p_stage = 0, p_kext = 0;
+      uint32_t p_nb = 0, p_item = 0;
       bool ok = true;
-      using I0 = std::integral_constant<int, 0>;
-      using I1 = std::integral_constant<int, 1>;
-
-      // next item of the CTA's list in which slot X has blocks (from s.it on)
-      auto load_item = [&](auto XC) {
-        constexpr int X = decltype(XC)::value;
-        MmaSlot& s = sl[X];
-        while (s.it < p.n_items) {
-          const WorkItem wi = p.items[s.it];
-          const SlotBlocks sb(wi, X);
-          s.nbt = wi.nkb + wi.ngb;
-          s.cnt = sb.count();
-          if (s.cnt > 0) {
-            s.kind = wi.kind;
-            s.nkb = wi.nkb;
-            s.ngb = wi.ngb;
-            s.jlo = sb.jlo;
-            s.jhi = sb.jhi;
-            s.olo = X ? wi.jlo[0] : wi.jlo[1];
-            s.ohi = X ? wi.jhi[0] : wi.jhi[1];
-            s.j = sb.first();
-            s.seen = 0;
-            return;
-          }
-          s.base += s.nbt;
-          s.it += gridDim.x;
-        }
-        s.j = -1;
-      };
-
-      // O_X += P_X V of the oldest pending block, if its P is written
-      auto try_pv = [&](auto XC) -> bool {
-        constexpr int X = decltype(XC)::value;
-        MmaSlot& s = sl[X];
-        if (s.npend == 0) return false;
-        const uint32_t w = s.pw0;
-        const int stage = w & 7, kext = ((w >> 3) & 15) * 16;
-        const bool first = (w >> 7) & 1, shared = (w >> 8) & 1;
-        if (first && ((w >> 10) & 1) && !mbar_test_wait(BAR(C::B_OE + X), (w >> 9) & 1))
-          return false;
-        if (!mbar_test_wait(BAR(C::B_PF + X), s.kP & 1)) return false;
+      // O_X += P_X V of the pending block, once its P is written
+      auto issue_pv = [&]() -> bool {
+        if (p_first && p_item > 0 && !bwait(BAR(C::B_OE + X), (p_item - 1) & 1, W)) return false;
+        if (!bwait(BAR(C::B_PF + X), kP & 1, W)) return false;
         tc_fence_after();
-        const uint32_t to = tmem + (X ? C::TM_O1 : C::TM_O0);
-        const uint32_t tp = tmem + (X ? C::TM_P1 : C::TM_P0);
-        const uint32_t vb = sV + stage * C::KVB;
-        for (int kk = 0; kk < kext / 16; ++kk)
+        const uint32_t vb = sV + p_stage * C::KVB;
+        for (int kk = 0; kk < p_kext / 16; ++kk)
           mma_ts(to, tp + kk * 8, sdesc_sw128(vb + kk * 2048u, C::HALF, 1024), id_pv,
-                 (!first || kk > 0) ? 1u : 0u);
+                 (!p_first || kk > 0) ? 1u : 0u);
         mma_commit(BAR(C::B_PV + X));
-        // the stage is free once every slot using the block has its PV
-        if (!shared || sl[X ^ 1].lastpv >= s.pn0) mma_commit(BAR(C::B_KE + stage));
-        s.lastpv = s.pn0;
-        ++s.kP;
-        s.pw0 = s.pw1;
-        s.pn0 = s.pn1;
-        --s.npend;
+        mma_commit(BAR(C::B_KE + p_stage));
+        ++kP;
+        pend = false;
         return true;
       };
-
-      // S_X = Q_X K^T of the slot's next block, if its inputs are ready
-      auto try_s = [&](auto XC) -> bool {
-        constexpr int X = decltype(XC)::value;
-        MmaSlot& s = sl[X];
-        if (s.j < 0) return false;
-        if (C::P_ALIAS ? s.npend > 0 : s.npend > 1) return false;
-        if (!C::P_ALIAS && s.kS > 0 && !mbar_test_wait(BAR(C::B_SR + X), (s.kS - 1) & 1))
-          return false;
-        const int bi = X * C::NQ + s.qn % C::NQ;
-        if (s.seen == 0 && !mbar_test_wait(BAR(C::B_QF + bi), (s.qn / C::NQ) & 1)) return false;
-        const uint32_t nb = s.base + s.j;
-        const int st = nb % C::NST;
-        if (!mbar_test_wait(BAR(C::B_KF + st), (nb / C::NST) & 1)) return false;
-        tc_fence_after();
-        const bool gblk = s.j >= s.nkb;
-        const uint32_t ds = tmem + (X ? C::TM_S1 : C::TM_S0);
-        const uint32_t qa = sQ + bi * C::QB, ka = sK + st * C::KVB;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32u;
-          mma_ss(ds, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 gblk ? id_g : id_s, k > 0 ? 1u : 0u);
-        }
-        mma_commit(BAR(C::B_SF + X));
-        if (s.seen == 0) ++s.items;
-        if (s.seen == s.cnt - 1) {
-          mma_commit(BAR(C::B_QE + bi));
-          ++s.qn;
-        }
-        // does the other slot use this block too?
-        bool shared;
-        if (s.kind == 0) shared = s.olo <= s.ohi && (gblk || (s.j >= s.olo && s.j <= s.ohi));
-        else shared = false;
-        const uint32_t item = s.items - 1;
-        const uint32_t w = (uint32_t)st | ((uint32_t)((gblk ? p.NGB : kBN) / 16) << 3) |
-                           ((s.seen == 0 ? 1u : 0u) << 7) | ((shared ? 1u : 0u) << 8) |
-                           ((item > 0 ? (item - 1) & 1 : 0u) << 9) | ((item > 0 ? 1u : 0u) << 10);
-        if (s.npend == 0) {
-          s.pw0 = w;
-          s.pn0 = (int)nb;
-        } else {
-          s.pw1 = w;
-          s.pn1 = (int)nb;
-        }
-        ++s.npend;
-        ++s.kS;
-        ++s.seen;
-        // advance to the slot's next block (possibly in a later item)
-        const SlotBlocks sb{s.kind, s.nkb, s.ngb, s.jlo, s.jhi, X};
-        s.j = sb.next(s.j);
-        if (s.j < 0) {
-          s.base += s.nbt;
-          s.it += gridDim.x;
-          load_item(XC);
-        }
-        return true;
-      };
-
-      sl[0].init(blockIdx.x);
-      sl[1].init(blockIdx.x);
-      load_item(I0{});
-      load_item(I1{});
-      uint32_t idle = 0;
-      uint64_t t_idle = 0;
-      while (sl[0].j >= 0 || sl[0].npend > 0 || sl[1].j >= 0 || sl[1].npend > 0) {
-        bool prog = try_pv(I0{});
-        prog |= try_pv(I1{});
-        prog |= try_s(I0{});
-        prog |= try_s(I1{});
-        if (prog) {
-          idle = 0;
-          continue;
-        }
-        __nanosleep(20);   // nothing ready: leave the issue slots to the softmax warps
-        if ((++idle & 31u) == 0) {
-          const uint64_t now = globaltimer_ns();
-          if (idle == 32) t_idle = now;
-          if (*abort_flag) { ok = false; break; }
-          if (now - t_idle > p.timeout_ns) {
-            *abort_flag = 1;
-            atomicOr(p.status, kStatusTimeout);
+      for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+        const WorkItem wi = p.items[it];
+        const SlotBlocks sb(wi, X);
+        const int nbt = wi.nkb + wi.ngb;
+        const int cnt = sb.count();
+        const bool present = sb.jlo <= sb.jhi;
+        int seen = 0;
+        for (int j = 0; j < nbt; ++j, ++nb) {
+          const int st = nb % C::NST;
+          // block nb reuses the stage of block nb - NST, which the producer
+          // refills only after that block's PVs
+          if (pend && p_nb + C::NST <= nb && !issue_pv()) { ok = false; break; }
+          const bool use = wi.kind == 0 ? present && (j >= wi.nkb || (j >= sb.jlo && j <= sb.jhi))
+                                        : (j < wi.nkb && (j & 1) == X);
+          if (!use) {
+            if (!bwait(BAR(C::B_KF + st), (nb / C::NST) & 1, W)) { ok = false; break; }
+            mbar_arrive(BAR(C::B_KE + st));
+            continue;
+          }
+          if (C::P_ALIAS && pend && !issue_pv()) { ok = false; break; }
+          const int bi = X * C::NQ + qn % C::NQ;
+          if (seen == 0 && !bwait(BAR(C::B_QF + bi), (qn / C::NQ) & 1, W)) { ok = false; break; }
+          if (!bwait(BAR(C::B_KF + st), (nb / C::NST) & 1, W)) { ok = false; break; }
+          if (!C::P_ALIAS && kS > 0 && !bwait(BAR(C::B_SR + X), (kS - 1) & 1, W)) {
             ok = false;
             break;
           }
+          tc_fence_after();
+          const bool gblk = j >= wi.nkb;
+          const uint32_t qa = sQ + bi * C::QB, ka = sK + st * C::KVB;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32u;
+            mma_ss(ds, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                   gblk ? id_g : id_s, k > 0 ? 1u : 0u);
+          }
+          mma_commit(BAR(C::B_SF + X));
+          const bool last = seen == cnt - 1;
+          if (last) {
+            mma_commit(BAR(C::B_QE + bi));
+            ++qn;
+          }
+          if (!C::P_ALIAS && pend && !issue_pv()) { ok = false; break; }
+          if (seen == 0) ++items;
+          pend = true;
+          p_stage = st;
+          p_kext = gblk ? p.NGB : kBN;
+          p_first = seen == 0;
+          p_item = items - 1;
+          p_nb = nb;
+          ++seen;
+          ++kS;
+          // the slot's last block of the item: its PV goes at once, so that
+          // the epilogue does not wait for the next item's loads
+          if (last && !issue_pv()) { ok = false; break; }
         }
       }
+      if (ok && pend && !issue_pv()) ok = false;
       if (!ok) {
-        mma_commit(BAR(C::B_DR));
-        wait_slow(BAR(C::B_DR), 0, W, false);
+        mma_commit(BAR(C::B_DR + X));
+        wait_slow(BAR(C::B_DR + X), 0, W, false);
       }
-    }
+    };
+    if (warp == 9) issuer(std::integral_constant<int, 0>{});
+    else issuer(std::integral_constant<int, 1>{});
     }
     // teardown (this warpgroup): all TMEM traffic of the CTA is done after the barrier
     __syncwarp();
@@ -601,9 +510,24 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           v2 = range_bits(0, nvalid, 64) & ~(range_bits(c_lo, c_hi, 64) & ~off2);
           v3 = range_bits(0, nvalid, 96) & ~(range_bits(c_lo, c_hi, 96) & ~off3);
         }
-        // warp-wide: which halves any row sees (S_X is read up to the last one)
-        const bool live0 = __any_sync(FULL, (v0 | v1) != 0u);
-        const bool live1 = __any_sync(FULL, (v2 | v3) != 0u);
+        // warp-wide classes of the 16-key chunks: seen by some row (vis) /
+        // by every row (full); S_X is read up to the last half any row sees
+        uint32_t vis = 0, full = 0;
+        {
+          const uint32_t o0 = __reduce_or_sync(FULL, v0), o1 = __reduce_or_sync(FULL, v1);
+          const uint32_t o2 = __reduce_or_sync(FULL, v2), o3 = __reduce_or_sync(FULL, v3);
+          const uint32_t a0 = __reduce_and_sync(FULL, v0), a1 = __reduce_and_sync(FULL, v1);
+          const uint32_t a2 = __reduce_and_sync(FULL, v2), a3 = __reduce_and_sync(FULL, v3);
+          const uint32_t ow[4] = {o0, o1, o2, o3}, aw[4] = {a0, a1, a2, a3};
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t oh = (ow[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
+            const uint32_t ah = (aw[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
+            vis |= (oh != 0u ? 1u : 0u) << ch;
+            full |= (ah == 0xffffu ? 1u : 0u) << ch;
+          }
+        }
+        const bool live0 = (vis & 0x0Fu) != 0u, live1 = (vis & 0xF0u) != 0u;
 
         // P_X (and O_X) are free once the previous O += P V of this slot has
         // completed; that is awaited just before the first write (for
@@ -622,11 +546,95 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           mbar_arrive(BAR(C::B_SR + X));
         }
 
+#if LF_FULLROW
+        // ---- the whole block (128 keys) at once: load, mask, max, exp, store P
+        {
+          const float2 sl2v = make_float2(sl2, sl2);
+          float s[128];
+          {
+            uint32_t r[128];
+            tmem_ld128(tS, r);
+#pragma unroll
+            for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
+          }
+          if (!C::P_ALIAS && (live0 || live1)) {
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_SR + X));
+          }
+          // mask the chunks not every row sees (chunks no row sees entirely)
+          if (full != 0xFFu) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              if (full & (1u << ch)) continue;
+              if (!(vis & (1u << ch))) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) s[16 * ch + e] = NEG_INF;
+              } else {
+                const uint32_t vw = ch < 4 ? (ch < 2 ? v0 : v1) : (ch < 6 ? v2 : v3);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const int bit = 16 * (ch & 1) + e;
+                  s[16 * ch + e] = (vw & (1u << bit)) ? s[16 * ch + e] : NEG_INF;
+                }
+              }
+            }
+          }
+          // running max (log2 units); a rare rescale of O when it grows by
+          // more than 2^8
+          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+          for (int e = 0; e < 128; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
+          const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+          const bool need = mxs > m_ref + 8.0f;
+          const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
+          if (__any_sync(FULL, need && m_ref != NEG_INF) && !firstblk) {
+            if (!await_pfree()) { ok = false; break; }
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c0, r);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(tO + c0, r);
+            }
+            tmem_st_wait();
+          }
+          l *= alpha;
+          if (need) m_ref = mxs;
+          const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+          const float2 nmu = make_float2(-mu, -mu);
+          // P = 2^(s*sl2 - m) over the 128 keys (masked ones give 0), its row
+          // sum, bf16 pairs stored 32 keys at a time
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int c = 32 * g + e;
+              const float2 x = fma2(make_float2(s[c], s[c + 1]), sl2v, nmu);
+              float2 pv;
+              if ((e & 15) < C::EMU16) {
+                pv = exp2_poly2(x);
+              } else {
+                pv.x = ex2_approx(x.x);
+                pv.y = ex2_approx(x.y);
+              }
+              acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+              pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
+            }
+            if (g == 0 && !await_pfree()) { ok = false; break; }
+            tmem_st16(tP + 16 * g, pk);
+          }
+          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+        }
+#else
         // ---- two halves of 64 keys: load, mask, max, exp, store P
         const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
-          const uint32_t va = hf ? v2 : v0, vb = hf ? v3 : v1;
           const uint32_t tPh = tP + 32 * hf;
           if (!(hf ? live1 : live0)) {
             if (!await_pfree()) { ok = false; break; }
@@ -648,37 +656,33 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             tc_fence_before();
             mbar_arrive(BAR(C::B_SR + X));
           }
-          // chunk classes of the warp: seen by no row / by every row / partly
-          const uint32_t ora = __reduce_or_sync(FULL, va), orb = __reduce_or_sync(FULL, vb);
-          const uint32_t anda = __reduce_and_sync(FULL, va), andb = __reduce_and_sync(FULL, vb);
-          uint32_t vis = 0, full = 0;   // bit c4: chunk c4 (16 keys) of this half
+          // mask the chunks not every row sees (chunks no row sees entirely)
+          const uint32_t va = hf ? v2 : v0, vb = hf ? v3 : v1;
+          const uint32_t hvis = (vis >> (4 * hf)) & 0xFu, hfull = (full >> (4 * hf)) & 0xFu;
+          if (hfull != 0xFu) {
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const uint32_t o = ((c4 < 2 ? ora : orb) >> (16 * (c4 & 1))) & 0xffffu;
-            const uint32_t n = ((c4 < 2 ? anda : andb) >> (16 * (c4 & 1))) & 0xffffu;
-            vis |= (o != 0u ? 1u : 0u) << c4;
-            full |= (n == 0xffffu ? 1u : 0u) << c4;
-          }
-          // masks of the partial chunks; running max over the visible ones
-          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+            for (int c4 = 0; c4 < 4; ++c4) {
+              if (hfull & (1u << c4)) continue;
+              if (!(hvis & (1u << c4))) {
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            if (!(vis & (1u << c4))) continue;
-            if (!(full & (1u << c4))) {
-              const uint32_t vw = c4 < 2 ? va : vb;
+                for (int e = 0; e < 16; ++e) s[16 * c4 + e] = NEG_INF;
+              } else {
+                const uint32_t vw = c4 < 2 ? va : vb;
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int bit = 16 * (c4 & 1) + e;
-                s[16 * c4 + e] = (vw & (1u << bit)) ? s[16 * c4 + e] : NEG_INF;
+                for (int e = 0; e < 16; ++e) {
+                  const int bit = 16 * (c4 & 1) + e;
+                  s[16 * c4 + e] = (vw & (1u << bit)) ? s[16 * c4 + e] : NEG_INF;
+                }
               }
             }
-#pragma unroll
-            for (int e = 0; e < 16; e += 2)
-              m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[16 * c4 + e], s[16 * c4 + e + 1]);
           }
 
           // running max (log2 units); a rare rescale of O (and of P's first
           // half) when it grows by more than 2^8
+          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
           const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
           const bool need = mxs > m_ref + 8.0f;
           const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
@@ -712,41 +716,35 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
           const float2 nmu = make_float2(-mu, -mu);
 
-          // P = 2^(s*sl2 - m) and its row sum, bf16 pairs 32 keys at a time
+          // P = 2^(s*sl2 - m) over all 64 keys (masked ones give 0), its row
+          // sum, and bf16 pairs
           float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
+          uint32_t pk[32];
 #pragma unroll
-          for (int g2 = 0; g2 < 2; ++g2) {
-            if (g2 == 0 && !await_pfree()) { ok = false; break; }
-            uint32_t pk[16];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int c4 = 2 * g2 + h2;
-              if (!(vis & (1u << c4))) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) pk[h2 * 8 + e] = 0u;
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                  const int c = 16 * c4 + e;
-                  const float2 x = fma2(make_float2(s[c], s[c + 1]), sl2v, nmu);
-                  float2 pv;
-                  if (e < C::EMU16) {
-                    pv = exp2_poly2(x);
-                  } else {
-                    pv.x = ex2_approx(x.x);
-                    pv.y = ex2_approx(x.y);
-                  }
-                  acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
-                  pk[h2 * 8 + (e >> 1)] = pack_bf16x2(pv.x, pv.y);
-                }
-              }
+          for (int e = 0; e < 64; e += 2) {
+            const float2 x = fma2(make_float2(s[e], s[e + 1]), sl2v, nmu);
+            float2 pv;
+            if ((e & 15) < C::EMU16) {
+              pv = exp2_poly2(x);
+            } else {
+              pv.x = ex2_approx(x.x);
+              pv.y = ex2_approx(x.y);
             }
-            tmem_st16(tPh + 16 * g2, pk);
+            acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+            pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
           }
-          if (!ok) break;
+          if (!await_pfree()) { ok = false; break; }
+          {
+            uint32_t a[16], b2[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) { a[e] = pk[e]; b2[e] = pk[16 + e]; }
+            tmem_st16(tPh, a);
+            tmem_st16(tPh + 16, b2);
+          }
           l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
         }
+#endif
         if (!ok) break;
         firstblk = false;
         tmem_st_wait();

@@ -158,14 +158,15 @@ __host__ __device__ __forceinline__ int sorted_lower(const int32_t* G, int n, in
   return lo;
 }
 
-// Bits of the columns base .. base+31 that lie in [lo, hi) (bit c - base).
+// Bits of the columns base .. base+31 that lie in [lo, hi) (bit c - base),
+// without branches.
 __host__ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   int a = lo - base, b = hi - base;
-  a = a < 0 ? 0 : a;
-  b = b > 32 ? 32 : b;
-  if (b <= a) return 0u;
-  const uint32_t upto_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
-  return upto_b & ~((1u << a) - 1u);
+  a = a < 0 ? 0 : (a > 32 ? 32 : a);
+  b = b < 0 ? 0 : (b > 32 ? 32 : b);
+  const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+  const uint32_t below_a = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+  return below_b & ~below_a;
 }
 
 // Number of positions p in [0, L) with p mod d == r.
