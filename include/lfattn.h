@@ -106,6 +106,40 @@ LF_API lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, v
                            lf_stream_t stream);
 
 /*
+ * lf_attn_fwd_noalloc — lf_attn_fwd for callers that may not allocate
+ * device memory.  The pages describe no such call; it exists for callers
+ * that cannot let a library allocate: inference engines that plan all device
+ * memory when they start and forbid allocation afterwards (for predictable
+ * latency and no out-of-memory failure mid-run), and processes whose caching
+ * allocator already holds the free device memory, where a direct allocation
+ * would fail or fragment it.
+ *
+ * Same arguments, arithmetic and errors as lf_attn_fwd (bf16 in / bf16 out);
+ * the output is the same.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine: its scratch (work list, global-position tables,
+ * gathered global rows, global-row partials) lives in one fixed device array
+ * of 32 MiB that the library declares and that every GPU loading the library
+ * holds until the process exits.  A problem needing more scratch is rejected
+ * with LF_ERR_UNSUPPORTED and a message giving both sizes (for example B=1,
+ * H=16, L=65536, D=128 with 16 global tokens needs about 55 MiB).  Problems
+ * without global tokens need only the work list and the global flags.
+ *
+ *   - The first call on a device looks up the array's device address there
+ *     (one cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - Every call uses the same array and overwrites what the previous call
+ *     left in it; nothing in it needs to start at zero.  Calls whose work
+ *     overlaps on the GPU (other streams, other threads) race on it: order
+ *     them on one stream, or synchronise between them.
+ *   - The per-kernel event tracing (lf_profile_*) does not record its
+ *     launches; lf_launch_count counts them.
+ */
+LF_API lf_status lf_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B,
+                                     int H, int L, int D, int w, const int32_t* dilation,
+                                     const int32_t* global_idx, int n_global, float scale,
+                                     lf_stream_t stream);
+
+/*
  * lf_attn_pairs — the attended key lists, per (head, query), in CSR form.
  * Batch-independent (the pattern does not depend on b).
  *

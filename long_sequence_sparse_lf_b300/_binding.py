@@ -46,6 +46,8 @@ def load_library() -> ctypes.CDLL:
     lib.lf_attn_fwd.restype = i32
     lib.lf_attn_fwd_f32.argtypes = fwd_args
     lib.lf_attn_fwd_f32.restype = i32
+    lib.lf_attn_fwd_noalloc.argtypes = fwd_args
+    lib.lf_attn_fwd_noalloc.restype = i32
     lib.lf_attn_fwd_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, ip, ip, i32,
                                      f32, vp]
     lib.lf_attn_fwd_host.restype = i32
@@ -132,6 +134,21 @@ def lf_attn_fwd_f32(q, k, v, out, w: int, dilation: Sequence[int],
     _check(lib.lf_attn_fwd_f32(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L,
                                D, int(w), _i32_array(dilation), _i32_array(global_idx),
                                len(global_idx), float(scale), _stream_handle(stream)))
+    return out
+
+
+def lf_attn_fwd_noalloc(q, k, v, out, w: int, dilation: Sequence[int],
+                        global_idx: Sequence[int], scale: float, stream=None):
+    """bf16 forward through the entry point that allocates no device memory
+    (its scratch is a fixed device array of the library; see lfattn.h)."""
+    _check_qkv(q, k, v, out, torch.bfloat16, "cuda")
+    B, H, L, D = q.shape
+    if len(dilation) != H:
+        raise ValueError("dilation must have H entries")
+    lib = load_library()
+    _check(lib.lf_attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                   L, D, int(w), _i32_array(dilation), _i32_array(global_idx),
+                                   len(global_idx), float(scale), _stream_handle(stream)))
     return out
 
 

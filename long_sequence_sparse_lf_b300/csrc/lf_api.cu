@@ -591,6 +591,205 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   return LF_OK;
 }
 
+// ------------------------------------------------- allocation-free forward
+//
+// Scratch of lf_attn_fwd_noalloc: one file-scope device array, sized once
+// for every GPU that loads the library (see kNoAllocScratchBytes).  It holds,
+// per call, the work list, the global-position tables, the gathered global
+// rows and the global-row partials.  Host code never names the array as a
+// device address; it takes the address from cudaGetSymbolAddress once per
+// device (noalloc_scratch below).
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDev {
+  bool ready = false;
+  uint8_t* scratch = nullptr;
+};
+std::vector<NoAllocDev> g_noalloc_dev;
+
+// Device address of the scratch array on the current device `dev`; looked
+// up on the first call for that device.
+lf_status noalloc_scratch(int dev, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_noalloc_dev.size() <= dev) g_noalloc_dev.resize(dev + 1);
+  NoAllocDev& nd = g_noalloc_dev[dev];
+  if (!nd.ready) {
+    void* ptr = nullptr;
+    LF_CUDA(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+    if (ptr == nullptr) return fail(LF_ERR_CUDA, "no device address for the scratch array");
+    nd.scratch = static_cast<uint8_t*>(ptr);
+    nd.ready = true;
+  }
+  *out = nd.scratch;
+  return LF_OK;
+}
+
+lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* out, int B, int H,
+                           int L, int D, int w, const int32_t* dilation, const int32_t* gidx,
+                           int n_g, float scale, cudaStream_t stream) {
+  t_last_error.clear();
+  if (B < 1) return fail(LF_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  if (!q || !k || !v || !out) return fail(LF_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LF_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(LF_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (D != 64 && D != 128) return fail(LF_ERR_UNSUPPORTED, "D=%d (supported: 64, 128)", D);
+  for (int h = 0; h < H; ++h)
+    if (dilation[h] > 1 && L % dilation[h] != 0)
+      return fail(LF_ERR_UNSUPPORTED, "L=%d is not a multiple of dilation[%d]=%d", L, h,
+                  dilation[h]);
+  if ((long long)B * H > (1LL << 30)) return fail(LF_ERR_UNSUPPORTED, "B*H too large");
+
+  // the plan, on the host only (the cached plans live in allocated memory)
+  Plan pl;
+  {
+    auto pat = std::make_shared<Pattern>();
+    pat->H = H;
+    pat->L = L;
+    pat->w = w;
+    pat->n_g = n_g;
+    pat->dil.assign(dilation, dilation + H);
+    if (n_g) pat->G.assign(gidx, gidx + n_g);
+    pat->isg.assign(L, 0);
+    for (int g : pat->G) pat->isg[g] = 1;
+    pl.pat = pat;
+  }
+  pl.B = B;
+  pl.D = D;
+  pl.head_slot.resize(H);
+  for (int h = 0; h < H; ++h) {
+    int sl = 0;
+    while (sl < pl.n_slots && pl.slot_dil[sl] != dilation[h]) ++sl;
+    if (sl == pl.n_slots) {
+      if (pl.n_slots == lf::kMaxDilSlots)
+        return fail(LF_ERR_UNSUPPORTED, "more than %d distinct dilation values", lf::kMaxDilSlots);
+      pl.slot_dil[pl.n_slots++] = dilation[h];
+    }
+    pl.head_slot[h] = sl;
+  }
+
+  // scratch layout: work list | global positions | global flags | gathered
+  // q, k, v | partial O | partial (m, l); each part 256-byte aligned
+  const int BH = B * H;
+  DevState* ds = nullptr;
+  int dev = 0;
+  if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
+  build_items(pl, ds->num_sms);
+  if (!items_consistent(pl)) return fail(LF_ERR_INVALID_ARG, "internal: inconsistent work list");
+  size_t off = 0;
+  const size_t off_items = off;
+  off += align_up(sizeof(WorkItem) * std::max<size_t>(pl.items.size(), 1), 256);
+  const size_t off_gidx = off;
+  off += align_up(sizeof(int32_t) * std::max(n_g, 1), 256);
+  const size_t off_isg = off;
+  off += align_up((size_t)L, 256);
+  const size_t off_g = off;
+  const size_t g_elems = (size_t)BH * pl.NGQ * D;
+  if (n_g > 0) off += align_up(3 * g_elems * 2, 256);
+  const size_t off_po = off;
+  const size_t n_part = (size_t)BH * pl.NGQ * pl.n_chunks;
+  if (n_g > 0) off += align_up(n_part * D * 4, 256);
+  const size_t off_pm = off;
+  if (n_g > 0) off += align_up(n_part * 2 * 4, 256);
+  if (off > kNoAllocScratchBytes)
+    return fail(LF_ERR_UNSUPPORTED,
+                "this problem needs %zu bytes of scratch; the allocation-free entry point has "
+                "%zu (use lf_attn_fwd)",
+                off, kNoAllocScratchBytes);
+
+  uint8_t* ws = nullptr;
+  if ((s = noalloc_scratch(dev, &ws)) != LF_OK) return s;
+  // tables into the scratch array (plain copies; nothing needs clearing:
+  // every byte the kernels read is written first, by these copies or by the
+  // gather kernel and the attention kernel's partial writes)
+  WorkItem* d_items = reinterpret_cast<WorkItem*>(ws + off_items);
+  int32_t* d_gidx = reinterpret_cast<int32_t*>(ws + off_gidx);
+  uint8_t* d_isg = ws + off_isg;
+  if (!pl.items.empty())
+    LF_CUDA(cudaMemcpyAsync(d_items, pl.items.data(), sizeof(WorkItem) * pl.items.size(),
+                            cudaMemcpyHostToDevice, stream));
+  if (n_g > 0)
+    LF_CUDA(cudaMemcpyAsync(d_gidx, gidx, sizeof(int32_t) * n_g, cudaMemcpyHostToDevice, stream));
+  LF_CUDA(cudaMemcpyAsync(d_isg, pl.pat->isg.data(), (size_t)L, cudaMemcpyHostToDevice, stream));
+
+  MainParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  for (int sl = 0; sl < pl.n_slots; ++sl) {
+    const int d = pl.slot_dil[sl];
+    prm.dil[sl] = d;
+    if ((s = map_residue(ds, &prm.tmQ[sl], q, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &prm.tmK[sl], k, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &prm.tmV[sl], v, D, L, d, BH)) != LF_OK) return s;
+  }
+  uint16_t* qg = reinterpret_cast<uint16_t*>(ws + off_g);
+  uint16_t* kg = qg + g_elems;
+  uint16_t* vg = kg + g_elems;
+  if (n_g > 0) {
+    if ((s = map_rows(ds, &prm.tmKp, k, D, L, BH, lf::kBN)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmVp, v, D, L, BH, lf::kBN)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmQg, qg, D, pl.NGQ, BH, lf::kBM)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmKg, kg, D, pl.NGQ, BH, pl.NGB)) != LF_OK) return s;
+    if ((s = map_rows(ds, &prm.tmVg, vg, D, pl.NGQ, BH, pl.NGB)) != LF_OK) return s;
+  }
+  prm.items = d_items;
+  prm.n_items = (int)pl.items.size();
+  prm.gidx = d_gidx;
+  prm.is_glob = d_isg;
+  prm.n_g = n_g;
+  prm.NGB = pl.NGB;
+  prm.NGQ = pl.NGQ;
+  prm.n_chunks = pl.n_chunks;
+  prm.out = out;
+  prm.out_f32 = 0;
+  prm.part_o = reinterpret_cast<float*>(ws + off_po);
+  prm.part_ml = reinterpret_cast<float*>(ws + off_pm);
+  prm.H = H;
+  prm.L = L;
+  prm.w = w;
+  prm.sl2 = scale * 1.4426950408889634f;
+  prm.status = ds->status;
+  prm.timeout_ns = wait_timeout_ns();
+
+  if (n_g > 0) {
+    const size_t total = (size_t)BH * pl.NGQ * (D / 8);
+    const int threads = 256;
+    const int blocks = (int)std::max<size_t>(1, std::min<size_t>((total + threads - 1) / threads,
+                                                                 (size_t)ds->num_sms * 8));
+    lf::lf_gather_globals_kernel<<<blocks, threads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
+        reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(qg),
+        reinterpret_cast<uint4*>(kg), reinterpret_cast<uint4*>(vg), d_gidx, n_g, pl.NGQ, L, D,
+        BH);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  if (prm.n_items > 0) {
+    const int grid = std::min(prm.n_items, ds->num_sms);
+    if (D == 64)
+      lf::lf_attn_main_kernel<64><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
+    else
+      lf::lf_attn_main_kernel<128><<<grid, lf::KCfg<128>::THREADS, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  if (n_g > 0) {
+    const int threads = 256;
+    const long long warps = (long long)BH * n_g;
+    const int blocks = (int)((warps + threads / 32 - 1) / (threads / 32));
+    if (D == 64)
+      lf::lf_combine_globals_kernel<64><<<blocks, threads, 0, stream>>>(
+          prm.part_o, prm.part_ml, d_gidx, out, 0, n_g, pl.NGQ, pl.n_chunks, L, BH);
+    else
+      lf::lf_combine_globals_kernel<128><<<blocks, threads, 0, stream>>>(
+          prm.part_o, prm.part_ml, d_gidx, out, 0, n_g, pl.NGQ, pl.n_chunks, L, BH);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  LF_CUDA(cudaGetLastError());
+  return LF_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -773,6 +972,20 @@ lf_status lf_profile_query(const char* name, double* total_ms, uint64_t* launche
   *total_ms = ms;
   *launches = n;
   return LF_OK;
+}
+
+lf_status lf_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B,
+                              int H, int L, int D, int w, const int32_t* dilation,
+                              const int32_t* global_idx, int n_global, float scale,
+                              lf_stream_t stream) {
+  try {
+    return fwd_noalloc_impl(q, k, v, out, B, H, L, D, w, dilation, global_idx, n_global, scale,
+                            static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
 }
 
 int lf_version(void) { return 100; }
