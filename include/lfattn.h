@@ -27,8 +27,12 @@
  *     NULL = the legacy default stream); only lf_attn_get_status,
  *     lf_attn_pairs (which returns a count) and lf_attn_fwd_host block.
  *   - Library-owned state: a cache of per-shape plans (device work lists and
- *     the global-position table) and per-call scratch taken from the
- *     stream-ordered allocator (cudaMallocAsync / cudaFreeAsync).
+ *     the global-position table), the kernel parameters of recent calls, and
+ *     one grow-only scratch buffer per (device, stream) taken from the
+ *     stream-ordered allocator (cudaMallocAsync / cudaFreeAsync), reused by
+ *     every later call on that stream.  A stream handle that is destroyed
+ *     and reused by a new stream inherits the buffer: finish the old
+ *     stream's work first.
  *   - No C++ exception crosses this interface.  A non-OK status leaves a
  *     message for lf_last_error() in the calling thread.
  *   - Device-side waits are bounded; a wait that runs out records a timeout
@@ -170,7 +174,8 @@ LF_API const char* lf_last_error(void);
  */
 LF_API lf_status lf_attn_get_status(lf_stream_t stream);
 
-/* Frees every cached plan (synchronises the device). */
+/* Frees every cached plan, cached call parameters and scratch buffer
+ * (synchronises the device). */
 LF_API void lf_plan_cache_clear(void);
 
 /* Number of kernels this library has launched in this process (all devices,

@@ -152,6 +152,43 @@ def lf_attn_fwd_noalloc(q, k, v, out, w: int, dilation: Sequence[int],
     return out
 
 
+class PreparedFwd:
+    """lf_attn_fwd (bf16) or lf_attn_fwd_f32 (fp32) with its arguments
+    marshalled once; calling the object runs the forward on the stream given
+    here.  The tensors are referenced, not copied: they must keep their
+    storage for as long as the object is used."""
+
+    def __init__(self, q, k, v, out, w: int, dilation: Sequence[int],
+                 global_idx: Sequence[int], scale: float, stream=None):
+        dtype = q.dtype
+        if dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("q must be bf16 or fp32")
+        _check_qkv(q, k, v, out, dtype, "cuda")
+        B, H, L, D = q.shape
+        if len(dilation) != H:
+            raise ValueError("dilation must have H entries")
+        lib = load_library()
+        self._fn = lib.lf_attn_fwd if dtype == torch.bfloat16 else lib.lf_attn_fwd_f32
+        dil, gi = _i32_array(dilation), _i32_array(global_idx)
+        self._keep = (q, k, v, out, dil, gi)
+        self.out = out
+        st = _stream_handle(stream)
+        self._args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, D,
+                      int(w), dil, gi, len(global_idx), float(scale), st)
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status != LF_OK:
+            _check(status)
+        return self.out
+
+
+def prepare_fwd(q, k, v, out, w: int, dilation: Sequence[int], global_idx: Sequence[int],
+                scale: float, stream=None) -> PreparedFwd:
+    """The forward of lf_attn_fwd / lf_attn_fwd_f32, marshalled for repeated calls."""
+    return PreparedFwd(q, k, v, out, w, dilation, global_idx, scale, stream)
+
+
 def lf_attn_fwd_host(q, k, v, out, w: int, dilation: Sequence[int],
                      global_idx: Sequence[int], scale: float, stream=None):
     """Forward on HOST tensors (bf16 or fp32); copies in and out, blocks."""

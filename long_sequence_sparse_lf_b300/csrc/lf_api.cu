@@ -442,6 +442,93 @@ lf_status map_rows(DevState* ds, CUtensorMap* m, const void* base, int D, int ro
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Scratch of lf_attn_fwd / lf_attn_fwd_f32: one grow-only buffer per
+// (device, stream).  Calls on one stream are ordered, so they can share it;
+// a larger need frees the old buffer and allocates a new one, both
+// stream-ordered.  lf_plan_cache_clear releases every buffer.
+struct Workspace {
+  uint8_t* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+lf_status get_workspace(int dev, cudaStream_t stream, size_t bytes, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_workspaces[{dev, stream}];
+  if (w.bytes < bytes) {
+    if (w.ptr) LF_CUDA(cudaFreeAsync(w.ptr, stream));
+    w.ptr = nullptr;
+    w.bytes = 0;
+    const size_t grow = align_up(bytes, size_t(1) << 20);
+    LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&w.ptr), grow, stream));
+    w.bytes = grow;
+  }
+  *out = w.ptr;
+  return LF_OK;
+}
+
+// Kernel parameters (tensor maps included) of recent calls, keyed by the
+// plan and every device address they embed, so that a repeated call encodes
+// nothing.
+using ParamKey = std::tuple<const Plan*, const void*, const void*, const void*, void*, bool,
+                            const uint8_t*, float>;
+std::map<ParamKey, std::unique_ptr<MainParams>> g_params;
+constexpr size_t kMaxCachedParams = 256;
+
+// Kernel parameters of one call: tensor maps of q, k, v (one residue view
+// per dilation value) and of the gathered global rows, and the scratch
+// addresses.
+lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, const void* qb,
+                       const void* kb, const void* vb, void* out, bool f32, uint8_t* ws,
+                       size_t off_g, size_t off_po, size_t off_pm, float scale,
+                       MainParams* prm_out) {
+  lf_status s = LF_OK;
+  const Plan* pl = &plan;
+  const Pattern* pat = &pattern;
+  const int D = pl->D, L = pat->L, H = pat->H, w = pat->w, n_g = pat->n_g;
+  const int BH = pl->B * H;
+  MainParams& P = *prm_out;
+  std::memset(&P, 0, sizeof(P));
+  for (int sl = 0; sl < pl->n_slots; ++sl) {
+    const int d = pl->slot_dil[sl];
+    P.dil[sl] = d;
+    if ((s = map_residue(ds, &P.tmQ[sl], qb, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &P.tmK[sl], kb, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &P.tmV[sl], vb, D, L, d, BH)) != LF_OK) return s;
+  }
+  const size_t g_elems = (size_t)BH * pl->NGQ * D;
+  uint16_t* qg = reinterpret_cast<uint16_t*>(ws + off_g);
+  uint16_t* kg = qg + g_elems;
+  uint16_t* vg = kg + g_elems;
+  if (n_g > 0) {
+    if ((s = map_rows(ds, &P.tmKp, kb, D, L, BH, lf::kBN)) != LF_OK) return s;
+    if ((s = map_rows(ds, &P.tmVp, vb, D, L, BH, lf::kBN)) != LF_OK) return s;
+    if ((s = map_rows(ds, &P.tmQg, qg, D, pl->NGQ, BH, lf::kBM)) != LF_OK) return s;
+    if ((s = map_rows(ds, &P.tmKg, kg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+    if ((s = map_rows(ds, &P.tmVg, vg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+  }
+  P.items = pl->d_items;
+  P.n_items = (int)pl->items.size();
+  P.gidx = pat->d_G;
+  P.is_glob = pat->d_isg;
+  P.n_g = n_g;
+  P.NGB = pl->NGB;
+  P.NGQ = pl->NGQ;
+  P.n_chunks = pl->n_chunks;
+  P.out = out;
+  P.out_f32 = f32 ? 1 : 0;
+  P.part_o = reinterpret_cast<float*>(ws + off_po);
+  P.part_ml = reinterpret_cast<float*>(ws + off_pm);
+  P.H = H;
+  P.L = L;
+  P.w = w;
+  P.sl2 = scale * 1.4426950408889634f;
+  P.status = ds->status;
+  P.timeout_ns = wait_timeout_ns();
+
+  return LF_OK;
+}
+
 lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool f32, int B, int H,
                    int L, int D, int w, const int32_t* dilation, const int32_t* gidx, int n_g,
                    float scale, cudaStream_t stream) {
@@ -484,15 +571,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   const size_t off_pm = off;
   if (n_g > 0) off += align_up(n_part * 2 * 4, 256);
   uint8_t* ws = nullptr;
-  if (off > 0) LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&ws), off, stream));
-
-  struct Freer {
-    uint8_t* p;
-    cudaStream_t s;
-    ~Freer() {
-      if (p) cudaFreeAsync(p, s);
-    }
-  } freer{ws, stream};
+  if (off > 0 && (s = get_workspace(dev, stream, off, &ws)) != LF_OK) return s;
 
   const void *qb = q, *kb = k, *vb = v;
   if (f32) {
@@ -512,43 +591,27 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
     vb = cq + 2 * elems;
   }
 
-  MainParams prm;
-  std::memset(&prm, 0, sizeof(prm));
-  for (int sl = 0; sl < pl->n_slots; ++sl) {
-    const int d = pl->slot_dil[sl];
-    prm.dil[sl] = d;
-    if ((s = map_residue(ds, &prm.tmQ[sl], qb, D, L, d, BH)) != LF_OK) return s;
-    if ((s = map_residue(ds, &prm.tmK[sl], kb, D, L, d, BH)) != LF_OK) return s;
-    if ((s = map_residue(ds, &prm.tmV[sl], vb, D, L, d, BH)) != LF_OK) return s;
+  const ParamKey pkey{pl, qb, kb, vb, out, f32, ws, scale};
+  MainParams* cached = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_params.find(pkey);
+    if (it != g_params.end()) cached = it->second.get();
   }
   uint16_t* qg = reinterpret_cast<uint16_t*>(ws + off_g);
   uint16_t* kg = qg + g_elems;
   uint16_t* vg = kg + g_elems;
-  if (n_g > 0) {
-    if ((s = map_rows(ds, &prm.tmKp, kb, D, L, BH, lf::kBN)) != LF_OK) return s;
-    if ((s = map_rows(ds, &prm.tmVp, vb, D, L, BH, lf::kBN)) != LF_OK) return s;
-    if ((s = map_rows(ds, &prm.tmQg, qg, D, pl->NGQ, BH, lf::kBM)) != LF_OK) return s;
-    if ((s = map_rows(ds, &prm.tmKg, kg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
-    if ((s = map_rows(ds, &prm.tmVg, vg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+  if (cached == nullptr) {
+    auto fresh = std::make_unique<MainParams>();
+    if ((s = build_params(ds, *pl, *pat, qb, kb, vb, out, f32, ws, off_g, off_po, off_pm, scale,
+                          fresh.get())) != LF_OK)
+      return s;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_params.size() >= kMaxCachedParams) g_params.clear();
+    cached = fresh.get();
+    g_params[pkey] = std::move(fresh);
   }
-  prm.items = pl->d_items;
-  prm.n_items = (int)pl->items.size();
-  prm.gidx = pat->d_G;
-  prm.is_glob = pat->d_isg;
-  prm.n_g = n_g;
-  prm.NGB = pl->NGB;
-  prm.NGQ = pl->NGQ;
-  prm.n_chunks = pl->n_chunks;
-  prm.out = out;
-  prm.out_f32 = f32 ? 1 : 0;
-  prm.part_o = reinterpret_cast<float*>(ws + off_po);
-  prm.part_ml = reinterpret_cast<float*>(ws + off_pm);
-  prm.H = H;
-  prm.L = L;
-  prm.w = w;
-  prm.sl2 = scale * 1.4426950408889634f;
-  prm.status = ds->status;
-  prm.timeout_ns = wait_timeout_ns();
+  const MainParams& prm = *cached;
 
   if (n_g > 0) {
     const size_t total = (size_t)BH * pl->NGQ * (D / 8);
@@ -927,6 +990,10 @@ lf_status lf_attn_get_status(lf_stream_t stream) {
 void lf_plan_cache_clear(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   cudaDeviceSynchronize();
+  g_params.clear();
+  for (auto& kv : g_workspaces)
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+  g_workspaces.clear();
   for (auto& kv : g_plans)
     if (kv.second->d_items) cudaFree(kv.second->d_items);
   g_plans.clear();

@@ -61,8 +61,8 @@
 #include "lf_common.cuh"
 #include "lf_ptx.cuh"
 
-#ifndef LF_FULLROW
-#define LF_FULLROW 0       // 1: softmax over the whole 128-key block at once
+#ifndef LF_SLOT_OFFSET
+#define LF_SLOT_OFFSET 1   // start slot 1 half a block after slot 0 (D = 64)
 #endif
 #ifndef LF_EMU16_D64
 #define LF_EMU16_D64 0     // exponentials per 16 columns done on the FMA pipe (D = 64)
@@ -126,28 +126,51 @@ static_assert(8 * KCfg<128>::REGS_SOFTMAX + 4 * KCfg<128>::REGS_OTHER <= 12 * kR
 struct Waiter {
   volatile int* abort;
   unsigned* status;
-  unsigned long long timeout_ns;
+  unsigned long long timeout_ns;   // host-set bound of every wait
 };
 
+// Bounded wait for an mbarrier phase.  Each try_wait suspends the thread for
+// at most kWaitSliceNs, so the iteration cap bounds the wait at about the
+// host-set timeout.  On expiry (or when another role has given up, if
+// honour_abort) it records the timeout and returns false.  Kept small: it is
+// inlined at every wait site.
+constexpr uint32_t kWaitSliceNs = 1024;
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
-                                       bool honour_abort) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (honour_abort && *w.abort) return false;
-      if (globaltimer_ns() - t0 > w.timeout_ns || it > (1u << 28)) {
-        *w.abort = 1;
-        atomicOr(w.status, kStatusTimeout);
-        return false;
-      }
-    }
+                                          bool honour_abort) {
+  const uint32_t cap = (uint32_t)(w.timeout_ns / kWaitSliceNs) + 1u;
+  for (uint32_t it = 0; it < cap; ++it) {
+    if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return true;
+    if (honour_abort && (it & 255u) == 255u && *w.abort) return false;
   }
+  *w.abort = 1;
+  atomicOr(w.status, kStatusTimeout);
+  return false;
 }
 
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const Waiter& w) {
-  if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(bar, parity, w, true);
+}
+
+// O_X += P_X V of one block, issued once its P is written (and, for the first
+// block of an item, once the epilogue has read O_X of the previous item).
+// Out of line: the issuer calls it from several places.
+template <int D>
+__device__ __noinline__ bool issue_pv_block(uint32_t b0, int X, uint32_t sV, uint32_t to,
+                                            uint32_t tp, uint32_t id_pv, int stage, int kext,
+                                            bool first, uint32_t item, uint32_t kP,
+                                            const Waiter& W) {
+  using C = KCfg<D>;
+  auto BAR = [&](int idx) -> uint32_t { return b0 + 8u * idx; };
+  if (first && item > 0 && !bwait(BAR(C::B_OE + X), (item - 1) & 1, W)) return false;
+  if (!bwait(BAR(C::B_PF + X), kP & 1, W)) return false;
+  tc_fence_after();
+  const uint32_t vb = sV + stage * C::KVB;
+  for (int kk = 0; kk < kext / 16; ++kk)
+    mma_ts(to, tp + kk * 8, sdesc_sw128(vb + kk * 2048u, C::HALF, 1024), id_pv,
+           (!first || kk > 0) ? 1u : 0u);
+  mma_commit(BAR(C::B_PV + X));
+  mma_commit(BAR(C::B_KE + stage));
+  return true;
 }
 
 template <int D>
@@ -298,8 +321,8 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
     // thread tens of cycles, more than a 128x64x16 product takes).
     // K/V stage b is released by one arrival per slot: the slot's PV commit
     // if it uses the block, else a plain arrival once the block is loaded.
-    auto issuer = [&](auto XC) {
-      constexpr int X = decltype(XC)::value;
+    {
+      const int X = warp - 9;
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_g = idesc_bf16(128, p.NGB, false);
       const uint32_t id_pv = idesc_bf16(128, D, true);
@@ -311,20 +334,20 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       int p_stage = 0, p_kext = 0;
       uint32_t p_nb = 0, p_item = 0;
       bool ok = true;
+      // Slot 1 starts half a block after slot 0 (its first S waits until slot
+      // 0 has read its first S), so that the two softmax warps sharing each
+      // SM sub-partition work out of phase: one exponentiates while the
+      // other loads and reduces.
+      if (LF_SLOT_OFFSET && !C::P_ALIAS && X == 1 && blockIdx.x < p.n_items &&
+          blk_count(p.items[blockIdx.x], 0) > 0 && !bwait(BAR(C::B_SR + 0), 0, W))
+        ok = false;
       // O_X += P_X V of the pending block, once its P is written
       auto issue_pv = [&]() -> bool {
-        if (p_first && p_item > 0 && !bwait(BAR(C::B_OE + X), (p_item - 1) & 1, W)) return false;
-        if (!bwait(BAR(C::B_PF + X), kP & 1, W)) return false;
-        tc_fence_after();
-        const uint32_t vb = sV + p_stage * C::KVB;
-        for (int kk = 0; kk < p_kext / 16; ++kk)
-          mma_ts(to, tp + kk * 8, sdesc_sw128(vb + kk * 2048u, C::HALF, 1024), id_pv,
-                 (!p_first || kk > 0) ? 1u : 0u);
-        mma_commit(BAR(C::B_PV + X));
-        mma_commit(BAR(C::B_KE + p_stage));
+        const bool r = issue_pv_block<D>(b0, X, sV, to, tp, id_pv, p_stage, p_kext, p_first,
+                                         p_item, kP, W);
         ++kP;
         pend = false;
-        return true;
+        return r;
       };
       for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
         const WorkItem wi = p.items[it];
@@ -388,9 +411,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
         mma_commit(BAR(C::B_DR + X));
         wait_slow(BAR(C::B_DR + X), 0, W, false);
       }
-    };
-    if (warp == 9) issuer(std::integral_constant<int, 0>{});
-    else issuer(std::integral_constant<int, 1>{});
+    }
     }
     // teardown (this warpgroup): all TMEM traffic of the CTA is done after the barrier
     __syncwarp();
@@ -473,52 +494,62 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           mbar_arrive(BAR(C::B_PF + X));
           continue;
         }
-        // ---- this row's visible columns of the block, as four 32-bit words
-        uint32_t v0, v1, v2, v3;
+        bool all_full = false;
         if (j < wi.nkb) {
-          // band block / key chunk: the columns [clo, chi]
+          // interior blocks (every row sees all 128 keys) need no masks
           const int kpos0 = wi.kb0 + kBN * j;
-          const int clo = wlo - kpos0, chi1 = whi - kpos0 + 1;
-          v0 = range_bits(clo, chi1, 0);
-          v1 = range_bits(clo, chi1, 32);
-          v2 = range_bits(clo, chi1, 64);
-          v3 = range_bits(clo, chi1, 96);
-        } else {
-          // gathered globals G[gbase + c]: not the padding, and not a global
-          // already in the row's window (columns [c_lo, c_hi) hold G[ga .. gz);
-          // for dilated heads only those on the row's residue class are in
-          // band(i): the off bits mark the others)
-          const int gbase = (j - wi.nkb) * p.NGB;
-          const int c_lo = ga - gbase, c_hi = gz - gbase, nvalid = p.n_g - gbase;
-          uint32_t off0 = 0, off1 = 0, off2 = 0, off3 = 0;
-          if (d > 1) {
-            const int cb = c_lo > 0 ? c_lo : 0, ce = c_hi < p.NGB ? c_hi : p.NGB;
-            for (int c = cb; c < ce; ++c) {
-              const int diff = __ldg(p.gidx + gbase + c) - i;
-              if (diff % d != 0) {
-                const uint32_t bit = 1u << (c & 31);
-                const int wsel = c >> 5;
-                off0 |= wsel == 0 ? bit : 0u;
-                off1 |= wsel == 1 ? bit : 0u;
-                off2 |= wsel == 2 ? bit : 0u;
-                off3 |= wsel == 3 ? bit : 0u;
+          all_full = __reduce_max_sync(FULL, wlo - kpos0) <= 0 &&
+                     __reduce_min_sync(FULL, whi - kpos0) >= kBN - 1;
+        }
+        // this row's visible columns as four 32-bit words, and the warp-wide
+        // classes of the 16-key chunks: seen by some row (vis) / by every row
+        // (full)
+        uint32_t v0 = ~0u, v1 = ~0u, v2 = ~0u, v3 = ~0u;
+        uint32_t vis = 0xFFu, full = 0xFFu;
+        if (!all_full) {
+          if (j < wi.nkb) {
+            // band block / key chunk: the columns [clo, chi]
+            const int kpos0 = wi.kb0 + kBN * j;
+            const int clo = wlo - kpos0, chi1 = whi - kpos0 + 1;
+            v0 = range_bits(clo, chi1, 0);
+            v1 = range_bits(clo, chi1, 32);
+            v2 = range_bits(clo, chi1, 64);
+            v3 = range_bits(clo, chi1, 96);
+          } else {
+            // gathered globals G[gbase + c]: not the padding, and not a global
+            // already in the row's window (columns [c_lo, c_hi) hold
+            // G[ga .. gz); for dilated heads only those on the row's residue
+            // class are in band(i): the off bits mark the others)
+            const int gbase = (j - wi.nkb) * p.NGB;
+            const int c_lo = ga - gbase, c_hi = gz - gbase, nvalid = p.n_g - gbase;
+            uint32_t off0 = 0, off1 = 0, off2 = 0, off3 = 0;
+            if (d > 1) {
+              const int cb = c_lo > 0 ? c_lo : 0, ce = c_hi < p.NGB ? c_hi : p.NGB;
+#pragma unroll 1
+              for (int c = cb; c < ce; ++c) {
+                const int diff = __ldg(p.gidx + gbase + c) - i;
+                if (diff % d != 0) {
+                  const uint32_t bit = 1u << (c & 31);
+                  const int wsel = c >> 5;
+                  off0 |= wsel == 0 ? bit : 0u;
+                  off1 |= wsel == 1 ? bit : 0u;
+                  off2 |= wsel == 2 ? bit : 0u;
+                  off3 |= wsel == 3 ? bit : 0u;
+                }
               }
             }
+            v0 = range_bits(0, nvalid, 0) & ~(range_bits(c_lo, c_hi, 0) & ~off0);
+            v1 = range_bits(0, nvalid, 32) & ~(range_bits(c_lo, c_hi, 32) & ~off1);
+            v2 = range_bits(0, nvalid, 64) & ~(range_bits(c_lo, c_hi, 64) & ~off2);
+            v3 = range_bits(0, nvalid, 96) & ~(range_bits(c_lo, c_hi, 96) & ~off3);
           }
-          v0 = range_bits(0, nvalid, 0) & ~(range_bits(c_lo, c_hi, 0) & ~off0);
-          v1 = range_bits(0, nvalid, 32) & ~(range_bits(c_lo, c_hi, 32) & ~off1);
-          v2 = range_bits(0, nvalid, 64) & ~(range_bits(c_lo, c_hi, 64) & ~off2);
-          v3 = range_bits(0, nvalid, 96) & ~(range_bits(c_lo, c_hi, 96) & ~off3);
-        }
-        // warp-wide classes of the 16-key chunks: seen by some row (vis) /
-        // by every row (full); S_X is read up to the last half any row sees
-        uint32_t vis = 0, full = 0;
-        {
           const uint32_t o0 = __reduce_or_sync(FULL, v0), o1 = __reduce_or_sync(FULL, v1);
           const uint32_t o2 = __reduce_or_sync(FULL, v2), o3 = __reduce_or_sync(FULL, v3);
           const uint32_t a0 = __reduce_and_sync(FULL, v0), a1 = __reduce_and_sync(FULL, v1);
           const uint32_t a2 = __reduce_and_sync(FULL, v2), a3 = __reduce_and_sync(FULL, v3);
           const uint32_t ow[4] = {o0, o1, o2, o3}, aw[4] = {a0, a1, a2, a3};
+          vis = 0;
+          full = 0;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint32_t oh = (ow[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
@@ -528,7 +559,6 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           }
         }
         const bool live0 = (vis & 0x0Fu) != 0u, live1 = (vis & 0xF0u) != 0u;
-
         // P_X (and O_X) are free once the previous O += P V of this slot has
         // completed; that is awaited just before the first write (for
         // D = 128, S_X(k) was issued after PV_X(k-1), so it already has)
@@ -541,97 +571,13 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           tc_fence_after();
           return true;
         };
+
         if (!C::P_ALIAS && !live0 && !live1) {
           tc_fence_before();
           mbar_arrive(BAR(C::B_SR + X));
         }
 
-#if LF_FULLROW
-        // ---- the whole block (128 keys) at once: load, mask, max, exp, store P
-        {
-          const float2 sl2v = make_float2(sl2, sl2);
-          float s[128];
-          {
-            uint32_t r[128];
-            tmem_ld128(tS, r);
-#pragma unroll
-            for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
-          }
-          if (!C::P_ALIAS && (live0 || live1)) {
-            tc_fence_before();
-            mbar_arrive(BAR(C::B_SR + X));
-          }
-          // mask the chunks not every row sees (chunks no row sees entirely)
-          if (full != 0xFFu) {
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              if (full & (1u << ch)) continue;
-              if (!(vis & (1u << ch))) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) s[16 * ch + e] = NEG_INF;
-              } else {
-                const uint32_t vw = ch < 4 ? (ch < 2 ? v0 : v1) : (ch < 6 ? v2 : v3);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const int bit = 16 * (ch & 1) + e;
-                  s[16 * ch + e] = (vw & (1u << bit)) ? s[16 * ch + e] : NEG_INF;
-                }
-              }
-            }
-          }
-          // running max (log2 units); a rare rescale of O when it grows by
-          // more than 2^8
-          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-          for (int e = 0; e < 128; e += 2)
-            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
-          const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-          const bool need = mxs > m_ref + 8.0f;
-          const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
-          if (__any_sync(FULL, need && m_ref != NEG_INF) && !firstblk) {
-            if (!await_pfree()) { ok = false; break; }
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t r[32];
-              tmem_ld32(tO + c0, r);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(tO + c0, r);
-            }
-            tmem_st_wait();
-          }
-          l *= alpha;
-          if (need) m_ref = mxs;
-          const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
-          const float2 nmu = make_float2(-mu, -mu);
-          // P = 2^(s*sl2 - m) over the 128 keys (masked ones give 0), its row
-          // sum, bf16 pairs stored 32 keys at a time
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int c = 32 * g + e;
-              const float2 x = fma2(make_float2(s[c], s[c + 1]), sl2v, nmu);
-              float2 pv;
-              if ((e & 15) < C::EMU16) {
-                pv = exp2_poly2(x);
-              } else {
-                pv.x = ex2_approx(x.x);
-                pv.y = ex2_approx(x.y);
-              }
-              acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
-              pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
-            }
-            if (g == 0 && !await_pfree()) { ok = false; break; }
-            tmem_st16(tP + 16 * g, pk);
-          }
-          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-        }
-#else
-        // ---- two halves of 64 keys: load, mask, max, exp, store P
+        // ---- two halves of 64 keys: load, mask, exponentials, row sum, P
         const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -677,63 +623,78 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             }
           }
 
-          // running max (log2 units); a rare rescale of O (and of P's first
-          // half) when it grows by more than 2^8
-          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
-          const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-          const bool need = mxs > m_ref + 8.0f;
-          const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
-          if (__any_sync(FULL, need && m_ref != NEG_INF)) {
-            if (!await_pfree()) { ok = false; break; }
-            if (!firstblk) {
-#pragma unroll 1
-              for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tO + c0, r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                tmem_st32(tO + c0, r);
-              }
-            }
-            if (hf == 1 && live0) {
-              uint32_t r[32];
-              tmem_st_wait();
-              tmem_ld32(tP, r);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float lo = __uint_as_float(r[e] << 16), hi = __uint_as_float(r[e] & 0xffff0000u);
-                r[e] = pack_bf16x2(lo * alpha, hi * alpha);
-              }
-              tmem_st32(tP, r);
-            }
-            tmem_st_wait();
-          }
-          l *= alpha;
-          if (need) m_ref = mxs;
-          const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
-          const float2 nmu = make_float2(-mu, -mu);
-
-          // P = 2^(s*sl2 - m) over all 64 keys (masked ones give 0), its row
-          // sum, and bf16 pairs
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
+          // Exponentials relative to the row's reference m_ref.  The row max is
+          // only computed when a row has no reference yet (first visible
+          // keys) or when the speculative pass finds a score far above it
+          // (the half's sum exceeds 2^16): then the reference moves, O (and
+          // P's first half) are rescaled, and the half is redone.
+          bool do_max = __any_sync(FULL, m_ref == NEG_INF);
+          float2 acc[4];
           uint32_t pk[32];
+#pragma unroll 1
+          for (int pass = 0; pass < 2; ++pass) {
+            if (do_max) {
+              float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float2 x = fma2(make_float2(s[e], s[e + 1]), sl2v, nmu);
-            float2 pv;
-            if ((e & 15) < C::EMU16) {
-              pv = exp2_poly2(x);
-            } else {
-              pv.x = ex2_approx(x.x);
-              pv.y = ex2_approx(x.y);
+              for (int e = 0; e < 64; e += 2)
+                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
+              const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+              const bool need = mxs > m_ref + 8.0f;
+              const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
+              if (__any_sync(FULL, need && m_ref != NEG_INF)) {
+                if (!await_pfree()) { ok = false; break; }
+                if (!firstblk) {
+#pragma unroll 1
+                  for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c0, r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(tO + c0, r);
+                  }
+                }
+                if (hf == 1 && live0) {
+                  uint32_t r[32];
+                  tmem_st_wait();
+                  tmem_ld32(tP, r);
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) {
+                    const float lo = __uint_as_float(r[e] << 16), hi = __uint_as_float(r[e] & 0xffff0000u);
+                    r[e] = pack_bf16x2(lo * alpha, hi * alpha);
+                  }
+                  tmem_st32(tP, r);
+                }
+                tmem_st_wait();
+              }
+              l *= alpha;
+              if (need) m_ref = mxs;
             }
-            acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
-            pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
+            const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+            const float2 nmu = make_float2(-mu, -mu);
+            // P = 2^(s*sl2 - m) over all 64 keys (masked ones give 0), its
+            // sum, and bf16 pairs
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              const float2 x = fma2(make_float2(s[e], s[e + 1]), sl2v, nmu);
+              float2 pv;
+              if ((e & 15) < C::EMU16) {
+                pv = exp2_poly2(x);
+              } else {
+                pv.x = ex2_approx(x.x);
+                pv.y = ex2_approx(x.y);
+              }
+              acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+              pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
+            }
+            if (do_max) break;
+            const float lh = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                             ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+            if (!__any_sync(FULL, !(lh <= 65536.0f))) break;
+            do_max = true;
           }
+          if (!ok) break;
           if (!await_pfree()) { ok = false; break; }
           {
             uint32_t a[16], b2[16];
@@ -744,7 +705,6 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           }
           l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
         }
-#endif
         if (!ok) break;
         firstblk = false;
         tmem_st_wait();

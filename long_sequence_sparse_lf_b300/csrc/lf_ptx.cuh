@@ -45,6 +45,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// true once the phase with the given parity has completed; the thread may
+// be suspended for up to about `hint_ns` nanoseconds while it is pending
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // non-blocking: true if the phase with the given parity has completed
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -227,6 +242,20 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
+// 64 consecutive columns starting at taddr, without waiting: the registers
+// are valid only after tmem_wait_ld_pin on them.
+__device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%64];"
+      : LF_R8(0), LF_R8(8), LF_R8(16), LF_R8(24), LF_R8(32), LF_R8(40), LF_R8(48), LF_R8(56)
+      : "r"(taddr)
+      : "memory");
+}
+
 // 128 consecutive columns starting at taddr; waits for completion.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -248,6 +277,29 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 }
 
 #undef LF_R8
+
+#define LF_P8(b) "+r"(r[b + 0]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), \
+                 "+r"(r[b + 4]), "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
+
+// Waits for this thread's outstanding TMEM loads; the registers of `r` are
+// tied to the wait, so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_pin(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : LF_P8(0), LF_P8(8), LF_P8(16), LF_P8(24), LF_P8(32), LF_P8(40), LF_P8(48), LF_P8(56)
+               :
+               : "memory");
+}
+
+// Ties the registers of `r` to this point of the program (after an earlier
+// tmem_wait_ld_pin), for loads that the same wait completed.
+__device__ __forceinline__ void regs_pin(uint32_t (&r)[64]) {
+  asm volatile(""
+               : LF_P8(0), LF_P8(8), LF_P8(16), LF_P8(24), LF_P8(32), LF_P8(40), LF_P8(48), LF_P8(56)
+               :
+               : "memory");
+}
+
+#undef LF_P8
 
 #define LF_W8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), \
                  "r"(r[b + 4]), "r"(r[b + 5]), "r"(r[b + 6]), "r"(r[b + 7])
@@ -306,7 +358,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // Packed pair arithmetic on the FMA pipe (one instruction for two fp32
 // lanes; sm_100 family).
+#ifndef LF_PACKED_F32X2
+#define LF_PACKED_F32X2 1
+#endif
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+#if LF_PACKED_F32X2
   float2 r;
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
       "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
@@ -314,9 +370,13 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       : "=f"(r.x), "=f"(r.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
+#else
+  return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+#endif
 }
 
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
+#if LF_PACKED_F32X2
   float2 r;
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
       "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
@@ -324,6 +384,9 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
       : "=f"(r.x), "=f"(r.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
+#else
+  return make_float2(a.x + b.x, a.y + b.y);
+#endif
 }
 
 // 2^x for a pair of arguments x <= 8 on the FMA pipe instead of the
