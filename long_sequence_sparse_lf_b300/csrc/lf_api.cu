@@ -17,6 +17,7 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -208,8 +209,11 @@ struct Plan {
   int slot_dil[lf::kMaxDilSlots] = {0};
   std::vector<int> head_slot;
   int NGB = 16, NGQ = 0, n_gblk = 0, n_chunks = 0;
-  std::vector<WorkItem> items;
-  WorkItem* d_items = nullptr;
+  std::vector<WorkItem> items;     // grouped by CTA (see cta_begin)
+  std::vector<int> cta_begin;      // [grid + 1] item ranges per CTA
+  int grid = 0;                    // CTAs of the attention kernel
+  WorkItem* d_items = nullptr;     // device copy of items, then cta_begin
+  int* d_cta = nullptr;
 };
 
 using PatKey = std::tuple<int, int, int, int, std::vector<int32_t>, std::vector<int32_t>>;
@@ -249,13 +253,30 @@ lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const in
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Work list of the attention kernel (see WorkItem): band pairs of
-// neighbouring 128-query tiles per (b, h, residue class), then the
-// global-row chunks; longest first.
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Work list of the attention kernel (see WorkItem): for each (b, h), its
+// band pairs of neighbouring 128-query tiles (per residue class), then its
+// global-row chunks, so that a head's keys are still in L2 when the global
+// rows read them.  The items are then spread over the CTAs longest first,
+// each to the least-loaded CTA (a cost per item = the blocks of its busier
+// slot, gathered blocks weighted by their width, plus one for the item's
+// own loads and epilogue), and stored grouped by CTA.
+int item_cost(const WorkItem& wi, int NGB) {
+  int c[2];
+  for (int X = 0; X < 2; ++X) {
+    const int n = lf::blk_count(wi, X);
+    if (wi.kind == 0 && n > 0)
+      c[X] = 8 * (n - wi.ngb) + (wi.ngb * NGB + 15) / 16;   // eighths of a block
+    else
+      c[X] = 8 * n;
+  }
+  return std::max(c[0], c[1]) + 8;
+}
+
 void build_items(Plan& pl, int num_sms) {
   const Pattern& pt = *pl.pat;
   const int H = pt.H, L = pt.L, w = pt.w, n_g = pt.n_g;
-  (void)num_sms;
   // global key blocks folded into every band tile
   if (n_g > 0) {
     pl.NGB = n_g <= lf::kBN ? ((n_g + 15) / 16) * 16 : lf::kBN;
@@ -266,9 +287,26 @@ void build_items(Plan& pl, int num_sms) {
     pl.n_gblk = 0;
     pl.NGQ = 0;
   }
-  std::vector<WorkItem>& items = pl.items;
-  items.clear();
-  int pair_cost = 0;
+  // key-chunk length of the global-row items: about half a band pair's
+  // blocks, so that they also fill the tail of the schedule
+  int pair_blocks = 0;
+  for (int h = 0; h < H; ++h) {
+    const int d = pt.dil[h];
+    const int Lr = lf::residue_len(L, d, 0);
+    const int span = std::min(2 * lf::kBM + 2 * w, Lr);
+    pair_blocks = std::max(pair_blocks, ceil_div(span, lf::kBN) + pl.n_gblk);
+  }
+  const int nblocks = ceil_div(L, lf::kBN);
+  int n_items1 = 0, CB = 0;
+  if (n_g > 0) {
+    CB = std::max(2, std::min(nblocks, pair_blocks));
+    n_items1 = ceil_div(nblocks, CB);
+    CB = ceil_div(nblocks, n_items1);   // even out the chunks
+    pl.n_chunks = 2 * n_items1;
+  } else {
+    pl.n_chunks = 0;
+  }
+  std::vector<WorkItem> order;
   for (int b = 0; b < pl.B; ++b) {
     for (int h = 0; h < H; ++h) {
       const int bh = b * H + h;
@@ -312,43 +350,56 @@ void build_items(Plan& pl, int num_sms) {
               wi.jhi[X] = 0;
             }
           }
-          pair_cost = std::max(pair_cost, lf::blk_count(wi, 0) + lf::blk_count(wi, 1));
-          items.push_back(wi);
+          order.push_back(wi);
         }
       }
+      for (int gt = 0; gt < pl.NGQ / lf::kBM; ++gt)
+        for (int c = 0; c < n_items1; ++c) {
+          WorkItem wi{};
+          wi.bh = bh;
+          wi.kind = 1;
+          wi.r = gt;
+          wi.t0 = 0;
+          wi.kb0 = c * CB * lf::kBN;
+          wi.nkb = std::min(CB, nblocks - c * CB);
+          wi.ngb = 0;
+          wi.slot = c;
+          wi.jlo[0] = wi.jlo[1] = 0;
+          wi.jhi[0] = wi.jhi[1] = -1;
+          order.push_back(wi);
+        }
     }
   }
-  if (n_g > 0) {
-    // chunks of CB key blocks, about one band pair's worth of blocks each
-    const int nblocks = ceil_div(L, lf::kBN);
-    int CB = std::max(2, std::min(nblocks, pair_cost > 0 ? pair_cost : nblocks));
-    const int n_items1 = ceil_div(nblocks, CB);
-    CB = ceil_div(nblocks, n_items1);   // even out the chunks
-    pl.n_chunks = 2 * n_items1;
-    for (int b = 0; b < pl.B; ++b)
-      for (int h = 0; h < H; ++h)
-        for (int gt = 0; gt < pl.NGQ / lf::kBM; ++gt)
-          for (int c = 0; c < n_items1; ++c) {
-            WorkItem wi{};
-            wi.bh = b * H + h;
-            wi.kind = 1;
-            wi.r = gt;
-            wi.t0 = 0;
-            wi.kb0 = c * CB * lf::kBN;
-            wi.nkb = std::min(CB, nblocks - c * CB);
-            wi.ngb = 0;
-            wi.slot = c;
-            wi.jlo[0] = wi.jlo[1] = 0;
-            wi.jhi[0] = wi.jhi[1] = -1;
-            items.push_back(wi);
-          }
-  } else {
-    pl.n_chunks = 0;
+  // longest first onto the least-loaded CTA
+  const int n = (int)order.size();
+  pl.grid = std::max(1, std::min(n, num_sms));
+  std::vector<int> idx(n);
+  std::vector<int> cost(n);
+  for (int x = 0; x < n; ++x) {
+    idx[x] = x;
+    cost[x] = item_cost(order[x], pl.NGB);
   }
-  // longest first (stable: neighbouring tiles stay together for L2 reuse)
-  std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) {
-    return lf::blk_count(a, 0) + lf::blk_count(a, 1) > lf::blk_count(b, 0) + lf::blk_count(b, 1);
-  });
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  std::vector<std::vector<int>> per_cta(pl.grid);
+  using Load = std::pair<long long, int>;   // (load, cta)
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < pl.grid; ++c) heap.push({0LL, c});
+  for (int x : idx) {
+    Load top = heap.top();
+    heap.pop();
+    per_cta[top.second].push_back(x);
+    top.first += cost[x];
+    heap.push(top);
+  }
+  pl.items.clear();
+  pl.items.reserve(n);
+  pl.cta_begin.assign(pl.grid + 1, 0);
+  for (int c = 0; c < pl.grid; ++c) {
+    // keep each CTA's items in list order (head by head, along the keys)
+    std::sort(per_cta[c].begin(), per_cta[c].end());
+    for (int x : per_cta[c]) pl.items.push_back(order[x]);
+    pl.cta_begin[c + 1] = (int)pl.items.size();
+  }
 }
 
 // Every block of an item must have a user: the kernel releases a K/V stage
@@ -390,10 +441,17 @@ lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pat
   }
   build_items(*pl, num_sms);
   if (!items_consistent(*pl)) return fail(LF_ERR_INVALID_ARG, "internal: inconsistent work list");
-  if (!pl->items.empty()) {
-    LF_CUDA(cudaMalloc(&pl->d_items, sizeof(WorkItem) * pl->items.size()));
-    LF_CUDA(cudaMemcpy(pl->d_items, pl->items.data(), sizeof(WorkItem) * pl->items.size(),
-                       cudaMemcpyHostToDevice));
+  {
+    const size_t ib = align_up(sizeof(WorkItem) * std::max<size_t>(pl->items.size(), 1), 256);
+    const size_t cb = sizeof(int) * pl->cta_begin.size();
+    uint8_t* dev_mem = nullptr;
+    LF_CUDA(cudaMalloc(reinterpret_cast<void**>(&dev_mem), ib + cb));
+    pl->d_items = reinterpret_cast<WorkItem*>(dev_mem);
+    pl->d_cta = reinterpret_cast<int*>(dev_mem + ib);
+    if (!pl->items.empty())
+      LF_CUDA(cudaMemcpy(pl->d_items, pl->items.data(), sizeof(WorkItem) * pl->items.size(),
+                         cudaMemcpyHostToDevice));
+    LF_CUDA(cudaMemcpy(pl->d_cta, pl->cta_begin.data(), cb, cudaMemcpyHostToDevice));
   }
   *out = pl.get();
   g_plans[key] = std::move(pl);
@@ -440,7 +498,6 @@ lf_status map_rows(DevState* ds, CUtensorMap* m, const void* base, int D, int ro
 
 // ------------------------------------------------------------------ forward
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Scratch of lf_attn_fwd / lf_attn_fwd_f32: one grow-only buffer per
 // (device, stream).  Calls on one stream are ordered, so they can share it;
@@ -508,6 +565,7 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
     if ((s = map_rows(ds, &P.tmVg, vg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
   }
   P.items = pl->d_items;
+  P.cta_begin = pl->d_cta;
   P.n_items = (int)pl->items.size();
   P.gidx = pat->d_G;
   P.is_glob = pat->d_isg;
@@ -627,7 +685,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
     });
   }
   if (prm.n_items > 0) {
-    const int grid = std::min(prm.n_items, ds->num_sms);
+    const int grid = pl->grid;
     traced("attn_main", stream, [&] {
       if (D == 64)
         lf::lf_attn_main_kernel<64><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
@@ -746,6 +804,8 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   size_t off = 0;
   const size_t off_items = off;
   off += align_up(sizeof(WorkItem) * std::max<size_t>(pl.items.size(), 1), 256);
+  const size_t off_cta = off;
+  off += align_up(sizeof(int) * pl.cta_begin.size(), 256);
   const size_t off_gidx = off;
   off += align_up(sizeof(int32_t) * std::max(n_g, 1), 256);
   const size_t off_isg = off;
@@ -770,11 +830,14 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   // every byte the kernels read is written first, by these copies or by the
   // gather kernel and the attention kernel's partial writes)
   WorkItem* d_items = reinterpret_cast<WorkItem*>(ws + off_items);
+  int* d_cta = reinterpret_cast<int*>(ws + off_cta);
   int32_t* d_gidx = reinterpret_cast<int32_t*>(ws + off_gidx);
   uint8_t* d_isg = ws + off_isg;
   if (!pl.items.empty())
     LF_CUDA(cudaMemcpyAsync(d_items, pl.items.data(), sizeof(WorkItem) * pl.items.size(),
                             cudaMemcpyHostToDevice, stream));
+  LF_CUDA(cudaMemcpyAsync(d_cta, pl.cta_begin.data(), sizeof(int) * pl.cta_begin.size(),
+                          cudaMemcpyHostToDevice, stream));
   if (n_g > 0)
     LF_CUDA(cudaMemcpyAsync(d_gidx, gidx, sizeof(int32_t) * n_g, cudaMemcpyHostToDevice, stream));
   LF_CUDA(cudaMemcpyAsync(d_isg, pl.pat->isg.data(), (size_t)L, cudaMemcpyHostToDevice, stream));
@@ -799,6 +862,7 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
     if ((s = map_rows(ds, &prm.tmVg, vg, D, pl.NGQ, BH, pl.NGB)) != LF_OK) return s;
   }
   prm.items = d_items;
+  prm.cta_begin = d_cta;
   prm.n_items = (int)pl.items.size();
   prm.gidx = d_gidx;
   prm.is_glob = d_isg;
@@ -830,7 +894,7 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   if (prm.n_items > 0) {
-    const int grid = std::min(prm.n_items, ds->num_sms);
+    const int grid = pl.grid;
     if (D == 64)
       lf::lf_attn_main_kernel<64><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
     else

@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   Waiter W{abort_flag, p.status, p.timeout_ns};
+  const int it_begin = p.cta_begin[blockIdx.x], it_end = p.cta_begin[blockIdx.x + 1];
 
   if (warp >= 8) {
     regs_dec<C::REGS_OTHER>();
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       uint32_t nb = 0;                 // K/V blocks armed
       uint32_t qn[2] = {0u, 0u};       // Q loads armed per slot
       bool ok = true;
-      for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      for (int it = it_begin; it < it_end && ok; ++it) {
         const WorkItem wi = p.items[it];
 #pragma unroll
         for (int X = 0; X < 2; ++X) {
@@ -338,8 +339,8 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       // 0 has read its first S), so that the two softmax warps sharing each
       // SM sub-partition work out of phase: one exponentiates while the
       // other loads and reduces.
-      if (LF_SLOT_OFFSET && !C::P_ALIAS && X == 1 && blockIdx.x < p.n_items &&
-          blk_count(p.items[blockIdx.x], 0) > 0 && !bwait(BAR(C::B_SR + 0), 0, W))
+      if (LF_SLOT_OFFSET && !C::P_ALIAS && X == 1 && it_begin < it_end &&
+          blk_count(p.items[it_begin], 0) > 0 && !bwait(BAR(C::B_SR + 0), 0, W))
         ok = false;
       // O_X += P_X V of the pending block, once its P is written
       auto issue_pv = [&]() -> bool {
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
         pend = false;
         return r;
       };
-      for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+      for (int it = it_begin; it < it_end && ok; ++it) {
         const WorkItem wi = p.items[it];
         const SlotBlocks sb(wi, X);
         const int nbt = wi.nkb + wi.ngb;
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
     const unsigned FULL = 0xffffffffu;
     uint32_t k = 0;   // blocks processed by this slot
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const WorkItem wi = p.items[it];
       const bool band = wi.kind == 0;
       const SlotBlocks sb(wi, X);

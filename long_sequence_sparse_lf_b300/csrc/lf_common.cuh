@@ -115,7 +115,8 @@ struct MainParams {
   CUtensorMap tmKg;                // gathered rows, box NGB rows
   CUtensorMap tmVg;
   int dil[kMaxDilSlots];           // dilation value of each slot
-  const WorkItem* items;
+  const WorkItem* items;           // grouped by CTA: CTA c runs items
+  const int* cta_begin;            //   [cta_begin[c], cta_begin[c+1]) in order
   int n_items;
   const int32_t* gidx;             // [n_g] sorted global positions
   const uint8_t* is_glob;          // [L] 1 where the position is global
