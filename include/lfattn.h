@@ -174,6 +174,16 @@ LF_API const char* lf_last_error(void);
  */
 LF_API lf_status lf_attn_get_status(lf_stream_t stream);
 
+/*
+ * lf_selftest_wait_timeout — exercises the device-side timeout path without
+ * a fault: one thread waits, with the attention kernel's bounded wait, on a
+ * barrier nothing completes; after about timeout_us microseconds (1 ..
+ * 1000000) it records the timeout and the kernel returns.  The next
+ * lf_attn_get_status on the stream then reports LF_ERR_TIMEOUT (and clears
+ * it); the context stays usable.
+ */
+LF_API lf_status lf_selftest_wait_timeout(int timeout_us, lf_stream_t stream);
+
 /* Frees every cached plan, cached call parameters and scratch buffer
  * (synchronises the device). */
 LF_API void lf_plan_cache_clear(void);

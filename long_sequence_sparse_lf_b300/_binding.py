@@ -62,6 +62,8 @@ def load_library() -> ctypes.CDLL:
     lib.lf_plan_cache_clear.restype = None
     lib.lf_launch_count.argtypes = []
     lib.lf_launch_count.restype = ctypes.c_uint64
+    lib.lf_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.lf_selftest_wait_timeout.restype = i32
     lib.lf_version.argtypes = []
     lib.lf_version.restype = i32
     lib.lf_profile_enable.argtypes = [i32]
@@ -236,6 +238,11 @@ def lf_last_error() -> str:
 def lf_attn_get_status(stream=None) -> int:
     """Synchronises the stream; returns the library status (0 = OK)."""
     return int(load_library().lf_attn_get_status(_stream_handle(stream)))
+
+
+def lf_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (see lfattn.h)."""
+    _check(load_library().lf_selftest_wait_timeout(int(timeout_us), _stream_handle(stream)))
 
 
 def lf_plan_cache_clear() -> None:

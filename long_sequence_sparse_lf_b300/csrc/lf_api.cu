@@ -1119,6 +1119,25 @@ lf_status lf_attn_fwd_noalloc(const void* q, const void* k, const void* v, void*
   }
 }
 
+lf_status lf_selftest_wait_timeout(int timeout_us, lf_stream_t stream) {
+  try {
+    t_last_error.clear();
+    if (timeout_us < 1 || timeout_us > 1000000)
+      return fail(LF_ERR_INVALID_ARG, "timeout_us=%d not in [1, 1000000]", timeout_us);
+    DevState* ds = nullptr;
+    int dev = 0;
+    lf_status s = get_dev(&ds, &dev);
+    if (s != LF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    lf::lf_selftest_wait_kernel<<<1, 32, 0, st>>>(ds->status, 1000ull * (unsigned)timeout_us);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    LF_CUDA(cudaGetLastError());
+    return LF_OK;
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
 int lf_version(void) { return 100; }
 
 }  // extern "C"

@@ -151,6 +151,35 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const Waite
   return wait_slow(bar, parity, w, true);
 }
 
+// Wait for the asynchronous copies / products a role has in flight before
+// its CTA exits after an abort.  Bounded by a fixed 2 s, independent of the
+// host-set timeout: in-flight TMA and tensor-core work always completes, and
+// a short host timeout must not let the CTA leave before it does.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  constexpr uint32_t kDrainIters = 2000000000u / kWaitSliceNs;
+  for (uint32_t it = 0; it < kDrainIters; ++it)
+    if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return;
+}
+
+// Self-test of the bounded wait: one thread waits, with the attention
+// kernel's own wait code, on an mbarrier that nothing arrives at; the wait
+// runs out after about timeout_ns and records kStatusTimeout.  No copy or
+// tensor-core work is in flight, so the kernel then simply returns.
+__global__ void lf_selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const Waiter w{&abort_flag, status, timeout_ns};
+    (void)bwait(smem_u32(&bar), 0, w);
+  }
+}
+
 // O_X += P_X V of one block, issued once its P is written (and, for the first
 // block of an item, once the epilogue has read O_X of the previous item).
 // Out of line: the issuer calls it from several places.
@@ -307,10 +336,10 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       if (!ok) {
         // drain: the last load armed on every buffer completes before the CTA exits
         for (uint32_t n = (nb > (uint32_t)C::NST ? nb - C::NST : 0u); n < nb; ++n)
-          wait_slow(BAR(C::B_KF + n % C::NST), (n / C::NST) & 1, W, false);
+          drain_wait(BAR(C::B_KF + n % C::NST), (n / C::NST) & 1);
         for (int X = 0; X < 2; ++X)
           for (uint32_t t = (qn[X] > (uint32_t)C::NQ ? qn[X] - C::NQ : 0u); t < qn[X]; ++t)
-            wait_slow(BAR(C::B_QF + X * C::NQ + t % C::NQ), (t / C::NQ) & 1, W, false);
+            drain_wait(BAR(C::B_QF + X * C::NQ + t % C::NQ), (t / C::NQ) & 1);
       }
     }
     } else if ((warp == 9 || warp == 10) && lane == 0) {
@@ -410,7 +439,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       if (ok && pend && !issue_pv()) ok = false;
       if (!ok) {
         mma_commit(BAR(C::B_DR + X));
-        wait_slow(BAR(C::B_DR + X), 0, W, false);
+        drain_wait(BAR(C::B_DR + X), 0);
       }
     }
     }
