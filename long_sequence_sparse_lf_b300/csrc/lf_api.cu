@@ -582,7 +582,7 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
   P.w = w;
   P.sl2 = scale * 1.4426950408889634f;
   P.status = ds->status;
-  P.timeout_ns = wait_timeout_ns();
+  P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
   return LF_OK;
 }
@@ -879,7 +879,7 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   prm.w = w;
   prm.sl2 = scale * 1.4426950408889634f;
   prm.status = ds->status;
-  prm.timeout_ns = wait_timeout_ns();
+  prm.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
   if (n_g > 0) {
     const size_t total = (size_t)BH * pl.NGQ * (D / 8);
@@ -1129,7 +1129,8 @@ lf_status lf_selftest_wait_timeout(int timeout_us, lf_stream_t stream) {
     lf_status s = get_dev(&ds, &dev);
     if (s != LF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    lf::lf_selftest_wait_kernel<<<1, 32, 0, st>>>(ds->status, 1000ull * (unsigned)timeout_us);
+    lf::lf_selftest_wait_kernel<<<1, 32, 0, st>>>(ds->status,
+                                                 lf::wait_iters_for(1000ull * (unsigned)timeout_us));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     LF_CUDA(cudaGetLastError());
     return LF_OK;

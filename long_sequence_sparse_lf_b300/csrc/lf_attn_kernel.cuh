@@ -126,19 +126,17 @@ static_assert(8 * KCfg<128>::REGS_SOFTMAX + 4 * KCfg<128>::REGS_OTHER <= 12 * kR
 struct Waiter {
   volatile int* abort;
   unsigned* status;
-  unsigned long long timeout_ns;   // host-set bound of every wait
+  uint32_t iters;   // try_wait attempts before giving up (host-computed from the timeout)
 };
 
 // Bounded wait for an mbarrier phase.  Each try_wait suspends the thread for
-// at most kWaitSliceNs, so the iteration cap bounds the wait at about the
+// at most kWaitSliceNs, so `iters` attempts bound the wait at about the
 // host-set timeout.  On expiry (or when another role has given up, if
 // honour_abort) it records the timeout and returns false.  Kept small: it is
 // inlined at every wait site.
-constexpr uint32_t kWaitSliceNs = 1024;
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
                                           bool honour_abort) {
-  const uint32_t cap = (uint32_t)(w.timeout_ns / kWaitSliceNs) + 1u;
-  for (uint32_t it = 0; it < cap; ++it) {
+  for (uint32_t it = 0; it < w.iters; ++it) {
     if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return true;
     if (honour_abort && (it & 255u) == 255u && *w.abort) return false;
   }
@@ -163,9 +161,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // Self-test of the bounded wait: one thread waits, with the attention
 // kernel's own wait code, on an mbarrier that nothing arrives at; the wait
-// runs out after about timeout_ns and records kStatusTimeout.  No copy or
+// runs out after wait_iters slices and records kStatusTimeout.  No copy or
 // tensor-core work is in flight, so the kernel then simply returns.
-__global__ void lf_selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
+__global__ void lf_selftest_wait_kernel(unsigned* status, uint32_t wait_iters) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -175,7 +173,7 @@ __global__ void lf_selftest_wait_kernel(unsigned* status, unsigned long long tim
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const Waiter w{&abort_flag, status, timeout_ns};
+    const Waiter w{&abort_flag, status, wait_iters};
     (void)bwait(smem_u32(&bar), 0, w);
   }
 }
@@ -266,7 +264,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  Waiter W{abort_flag, p.status, p.timeout_ns};
+  Waiter W{abort_flag, p.status, p.wait_iters};
   const int it_begin = p.cta_begin[blockIdx.x], it_end = p.cta_begin[blockIdx.x + 1];
 
   if (warp >= 8) {

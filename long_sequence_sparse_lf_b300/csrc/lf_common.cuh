@@ -22,6 +22,13 @@ constexpr int kBN = 128;            // keys per band block (MMA N)
 
 enum : uint32_t { kStatusTimeout = 1u, kStatusBadItem = 2u };
 
+// One try_wait suspends a waiting thread for at most this long; the host
+// turns a timeout into a count of such slices.
+constexpr uint32_t kWaitSliceNs = 1024;
+__host__ __device__ constexpr uint32_t wait_iters_for(unsigned long long timeout_ns) {
+  return (uint32_t)(timeout_ns / kWaitSliceNs) + 1u;
+}
+
 // One unit of work of the persistent attention kernel.  A CTA runs two
 // 128-row query tiles side by side (tile slots X = 0 and X = 1) over one
 // shared stream of 128-key blocks; each block names which slots use it.
@@ -131,7 +138,7 @@ struct MainParams {
   int H, L, w;
   float sl2;                       // scale * log2(e)
   unsigned* status;                // device status word
-  unsigned long long timeout_ns;   // bound on every wait
+  uint32_t wait_iters;             // bound on every wait, in try_wait slices
 };
 
 // ---------------------------------------------------------- predicates
