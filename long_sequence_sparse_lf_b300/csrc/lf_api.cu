@@ -198,9 +198,21 @@ struct Pattern {
   std::vector<int32_t> dil, G;
   int32_t* d_G = nullptr;
   uint8_t* d_isg = nullptr;
+  int32_t* d_gcnt = nullptr;
   int32_t* d_dil = nullptr;
   std::vector<uint8_t> isg;
+  std::vector<int32_t> gcnt;   // [L + 1] number of global positions below x
 };
+
+// Global-position tables of a pattern: the flag per position and the prefix
+// count, so that the globals inside any window [a, b) are G[gcnt[a] ..
+// gcnt[b]) without a search.
+void fill_global_tables(Pattern& pt) {
+  pt.isg.assign(pt.L, 0);
+  for (int g : pt.G) pt.isg[g] = 1;
+  pt.gcnt.assign(pt.L + 1, 0);
+  for (int x = 0; x < pt.L; ++x) pt.gcnt[x + 1] = pt.gcnt[x] + pt.isg[x];
+}
 
 struct Plan {
   std::shared_ptr<Pattern> pat;
@@ -238,10 +250,12 @@ lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const in
   pat->n_g = n_g;
   pat->dil.assign(dil, dil + H);
   if (n_g) pat->G.assign(gidx, gidx + n_g);
-  pat->isg.assign(L, 0);
-  for (int g : pat->G) pat->isg[g] = 1;
+  fill_global_tables(*pat);
   LF_CUDA(cudaMalloc(&pat->d_isg, L));
   LF_CUDA(cudaMemcpy(pat->d_isg, pat->isg.data(), L, cudaMemcpyHostToDevice));
+  LF_CUDA(cudaMalloc(&pat->d_gcnt, sizeof(int32_t) * (L + 1)));
+  LF_CUDA(cudaMemcpy(pat->d_gcnt, pat->gcnt.data(), sizeof(int32_t) * (L + 1),
+                     cudaMemcpyHostToDevice));
   LF_CUDA(cudaMalloc(&pat->d_dil, sizeof(int32_t) * H));
   LF_CUDA(cudaMemcpy(pat->d_dil, dil, sizeof(int32_t) * H, cudaMemcpyHostToDevice));
   LF_CUDA(cudaMalloc(&pat->d_G, sizeof(int32_t) * std::max(n_g, 1)));
@@ -569,6 +583,7 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
   P.n_items = (int)pl->items.size();
   P.gidx = pat->d_G;
   P.is_glob = pat->d_isg;
+  P.gcnt = pat->d_gcnt;
   P.n_g = n_g;
   P.NGB = pl->NGB;
   P.NGQ = pl->NGQ;
@@ -775,8 +790,7 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
     pat->n_g = n_g;
     pat->dil.assign(dilation, dilation + H);
     if (n_g) pat->G.assign(gidx, gidx + n_g);
-    pat->isg.assign(L, 0);
-    for (int g : pat->G) pat->isg[g] = 1;
+    fill_global_tables(*pat);
     pl.pat = pat;
   }
   pl.B = B;
@@ -793,8 +807,9 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
     pl.head_slot[h] = sl;
   }
 
-  // scratch layout: work list | global positions | global flags | gathered
-  // q, k, v | partial O | partial (m, l); each part 256-byte aligned
+  // scratch layout: work list | global positions | global flags | global
+  // prefix counts | gathered q, k, v | partial O | partial (m, l); each part
+  // 256-byte aligned
   const int BH = B * H;
   DevState* ds = nullptr;
   int dev = 0;
@@ -810,6 +825,8 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   off += align_up(sizeof(int32_t) * std::max(n_g, 1), 256);
   const size_t off_isg = off;
   off += align_up((size_t)L, 256);
+  const size_t off_gcnt = off;
+  off += align_up(sizeof(int32_t) * ((size_t)L + 1), 256);
   const size_t off_g = off;
   const size_t g_elems = (size_t)BH * pl.NGQ * D;
   if (n_g > 0) off += align_up(3 * g_elems * 2, 256);
@@ -833,6 +850,7 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   int* d_cta = reinterpret_cast<int*>(ws + off_cta);
   int32_t* d_gidx = reinterpret_cast<int32_t*>(ws + off_gidx);
   uint8_t* d_isg = ws + off_isg;
+  int32_t* d_gcnt = reinterpret_cast<int32_t*>(ws + off_gcnt);
   if (!pl.items.empty())
     LF_CUDA(cudaMemcpyAsync(d_items, pl.items.data(), sizeof(WorkItem) * pl.items.size(),
                             cudaMemcpyHostToDevice, stream));
@@ -841,6 +859,8 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   if (n_g > 0)
     LF_CUDA(cudaMemcpyAsync(d_gidx, gidx, sizeof(int32_t) * n_g, cudaMemcpyHostToDevice, stream));
   LF_CUDA(cudaMemcpyAsync(d_isg, pl.pat->isg.data(), (size_t)L, cudaMemcpyHostToDevice, stream));
+  LF_CUDA(cudaMemcpyAsync(d_gcnt, pl.pat->gcnt.data(), sizeof(int32_t) * ((size_t)L + 1),
+                          cudaMemcpyHostToDevice, stream));
 
   MainParams prm;
   std::memset(&prm, 0, sizeof(prm));
@@ -866,6 +886,7 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   prm.n_items = (int)pl.items.size();
   prm.gidx = d_gidx;
   prm.is_glob = d_isg;
+  prm.gcnt = d_gcnt;
   prm.n_g = n_g;
   prm.NGB = pl.NGB;
   prm.NGQ = pl.NGQ;
@@ -1064,6 +1085,7 @@ void lf_plan_cache_clear(void) {
   for (auto& kv : g_patterns) {
     cudaFree(kv.second->d_G);
     cudaFree(kv.second->d_isg);
+    cudaFree(kv.second->d_gcnt);
     cudaFree(kv.second->d_dil);
   }
   g_patterns.clear();

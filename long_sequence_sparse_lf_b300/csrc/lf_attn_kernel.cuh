@@ -72,8 +72,8 @@
 #define LF_REGS_OT64 72
 #endif
 #ifndef LF_REGS_SM128
-#define LF_REGS_SM128 200  // (D = 128)
-#define LF_REGS_OT128 104
+#define LF_REGS_SM128 216  // (D = 128)
+#define LF_REGS_OT128 72
 #endif
 #ifndef LF_EMU16_D128
 #define LF_EMU16_D128 0    // (D = 128)
@@ -499,11 +499,18 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       }
       const bool active = __any_sync(FULL, rowvalid);
       // globals inside the row's window: G[ga .. gz) (band items only); for
-      // dilated heads only those on the row's residue class are in band(i)
+      // dilated heads only those on the row's residue class are in band(i).
+      // Whether the row itself is a global token (its output then comes from
+      // the global-row items).  Independent loads from the prefix-count
+      // table, issued here and first needed blocks later.
       int ga = 0, gz = 0;
-      if (band && wi.ngb > 0) {
-        ga = sorted_lower(p.gidx, p.n_g, i - d * p.w);
-        gz = sorted_lower(p.gidx, p.n_g, i + d * p.w + 1);
+      bool row_glob = false;
+      if (band && p.n_g > 0) {
+        const int a = min(max(i - d * p.w, 0), p.L), b = min(max(i + d * p.w + 1, 0), p.L);
+        const int ic = min(i, p.L - 1);
+        ga = __ldg(p.gcnt + a);
+        gz = __ldg(p.gcnt + b);
+        row_glob = __ldg(p.gcnt + ic + 1) != __ldg(p.gcnt + ic);
       }
       float m_ref = NEG_INF, l = 0.f;
       bool firstblk = true;
@@ -752,7 +759,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       }
       // O is read 32 columns at a time and written straight out
       if (band) {
-        const bool store = rowvalid && p.is_glob[i] == 0;
+        const bool store = rowvalid && !row_glob;
         const float inv = l > 0.f ? 1.0f / l : 0.f;
         const size_t base = (static_cast<size_t>(wi.bh) * p.L + i) * D;
 #pragma unroll

@@ -127,6 +127,7 @@ struct MainParams {
   int n_items;
   const int32_t* gidx;             // [n_g] sorted global positions
   const uint8_t* is_glob;          // [L] 1 where the position is global
+  const int32_t* gcnt;             // [L + 1] number of global positions below x
   int n_g;
   int NGB;                         // rows of one gathered global key block (16..128)
   int NGQ;                         // padded gathered rows per head (multiple of 128)
