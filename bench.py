@@ -409,6 +409,151 @@ def run_ours(args, wl):
     return 0
 
 
+LAYER_KERNELS = ("layer_gemm_qkv", "layer_split_qkv", "gather_globals", "attn_main",
+                 "combine_globals", "layer_merge_ln1", "layer_gemm_ff", "layer_ln2")
+
+
+def run_layer(args):
+    """One Longformer layer forward (lf_layer_fwd) on a layer workload: QKV
+    GEMM, head split, the sparse attention, residual + LayerNorm, the
+    feed-forward GEMM, residual + LayerNorm.  Useful FLOPs = the two GEMMs
+    (2*M*h*3h + 2*M*h*h, M = B*L tokens, h = hidden) + the attention's
+    4*B*D*pairs; the metric is tokens per second."""
+    import long_sequence_sparse_lf_b300 as lf
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lf.load_library()
+    lw = W.LAYER_CONFIGS[args.layer]
+    host_inputs = W.make_layer_inputs(lw)
+    x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2 = (t.to(dev) for t in host_inputs)
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    _, _, pairs = lf.lf_attn_pairs(lw.H, lw.L, lw.w, lw.dilation, lw.global_idx,
+                                   count_only=True, device=dev)
+    M, h = lw.B * lw.L, lw.hidden
+    gemm_flops = {"layer_gemm_qkv": 2 * M * h * 3 * h, "layer_gemm_ff": 2 * M * h * h}
+    attn_flops = 4 * lw.B * lw.D * pairs
+    flops = sum(gemm_flops.values()) + attn_flops
+
+    def step(xin, yout):
+        lf.lf_layer_fwd(xin, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, yout, lw.H, lw.w,
+                        lw.dilation, lw.global_idx, lw.scale, lw.eps, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(x, out)
+    torch.cuda.synchronize(dev)
+    if lf.lf_attn_get_status(stream) != 0:
+        raise SystemExit("device status error after warm-up: " + lf.lf_last_error())
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    lf.lf_profile_reset()
+    lf.lf_profile_enable(True)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = lf.lf_launch_count()
+    for s_ in range(args.steps):
+        flush.zero_()
+        evs[s_][0].record(stream)
+        step(x, out)
+        evs[s_][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = lf.lf_launch_count() - launches0
+    clocks = sampler.stop()
+    lf.lf_profile_enable(False)
+    total_ms = float(sum(a.elapsed_time(b) for a, b in evs))
+    per_kernel = {}
+    for name in LAYER_KERNELS:
+        ms, n = lf.lf_profile_query(name)
+        if n:
+            per_kernel[name] = ms / args.steps
+    lf.lf_profile_reset()
+    if lf.lf_attn_get_status(stream) != 0:
+        raise SystemExit("device status error in timed region: " + lf.lf_last_error())
+    ms_per_step = total_ms / args.steps
+    value = M * args.steps / (total_ms * 1e-3)
+
+    # ---- end to end: x from pinned host memory, the layer, the result back
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    xh = host_inputs[0].contiguous().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    xd, od = torch.empty_like(x), torch.empty_like(out)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        step(xd, od)
+        oh.copy_(od, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+    io_bytes = xh.numel() * xh.element_size()
+
+    # ---- roofline of the kernel with the largest share of the step
+    peaks, peak_src = load_peaks()
+    top = max(per_kernel, key=per_kernel.get)
+    top_s = per_kernel[top] * 1e-3
+    if top in gemm_flops:
+        ach = gemm_flops[top] / top_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+    elif top == "attn_main":
+        ach = attn_flops / top_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+    else:
+        bytes_ = {"layer_split_qkv": M * h * 3 * (4 + 2), "layer_merge_ln1": M * h * 6,
+                  "layer_ln2": M * h * 8}.get(top, 0)
+        ach = bytes_ / top_s / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    roof.update({"traffic": None, "kernel": top, "kernel_ms": per_kernel[top],
+                 "peak_source": "measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                 else "fallback"})
+    line = {
+        "metric": "Longformer layer fwd tokens/s (QKV GEMM, sparse attention, LN, FF GEMM, "
+                  "LN; 1 B300)",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded inputs and random-init weights of the layer's shape)",
+        "config": {"workload": lw.name, "B": lw.B, "L": lw.L, "H": lw.H, "D": lw.D,
+                   "hidden": h, "w": lw.w, "n_global": len(lw.global_idx),
+                   "l2": "flushed between timed steps (256 MiB memset)",
+                   "useful_tflop_per_step": flops / 1e12},
+        "useful_tflops": flops * args.steps / (total_ms * 1e-3) / 1e12,
+        "kernel_ms_per_step": per_kernel,
+        "roofline": roof,
+        "gpu_launches": launches,
+        "e2e": {"value": M * e2e_steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+                "steps": e2e_steps, "api": "lf_layer_fwd with x copied from pinned host "
+                                           "memory and the result copied back"},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle as O
+        rows = list(range(0, lw.L, max(1, lw.L // 64)))
+        xs = [t.double().numpy() for t in host_inputs]
+        t0 = time.perf_counter()
+        O.longformer_layer(*xs, lw.H, lw.w, lw.dilation, lw.global_idx, lw.scale, lw.eps,
+                           store_bf16=True, rows=rows)
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": lw.B * len(rows) / secs, "unit": "tokens/s", "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 layer oracle for {len(rows)} token rows per batch element "
+                      f"(its q/k/v GEMM over all {lw.L} tokens is included)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,9 +564,18 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layer", default=None, choices=sorted(W.LAYER_CONFIGS),
+                    help="time one Longformer layer forward (lf_layer_fwd) instead of the "
+                         "attention alone")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.layer is not None:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the layer line has no "
+                              "reference arm; time the oracle with the default layer run"}))
+            return 0
+        return run_layer(args)
     wl = W.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, wl)

@@ -98,6 +98,46 @@ LF_API lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, vo
                           lf_stream_t stream);
 
 /*
+ * lf_layer_fwd — one Longformer layer forward, bf16 activations.
+ *
+ * The layer of "基于Block-Sparse Attention的Longformer" (block-sparse
+ * Longformer) §6 "Longformer的整体架构", with its attention read as the
+ * sparse attention above (one softmax per row over band(i) ∪ G, per head):
+ *   [q | k | v] = x W_qkv^T + b_qkv, rounded to bf16, split into H heads
+ *   a  = attention(q, k, v)      (lf_attn_fwd: D = hidden / H, w, dilation,
+ *                                 global_idx, scale)
+ *   x1 = bf16(LN1(x + a))         (a merged back to [B, L, hidden])
+ *   y  = bf16(LN2(x1 + x1 W_ff^T + b_ff))
+ * where LN(v) = (v - mean(v)) / sqrt(var(v) + eps) * gamma + beta over the
+ * hidden axis (biased variance).  The page's feed-forward step is one linear
+ * map (no activation); there is no output projection after the attention.
+ *
+ *   x      device, bf16 [B, L, hidden], read only.
+ *   w_qkv  device, bf16 [3*hidden, hidden]: rows 0..hidden-1 map to q, then
+ *          k, then v (the nn.Linear layout: out = x W^T + b).
+ *   b_qkv  device, fp32 [3*hidden].
+ *   w_ff   device, bf16 [hidden, hidden];  b_ff device, fp32 [hidden].
+ *   ln1, ln2 device, fp32 [2*hidden]: gamma, then beta.
+ *   out    device, bf16 [B, L, hidden], written (every element); may not
+ *          alias x.
+ *   hidden = H * D with D in {64, 128}; hidden in {64, 128, 256, 384, 512,
+ *          768, 1024, 1536, 2048} (else LF_ERR_UNSUPPORTED).
+ *   w, dilation, global_idx, n_global, scale: as for lf_attn_fwd.
+ *   eps    finite, > 0.
+ *
+ * The two linear maps are cuBLASLt GEMMs (bf16 inputs, fp32 accumulation and
+ * results); the head split, the attention, and the residual + LayerNorm
+ * steps run in this library's kernels.  Scratch: a second grow-only buffer
+ * per (device, stream), about (B*L*hidden*24 bytes + 32 MiB), apart from the
+ * attention's.  Pointers must be 16-byte aligned (LF_ERR_INVALID_ARG).
+ */
+LF_API lf_status lf_layer_fwd(const void* x, const void* w_qkv, const float* b_qkv,
+                              const void* w_ff, const float* b_ff, const float* ln1,
+                              const float* ln2, void* out, int B, int L, int hidden, int H, int w,
+                              const int32_t* dilation, const int32_t* global_idx, int n_global,
+                              float scale, float eps, lf_stream_t stream);
+
+/*
  * lf_attn_fwd_host — lf_attn_fwd (is_f32 == 0) or lf_attn_fwd_f32
  * (is_f32 != 0) on HOST buffers: copies q, k, v to device memory it
  * allocates on `stream`, runs the forward, copies the result into the host

@@ -73,6 +73,9 @@ def load_library() -> ctypes.CDLL:
     lib.lf_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_uint64)]
     lib.lf_profile_query.restype = i32
+    lib.lf_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip, ip,
+                                 i32, f32, f32, vp]
+    lib.lf_layer_fwd.restype = i32
     _lib = lib
     return lib
 
@@ -282,3 +285,37 @@ def attention(q, k, v, w: int, dilation: Sequence[int], global_idx: Sequence[int
     if q.dtype == torch.float32:
         return lf_attn_fwd_f32(q, k, v, out, w, dilation, global_idx, scale, stream)
     return lf_attn_fwd(q, k, v, out, w, dilation, global_idx, scale, stream)
+
+
+def lf_layer_fwd(x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, out, H: int, w: int,
+                 dilation: Sequence[int], global_idx: Sequence[int], scale: float,
+                 eps: float = 1e-5, stream=None):
+    """One Longformer layer forward (see lf_layer_fwd in include/lfattn.h).
+
+    x, out: bf16 cuda [B, L, hidden]; w_qkv bf16 [3*hidden, hidden]; b_qkv
+    fp32 [3*hidden]; w_ff bf16 [hidden, hidden]; b_ff fp32 [hidden]; ln1, ln2
+    fp32 [2*hidden] (gamma, then beta).  Writes ``out``."""
+    if x.dim() != 3:
+        raise ValueError("x must be [B, L, hidden]")
+    B, L, hidden = x.shape
+    shapes = (("x", x, torch.bfloat16, (B, L, hidden)),
+              ("w_qkv", w_qkv, torch.bfloat16, (3 * hidden, hidden)),
+              ("b_qkv", b_qkv, torch.float32, (3 * hidden,)),
+              ("w_ff", w_ff, torch.bfloat16, (hidden, hidden)),
+              ("b_ff", b_ff, torch.float32, (hidden,)),
+              ("ln1", ln1, torch.float32, (2 * hidden,)),
+              ("ln2", ln2, torch.float32, (2 * hidden,)),
+              ("out", out, torch.bfloat16, (B, L, hidden)))
+    for name, t, dt, shp in shapes:
+        if not isinstance(t, torch.Tensor) or t.dtype != dt or t.device.type != "cuda":
+            raise TypeError(f"{name} must be a {dt} cuda tensor")
+        if not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be contiguous with shape {shp}, got {tuple(t.shape)}")
+    if len(dilation) != H:
+        raise ValueError("dilation must have H entries")
+    lib = load_library()
+    _check(lib.lf_layer_fwd(x.data_ptr(), w_qkv.data_ptr(), b_qkv.data_ptr(), w_ff.data_ptr(),
+                            b_ff.data_ptr(), ln1.data_ptr(), ln2.data_ptr(), out.data_ptr(),
+                            B, L, hidden, H, int(w), _i32_array(dilation),
+                            _i32_array(global_idx), len(global_idx), float(scale), float(eps),
+                            _stream_handle(stream)))

@@ -22,10 +22,13 @@
 #include <tuple>
 #include <vector>
 
+#include <cublasLt.h>
+
 #include "../../include/lfattn.h"
 #include "lf_attn_kernel.cuh"
 #include "lf_aux_kernels.cuh"
 #include "lf_common.cuh"
+#include "lf_layer_kernels.cuh"
 
 namespace {
 
@@ -938,6 +941,220 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
   return LF_OK;
 }
 
+
+// ------------------------------------------------------------ layer forward
+//
+// The Longformer layer of "基于Block-Sparse Attention的Longformer" §6, with
+// the attention read as one softmax over band ∪ G per head (the attention
+// above):
+//   [q | k | v] = x W_qkv^T + b_qkv           (one GEMM, fp32 result)
+//   q, k, v     = bf16, split into H heads     (split_qkv)
+//   a           = attention(q, k, v)           (fwd_impl)
+//   x1          = bf16(LN1(x + merge(a)))      (merge_ln1)
+//   F           = x1 W_ff^T                    (one GEMM, fp32 result)
+//   y           = bf16(LN2(x1 + F + b_ff))     (ln2)
+// The GEMMs are plain library GEMMs (cuBLASLt, bf16 inputs, fp32
+// accumulation and output); everything else runs in this library's kernels.
+
+struct LayerWorkspace {
+  uint8_t* ptr = nullptr;
+  size_t bytes = 0;
+};
+// kept apart from the attention's scratch, which the layer's attention step
+// uses at the same time
+std::map<std::pair<int, cudaStream_t>, LayerWorkspace> g_layer_ws;
+
+lf_status get_layer_workspace(int dev, cudaStream_t stream, size_t bytes, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  LayerWorkspace& w = g_layer_ws[{dev, stream}];
+  if (w.bytes < bytes) {
+    if (w.ptr) LF_CUDA(cudaFreeAsync(w.ptr, stream));
+    w.ptr = nullptr;
+    w.bytes = 0;
+    const size_t grow = align_up(bytes, size_t(1) << 20);
+    LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&w.ptr), grow, stream));
+    w.bytes = grow;
+  }
+  *out = w.ptr;
+  return LF_OK;
+}
+
+constexpr size_t kGemmWorkspace = size_t(32) << 20;
+
+struct GemmPlan {
+  cublasLtMatmulDesc_t op = nullptr;
+  cublasLtMatrixLayout_t a = nullptr, b = nullptr, c = nullptr;
+  cublasLtMatmulAlgo_t algo{};
+};
+using GemmKey = std::tuple<int, long long, int, int>;   // device, M, N, K
+std::map<GemmKey, GemmPlan> g_gemms;
+std::map<int, cublasLtHandle_t> g_lt;
+
+#define LF_LT(call)                                                                  \
+  do {                                                                               \
+    cublasStatus_t st_ = (call);                                                     \
+    if (st_ != CUBLAS_STATUS_SUCCESS) return fail(LF_ERR_CUDA, "%s: cuBLASLt status %d", #call, (int)st_); \
+  } while (0)
+
+// Y[M, N] = X[M, K] W[N, K]^T: X, W bf16 row-major, Y fp32 row-major.  In
+// cuBLASLt's column-major terms Y^T = W X^T, i.e. op(A) = W (A stored K x N,
+// transposed) and B = X^T (stored K x M).
+lf_status gemm_xwt(int dev, const void* X, const void* W, float* Y, long long M, int N, int K,
+                   void* ws, cudaStream_t stream) {
+  cublasLtHandle_t h = nullptr;
+  GemmPlan* gp = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto hi = g_lt.find(dev);
+    if (hi == g_lt.end()) {
+      LF_LT(cublasLtCreate(&h));
+      g_lt[dev] = h;
+    } else {
+      h = hi->second;
+    }
+    auto it = g_gemms.find(GemmKey{dev, M, N, K});
+    if (it != g_gemms.end()) gp = &it->second;
+  }
+  if (gp == nullptr) {
+    GemmPlan p;
+    LF_LT(cublasLtMatmulDescCreate(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F));
+    const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
+    LF_LT(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)));
+    LF_LT(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)));
+    LF_LT(cublasLtMatrixLayoutCreate(&p.a, CUDA_R_16BF, K, N, K));
+    LF_LT(cublasLtMatrixLayoutCreate(&p.b, CUDA_R_16BF, K, M, K));
+    LF_LT(cublasLtMatrixLayoutCreate(&p.c, CUDA_R_32F, N, M, N));
+    cublasLtMatmulPreference_t pref = nullptr;
+    LF_LT(cublasLtMatmulPreferenceCreate(&pref));
+    const size_t wsb = kGemmWorkspace;
+    LF_LT(cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
+                                               &wsb, sizeof(wsb)));
+    cublasLtMatmulHeuristicResult_t res{};
+    int n = 0;
+    const cublasStatus_t st =
+        cublasLtMatmulAlgoGetHeuristic(h, p.op, p.a, p.b, p.c, p.c, pref, 1, &res, &n);
+    cublasLtMatmulPreferenceDestroy(pref);
+    if (st != CUBLAS_STATUS_SUCCESS || n < 1)
+      return fail(LF_ERR_UNSUPPORTED, "no cuBLASLt algorithm for a %lld x %d x %d GEMM", M, N, K);
+    p.algo = res.algo;
+    std::lock_guard<std::mutex> lk(g_mu);
+    gp = &(g_gemms[GemmKey{dev, M, N, K}] = p);
+  }
+  const float alpha = 1.f, beta = 0.f;
+  LF_LT(cublasLtMatmul(h, gp->op, &alpha, W, gp->a, X, gp->b, &beta, Y, gp->c, Y, gp->c,
+                       &gp->algo, ws, kGemmWorkspace, stream));
+  return LF_OK;
+}
+
+lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const void* w_ff,
+                     const float* b_ff, const float* ln1, const float* ln2, void* out, int B, int L,
+                     int hidden, int H, int w, const int32_t* dilation, const int32_t* gidx,
+                     int n_g, float scale, float eps, cudaStream_t stream) {
+  t_last_error.clear();
+  if (B < 1 || L < 1 || H < 1 || hidden < 1)
+    return fail(LF_ERR_INVALID_ARG, "B=%d, L=%d, H=%d and hidden=%d must be >= 1", B, L, H, hidden);
+  if (hidden % H != 0) return fail(LF_ERR_INVALID_ARG, "hidden=%d is not a multiple of H=%d", hidden, H);
+  const int D = hidden / H;
+  if (D != 64 && D != 128) return fail(LF_ERR_UNSUPPORTED, "head size %d (supported: 64, 128)", D);
+  const void* ptrs[8] = {x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, out};
+  for (const void* q : ptrs) {
+    if (q == nullptr) return fail(LF_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned16(q)) return fail(LF_ERR_INVALID_ARG, "a tensor pointer is not 16-byte aligned");
+  }
+  if (!std::isfinite(eps) || !(eps > 0.f)) return fail(LF_ERR_INVALID_ARG, "eps must be finite and > 0");
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(LF_ERR_INVALID_ARG, "scale must be finite and > 0");
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  // the LayerNorm kernels hold a row in registers, two columns per lane
+  // and step; they are instantiated for these widths
+  const int per2 = hidden / 64;
+  if (per2 != 1 && per2 != 2 && per2 != 4 && per2 != 6 && per2 != 8 && per2 != 12 &&
+      per2 != 16 && per2 != 24 && per2 != 32)
+    return fail(LF_ERR_UNSUPPORTED,
+                "hidden=%d (supported: 64, 128, 256, 384, 512, 768, 1024, 1536, 2048)", hidden);
+  DevState* ds = nullptr;
+  int dev = 0;
+  if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
+
+  const long long M = (long long)B * L;
+  const size_t act = (size_t)M * hidden;   // elements of one [B, L, hidden] activation
+  size_t off = 0;
+  const size_t off_y = off;                // fp32 [M, 3*hidden], later F fp32 [M, hidden]
+  off += align_up(act * 3 * 4, 256);
+  const size_t off_qkv = off;              // bf16 3 x [B, H, L, D]
+  off += align_up(act * 3 * 2, 256);
+  const size_t off_a = off;                // bf16 [B, H, L, D]
+  off += align_up(act * 2, 256);
+  const size_t off_x1 = off;               // bf16 [M, hidden]
+  off += align_up(act * 2, 256);
+  const size_t off_gw = off;               // GEMM workspace
+  off += kGemmWorkspace;
+  uint8_t* ws = nullptr;
+  if ((s = get_layer_workspace(dev, stream, off, &ws)) != LF_OK) return s;
+  float* y = reinterpret_cast<float*>(ws + off_y);
+  uint16_t* qkv = reinterpret_cast<uint16_t*>(ws + off_qkv);
+  uint16_t* a = reinterpret_cast<uint16_t*>(ws + off_a);
+  uint16_t* x1 = reinterpret_cast<uint16_t*>(ws + off_x1);
+  void* gws = ws + off_gw;
+
+  lf_status gs = LF_OK;
+  traced("layer_gemm_qkv", stream,
+         [&] { gs = gemm_xwt(dev, x, w_qkv, y, M, 3 * hidden, hidden, gws, stream); });
+  if (gs != LF_OK) return gs;
+  {
+    const size_t total = act * 3 / 4;
+    const int threads = 256;
+    const int blocks = (int)std::max<size_t>(
+        1, std::min<size_t>((total + threads - 1) / threads, (size_t)ds->num_sms * 16));
+    traced("layer_split_qkv", stream, [&] {
+      lf::lf_layer_split_qkv_kernel<<<blocks, threads, 0, stream>>>(
+          reinterpret_cast<const float4*>(y), reinterpret_cast<const float4*>(b_qkv),
+          reinterpret_cast<uint2*>(qkv), B, H, L, D);
+    });
+  }
+  if ((s = fwd_impl(qkv, qkv + act, qkv + 2 * act, a, false, B, H, L, D, w, dilation, gidx, n_g,
+                    scale, stream)) != LF_OK)
+    return s;
+  const int threads = 256;
+  const unsigned rows_blocks = (unsigned)((M + threads / 32 - 1) / (threads / 32));
+  auto launch_ln1 = [&](auto per2c) {
+    constexpr int P = decltype(per2c)::value;
+    traced("layer_merge_ln1", stream, [&] {
+      lf::lf_layer_merge_ln1_kernel<P><<<rows_blocks, threads, 0, stream>>>(
+          reinterpret_cast<const uint32_t*>(x), reinterpret_cast<const uint32_t*>(a), ln1,
+          reinterpret_cast<uint32_t*>(x1), B, H, L, D, eps);
+    });
+  };
+  auto launch_ln2 = [&](auto per2c) {
+    constexpr int P = decltype(per2c)::value;
+    traced("layer_ln2", stream, [&] {
+      lf::lf_layer_ln2_kernel<P><<<rows_blocks, threads, 0, stream>>>(
+          reinterpret_cast<const uint32_t*>(x1), reinterpret_cast<const float2*>(y),
+          reinterpret_cast<const float2*>(b_ff), ln2, reinterpret_cast<uint32_t*>(out), M, eps);
+    });
+  };
+  auto with_width = [&](auto&& f) {
+    switch (per2) {
+      case 1: f(std::integral_constant<int, 1>{}); break;
+      case 2: f(std::integral_constant<int, 2>{}); break;
+      case 4: f(std::integral_constant<int, 4>{}); break;
+      case 6: f(std::integral_constant<int, 6>{}); break;
+      case 8: f(std::integral_constant<int, 8>{}); break;
+      case 12: f(std::integral_constant<int, 12>{}); break;
+      case 16: f(std::integral_constant<int, 16>{}); break;
+      case 24: f(std::integral_constant<int, 24>{}); break;
+      default: f(std::integral_constant<int, 32>{}); break;
+    }
+  };
+  with_width(launch_ln1);
+  traced("layer_gemm_ff", stream,
+         [&] { gs = gemm_xwt(dev, x1, w_ff, y, M, hidden, hidden, gws, stream); });
+  if (gs != LF_OK) return gs;
+  with_width(launch_ln2);
+  LF_CUDA(cudaGetLastError());
+  return LF_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -964,6 +1181,21 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, void* out
   try {
     return fwd_impl(q, k, v, out, true, B, H, L, D, w, dilation, global_idx, n_global, scale,
                     static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_layer_fwd(const void* x, const void* w_qkv, const float* b_qkv, const void* w_ff,
+                       const float* b_ff, const float* ln1, const float* ln2, void* out, int B,
+                       int L, int hidden, int H, int w, const int32_t* dilation,
+                       const int32_t* global_idx, int n_global, float scale, float eps,
+                       lf_stream_t stream) {
+  try {
+    return layer_impl(x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, out, B, L, hidden, H, w, dilation,
+                      global_idx, n_global, scale, eps, static_cast<cudaStream_t>(stream));
   } catch (const std::exception& e) {
     return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
   } catch (...) {
@@ -1079,6 +1311,16 @@ void lf_plan_cache_clear(void) {
   for (auto& kv : g_workspaces)
     if (kv.second.ptr) cudaFree(kv.second.ptr);
   g_workspaces.clear();
+  for (auto& kv : g_layer_ws)
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+  g_layer_ws.clear();
+  for (auto& kv : g_gemms) {
+    cublasLtMatmulDescDestroy(kv.second.op);
+    cublasLtMatrixLayoutDestroy(kv.second.a);
+    cublasLtMatrixLayoutDestroy(kv.second.b);
+    cublasLtMatrixLayoutDestroy(kv.second.c);
+  }
+  g_gemms.clear();
   for (auto& kv : g_plans)
     if (kv.second->d_items) cudaFree(kv.second->d_items);
   g_plans.clear();

@@ -111,3 +111,56 @@ def random_globals(L: int, n: int, seed: int) -> tuple:
     g = torch.Generator().manual_seed(seed)
     n = min(n, L)
     return tuple(sorted(torch.randperm(L, generator=g)[:n].tolist()))
+
+
+# ------------------------------------------------------------ layer inputs
+# Synthetic inputs of one Longformer layer (random-init weights of the
+# page's layer shape; no trained weights exist here).  Only random numbers:
+#   x      ~ N(0, 1)                 bf16 [B, L, hidden]
+#   w_qkv  ~ N(0, 1/hidden)          bf16 [3*hidden, hidden] (q, k, v rows)
+#   b_qkv  ~ N(0, 0.02^2)            fp32 [3*hidden]
+#   w_ff   ~ N(0, 1/hidden)          bf16 [hidden, hidden]
+#   b_ff   ~ N(0, 0.02^2)            fp32 [hidden]
+#   ln1/2  gamma ~ 1 + N(0, 0.1^2), beta ~ N(0, 0.1^2), fp32 [2*hidden]
+# drawn in that order from one CPU generator seeded with `seed`.
+
+@dataclasses.dataclass(frozen=True)
+class LayerWorkload:
+    name: str
+    B: int
+    L: int
+    H: int
+    D: int
+    w: int
+    dilation: tuple
+    global_idx: tuple
+    seed: int
+    eps: float = 1e-5
+
+    @property
+    def hidden(self) -> int:
+        return self.H * self.D
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+LAYER_CONFIGS = {
+    "layer-tiny": LayerWorkload("layer-tiny", 1, 512, 2, 64, 32, (1, 1), (0, 1), 10),
+    "layer-base": LayerWorkload("layer-base", 2, 4096, 12, 64, 256, (1,) * 12, (0,), 11),
+}
+
+
+def make_layer_inputs(lw: LayerWorkload):
+    """CPU tensors (x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2) per the recipe above."""
+    g = torch.Generator("cpu").manual_seed(lw.seed)
+    h = lw.hidden
+    x = torch.randn((lw.B, lw.L, h), generator=g).to(torch.bfloat16)
+    w_qkv = (torch.randn((3 * h, h), generator=g) / math.sqrt(h)).to(torch.bfloat16)
+    b_qkv = torch.randn((3 * h,), generator=g) * 0.02
+    w_ff = (torch.randn((h, h), generator=g) / math.sqrt(h)).to(torch.bfloat16)
+    b_ff = torch.randn((h,), generator=g) * 0.02
+    ln1 = torch.cat([1 + 0.1 * torch.randn((h,), generator=g), 0.1 * torch.randn((h,), generator=g)])
+    ln2 = torch.cat([1 + 0.1 * torch.randn((h,), generator=g), 0.1 * torch.randn((h,), generator=g)])
+    return x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2

@@ -12,6 +12,8 @@ Sources (web pages; cited by title and section):
   [Reformer-hash] "Reformer哈希", section "核心原理" (the attention formula).
   [Eff-survey]    the commentary on "Efficient Transformers: A Survey",
                   section 2.1 (where the cost of dense attention comes from).
+  [LF-blocksparse] §6 "Longformer的整体架构" also defines the layer around the
+                  attention (``longformer_layer`` below).
 
 What is computed (the plain definition; readings of open points are listed
 in the repository's design notes and repeated at each function):
@@ -246,3 +248,80 @@ def total_pairs(L: int, w: int, dilation: Sequence[int],
             cache[d] = pair_count(L, w, d, G)
         tot += cache[d]
     return tot
+
+
+# --------------------------------------------------------------------------
+# The layer around the attention
+# --------------------------------------------------------------------------
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round to bfloat16 (nearest, ties to even) and return float64 values.
+
+    The value is first rounded to float32 (nearest even), then its 32-bit
+    pattern is rounded to the upper 16 bits: add 0x7FFF plus the lowest kept
+    bit, clear the low 16 bits.  Used only where the layer stores an
+    activation in bf16 (see ``longformer_layer``); NaN and infinities do not
+    occur in the layer's values.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def layer_norm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray,
+               eps: float) -> np.ndarray:
+    """LayerNorm over the last axis, float64: (x - mean) / sqrt(var + eps)
+    * gamma + beta with the biased variance (the mean of squared
+    deviations), the normalisation the page's layer applies after each
+    residual ([LF-blocksparse] §6, nn.LayerNorm)."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * np.asarray(gamma, np.float64) + \
+        np.asarray(beta, np.float64)
+
+
+def longformer_layer(x: np.ndarray, w_qkv: np.ndarray, b_qkv: np.ndarray,
+                     w_ff: np.ndarray, b_ff: np.ndarray, ln1: np.ndarray,
+                     ln2: np.ndarray, H: int, w: int, dilation: Sequence[int],
+                     G: Sequence[int], scale: float, eps: float,
+                     store_bf16: bool = True,
+                     rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """One Longformer layer forward, float64 ([LF-blocksparse] §6).
+
+    The page's layer maps x to q, k and v with three linear maps, applies the
+    attention, adds the result to x and normalises (LayerNorm), then applies
+    one linear feed-forward map (no activation), adds and normalises again.
+    Its attention is read as the sparse attention of ``attention`` (one
+    softmax per row over band(i) ∪ G) with the hidden axis split into H
+    heads of D = hidden / H; the page's two attention sublayers, each with
+    its own residual and norm, are that single attention (the repository's
+    design notes list this reading).
+
+    x: [B, L, hidden]; w_qkv: [3*hidden, hidden] (q rows, then k, then v;
+    out = x W^T + b as for nn.Linear); b_qkv: [3*hidden]; w_ff: [hidden,
+    hidden]; b_ff: [hidden]; ln1, ln2: [2, hidden] or [2*hidden] (gamma, then
+    beta).  With store_bf16 (the library's storage), q, k, v, the attention
+    output, x1 and the result are rounded to bf16 where the layer stores
+    them; everything else is float64.  ``rows`` (token positions shared by
+    the batch) limits the attention and everything after it to those rows;
+    the result is then [B, len(rows), hidden].
+    """
+    rnd = bf16_round if store_bf16 else (lambda t: np.asarray(t, np.float64))
+    x = np.asarray(x, dtype=np.float64)
+    B, L, hidden = x.shape
+    D = hidden // H
+    ln1 = np.asarray(ln1, np.float64).reshape(2, hidden)
+    ln2 = np.asarray(ln2, np.float64).reshape(2, hidden)
+    y = x @ np.asarray(w_qkv, np.float64).T + np.asarray(b_qkv, np.float64)
+    y = rnd(y)
+    # [B, L, 3, H, D] -> three [B, H, L, D]
+    y = y.reshape(B, L, 3, H, D).transpose(2, 0, 3, 1, 4)
+    a = attention(y[0], y[1], y[2], w, dilation, G, scale, rows=rows)   # [B, H, R, D]
+    R = a.shape[2]
+    a = rnd(a).transpose(0, 2, 1, 3).reshape(B, R, hidden)
+    xr = x if rows is None else x[:, np.asarray(rows, dtype=np.int64), :]
+    x1 = rnd(layer_norm(xr + a, ln1[0], ln1[1], eps))
+    f = x1 @ np.asarray(w_ff, np.float64).T + np.asarray(b_ff, np.float64)
+    return rnd(layer_norm(x1 + f, ln2[0], ln2[1], eps))
