@@ -239,10 +239,16 @@ LF_API uint64_t lf_launch_count(void);
  * device time (ms) and number of launches of the kernels whose name
  * contains `name` (NULL or "" = all) since the last lf_profile_reset.
  * Kernel names: "attn_main", "gather_globals", "combine_globals",
- * "cast_f32_bf16", "pairs_count", "pairs_scan", "pairs_fill".
- * Tracing adds two event records per launch; it is off by default.
+ * "cast_f32_bf16", "pairs_count", "pairs_scan", "pairs_fill", and for the
+ * layer "layer_gemm_qkv", "layer_split_qkv", "layer_merge_ln1",
+ * "layer_gemm_ff", "layer_ln2".
+ * Tracing adds two event records per traced launch (each costs the stream
+ * about a microsecond); it is off by default.  lf_profile_only restricts it
+ * to the kernels whose name contains `name` (NULL or "" = all, the default),
+ * so that a timed loop brackets only the kernel it measures.
  */
 LF_API void lf_profile_enable(int on);
+LF_API void lf_profile_only(const char* name);
 LF_API void lf_profile_reset(void);
 LF_API lf_status lf_profile_query(const char* name, double* total_ms, uint64_t* launches);
 

@@ -8,6 +8,6 @@ from ._binding import (  # noqa: F401
     LfError, attention, lf_attn_fwd, lf_attn_fwd_f32, lf_attn_fwd_host, lf_attn_fwd_noalloc,
     lf_attn_get_status, lf_attn_pairs, lf_last_error, lf_launch_count, lf_layer_fwd,
     lf_selftest_wait_timeout,
-    lf_plan_cache_clear, lf_profile_enable, lf_profile_query, lf_profile_reset,
+    lf_plan_cache_clear, lf_profile_enable, lf_profile_only, lf_profile_query, lf_profile_reset,
     lf_version, load_library, LIB_PATH, PreparedFwd, prepare_fwd,
 )

@@ -68,6 +68,8 @@ def load_library() -> ctypes.CDLL:
     lib.lf_version.restype = i32
     lib.lf_profile_enable.argtypes = [i32]
     lib.lf_profile_enable.restype = None
+    lib.lf_profile_only.argtypes = [ctypes.c_char_p]
+    lib.lf_profile_only.restype = None
     lib.lf_profile_reset.argtypes = []
     lib.lf_profile_reset.restype = None
     lib.lf_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
@@ -262,6 +264,11 @@ def lf_version() -> int:
 
 def lf_profile_enable(on: bool = True) -> None:
     load_library().lf_profile_enable(1 if on else 0)
+
+
+def lf_profile_only(name=None) -> None:
+    """Trace only the kernels whose name contains ``name`` (None = all)."""
+    load_library().lf_profile_only(name.encode() if name else None)
 
 
 def lf_profile_reset() -> None:

@@ -47,6 +47,7 @@ struct TraceRec {
 };
 std::atomic<int> g_trace_on{0};
 std::mutex g_trace_mu;
+std::string g_trace_only;   // trace only kernels whose name contains this (empty = all)
 std::vector<TraceRec> g_trace;
 std::vector<cudaEvent_t> g_event_pool;
 
@@ -65,7 +66,12 @@ cudaEvent_t trace_event() {
 // on, brackets it with two events recorded on the same stream.
 template <class F>
 void traced(const char* name, cudaStream_t s, F&& launch) {
-  if (g_trace_on.load(std::memory_order_relaxed)) {
+  bool on = g_trace_on.load(std::memory_order_relaxed) != 0;
+  if (on) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    on = g_trace_only.empty() || std::strstr(name, g_trace_only.c_str()) != nullptr;
+  }
+  if (on) {
     std::lock_guard<std::mutex> lk(g_trace_mu);
     TraceRec r{name, trace_event(), trace_event()};
     cudaEventRecord(r.e0, s);
@@ -986,7 +992,7 @@ struct GemmPlan {
   cublasLtMatrixLayout_t a = nullptr, b = nullptr, c = nullptr;
   cublasLtMatmulAlgo_t algo{};
 };
-using GemmKey = std::tuple<int, long long, int, int>;   // device, M, N, K
+using GemmKey = std::tuple<int, long long, int, int, bool>;   // device, M, N, K, bf16 Y
 std::map<GemmKey, GemmPlan> g_gemms;
 std::map<int, cublasLtHandle_t> g_lt;
 
@@ -996,11 +1002,12 @@ std::map<int, cublasLtHandle_t> g_lt;
     if (st_ != CUBLAS_STATUS_SUCCESS) return fail(LF_ERR_CUDA, "%s: cuBLASLt status %d", #call, (int)st_); \
   } while (0)
 
-// Y[M, N] = X[M, K] W[N, K]^T: X, W bf16 row-major, Y fp32 row-major.  In
-// cuBLASLt's column-major terms Y^T = W X^T, i.e. op(A) = W (A stored K x N,
-// transposed) and B = X^T (stored K x M).
-lf_status gemm_xwt(int dev, const void* X, const void* W, float* Y, long long M, int N, int K,
-                   void* ws, cudaStream_t stream) {
+// Y[M, N] = X[M, K] W[N, K]^T: X, W bf16 row-major, Y fp32 (or bf16, rounded
+// to nearest even) row-major, fp32 accumulation.  In cuBLASLt's column-major
+// terms Y^T = W X^T, i.e. op(A) = W (A stored K x N, transposed) and B = X^T
+// (stored K x M).
+lf_status gemm_xwt(int dev, const void* X, const void* W, void* Y, bool y_bf16, long long M,
+                   int N, int K, void* ws, cudaStream_t stream) {
   cublasLtHandle_t h = nullptr;
   GemmPlan* gp = nullptr;
   {
@@ -1012,7 +1019,7 @@ lf_status gemm_xwt(int dev, const void* X, const void* W, float* Y, long long M,
     } else {
       h = hi->second;
     }
-    auto it = g_gemms.find(GemmKey{dev, M, N, K});
+    auto it = g_gemms.find(GemmKey{dev, M, N, K, y_bf16});
     if (it != g_gemms.end()) gp = &it->second;
   }
   if (gp == nullptr) {
@@ -1023,7 +1030,7 @@ lf_status gemm_xwt(int dev, const void* X, const void* W, float* Y, long long M,
     LF_LT(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)));
     LF_LT(cublasLtMatrixLayoutCreate(&p.a, CUDA_R_16BF, K, N, K));
     LF_LT(cublasLtMatrixLayoutCreate(&p.b, CUDA_R_16BF, K, M, K));
-    LF_LT(cublasLtMatrixLayoutCreate(&p.c, CUDA_R_32F, N, M, N));
+    LF_LT(cublasLtMatrixLayoutCreate(&p.c, y_bf16 ? CUDA_R_16BF : CUDA_R_32F, N, M, N));
     cublasLtMatmulPreference_t pref = nullptr;
     LF_LT(cublasLtMatmulPreferenceCreate(&pref));
     const size_t wsb = kGemmWorkspace;
@@ -1038,7 +1045,7 @@ lf_status gemm_xwt(int dev, const void* X, const void* W, float* Y, long long M,
       return fail(LF_ERR_UNSUPPORTED, "no cuBLASLt algorithm for a %lld x %d x %d GEMM", M, N, K);
     p.algo = res.algo;
     std::lock_guard<std::mutex> lk(g_mu);
-    gp = &(g_gemms[GemmKey{dev, M, N, K}] = p);
+    gp = &(g_gemms[GemmKey{dev, M, N, K, y_bf16}] = p);
   }
   const float alpha = 1.f, beta = 0.f;
   LF_LT(cublasLtMatmul(h, gp->op, &alpha, W, gp->a, X, gp->b, &beta, Y, gp->c, Y, gp->c,
@@ -1065,8 +1072,8 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(LF_ERR_INVALID_ARG, "scale must be finite and > 0");
   lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
   if (s != LF_OK) return s;
-  // the LayerNorm kernels hold a row in registers, two columns per lane
-  // and step; they are instantiated for these widths
+  // the LayerNorm kernels hold a row in registers (hidden / 32 values per
+  // lane); they are instantiated for these widths
   const int per2 = hidden / 64;
   if (per2 != 1 && per2 != 2 && per2 != 4 && per2 != 6 && per2 != 8 && per2 != 12 &&
       per2 != 16 && per2 != 24 && per2 != 32)
@@ -1079,8 +1086,8 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   const long long M = (long long)B * L;
   const size_t act = (size_t)M * hidden;   // elements of one [B, L, hidden] activation
   size_t off = 0;
-  const size_t off_y = off;                // fp32 [M, 3*hidden], later F fp32 [M, hidden]
-  off += align_up(act * 3 * 4, 256);
+  const size_t off_y = off;                // bf16 Y [M, 3*hidden], later fp32 F [M, hidden]
+  off += align_up(act * 3 * 2, 256);
   const size_t off_qkv = off;              // bf16 3 x [B, H, L, D]
   off += align_up(act * 3 * 2, 256);
   const size_t off_a = off;                // bf16 [B, H, L, D]
@@ -1091,7 +1098,7 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   off += kGemmWorkspace;
   uint8_t* ws = nullptr;
   if ((s = get_layer_workspace(dev, stream, off, &ws)) != LF_OK) return s;
-  float* y = reinterpret_cast<float*>(ws + off_y);
+  void* y = ws + off_y;
   uint16_t* qkv = reinterpret_cast<uint16_t*>(ws + off_qkv);
   uint16_t* a = reinterpret_cast<uint16_t*>(ws + off_a);
   uint16_t* x1 = reinterpret_cast<uint16_t*>(ws + off_x1);
@@ -1099,56 +1106,52 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
 
   lf_status gs = LF_OK;
   traced("layer_gemm_qkv", stream,
-         [&] { gs = gemm_xwt(dev, x, w_qkv, y, M, 3 * hidden, hidden, gws, stream); });
+         [&] { gs = gemm_xwt(dev, x, w_qkv, y, true, M, 3 * hidden, hidden, gws, stream); });
   if (gs != LF_OK) return gs;
-  {
-    const size_t total = act * 3 / 4;
-    const int threads = 256;
-    const int blocks = (int)std::max<size_t>(
-        1, std::min<size_t>((total + threads - 1) / threads, (size_t)ds->num_sms * 16));
-    traced("layer_split_qkv", stream, [&] {
-      lf::lf_layer_split_qkv_kernel<<<blocks, threads, 0, stream>>>(
-          reinterpret_cast<const float4*>(y), reinterpret_cast<const float4*>(b_qkv),
-          reinterpret_cast<uint2*>(qkv), B, H, L, D);
-    });
-  }
+  if (M > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "B*L=%lld tokens is too many", M);
+  traced("layer_split_qkv", stream, [&] {
+    lf::lf_layer_split_qkv_kernel<<<(unsigned)M, 3 * hidden / 8, 0, stream>>>(
+        reinterpret_cast<const uint4*>(y), reinterpret_cast<const float4*>(b_qkv),
+        reinterpret_cast<uint4*>(qkv), B, H, L, D);
+  });
   if ((s = fwd_impl(qkv, qkv + act, qkv + 2 * act, a, false, B, H, L, D, w, dilation, gidx, n_g,
                     scale, stream)) != LF_OK)
     return s;
   const int threads = 256;
   const unsigned rows_blocks = (unsigned)((M + threads / 32 - 1) / (threads / 32));
-  auto launch_ln1 = [&](auto per2c) {
-    constexpr int P = decltype(per2c)::value;
+  // the LayerNorm kernels, with the widest vector (VW columns, NJ steps per
+  // lane) the width allows
+  auto launch_ln1 = [&](auto vw, auto nj) {
+    constexpr int VW = decltype(vw)::value, NJ = decltype(nj)::value;
     traced("layer_merge_ln1", stream, [&] {
-      lf::lf_layer_merge_ln1_kernel<P><<<rows_blocks, threads, 0, stream>>>(
-          reinterpret_cast<const uint32_t*>(x), reinterpret_cast<const uint32_t*>(a), ln1,
-          reinterpret_cast<uint32_t*>(x1), B, H, L, D, eps);
+      lf::lf_layer_merge_ln1_kernel<VW, NJ><<<rows_blocks, threads, 0, stream>>>(
+          static_cast<const uint16_t*>(x), a, ln1, x1, B, H, L, D, eps);
     });
   };
-  auto launch_ln2 = [&](auto per2c) {
-    constexpr int P = decltype(per2c)::value;
+  auto launch_ln2 = [&](auto vw, auto nj) {
+    constexpr int VW = decltype(vw)::value, NJ = decltype(nj)::value;
     traced("layer_ln2", stream, [&] {
-      lf::lf_layer_ln2_kernel<P><<<rows_blocks, threads, 0, stream>>>(
-          reinterpret_cast<const uint32_t*>(x1), reinterpret_cast<const float2*>(y),
-          reinterpret_cast<const float2*>(b_ff), ln2, reinterpret_cast<uint32_t*>(out), M, eps);
+      lf::lf_layer_ln2_kernel<VW, NJ><<<rows_blocks, threads, 0, stream>>>(
+          x1, static_cast<const float*>(y), b_ff, ln2, static_cast<uint16_t*>(out), M, eps);
     });
   };
   auto with_width = [&](auto&& f) {
-    switch (per2) {
-      case 1: f(std::integral_constant<int, 1>{}); break;
-      case 2: f(std::integral_constant<int, 2>{}); break;
-      case 4: f(std::integral_constant<int, 4>{}); break;
-      case 6: f(std::integral_constant<int, 6>{}); break;
-      case 8: f(std::integral_constant<int, 8>{}); break;
-      case 12: f(std::integral_constant<int, 12>{}); break;
-      case 16: f(std::integral_constant<int, 16>{}); break;
-      case 24: f(std::integral_constant<int, 24>{}); break;
-      default: f(std::integral_constant<int, 32>{}); break;
+    using I = std::integral_constant<int, 1>;
+    switch (hidden) {
+      case 64: f(std::integral_constant<int, 2>{}, I{}); break;
+      case 128: f(std::integral_constant<int, 4>{}, I{}); break;
+      case 256: f(std::integral_constant<int, 8>{}, I{}); break;
+      case 384: f(std::integral_constant<int, 4>{}, std::integral_constant<int, 3>{}); break;
+      case 512: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 2>{}); break;
+      case 768: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 3>{}); break;
+      case 1024: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 4>{}); break;
+      case 1536: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 6>{}); break;
+      default: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 8>{}); break;
     }
   };
   with_width(launch_ln1);
   traced("layer_gemm_ff", stream,
-         [&] { gs = gemm_xwt(dev, x1, w_ff, y, M, hidden, hidden, gws, stream); });
+         [&] { gs = gemm_xwt(dev, x1, w_ff, y, false, M, hidden, hidden, gws, stream); });
   if (gs != LF_OK) return gs;
   with_width(launch_ln2);
   LF_CUDA(cudaGetLastError());
@@ -1336,6 +1339,11 @@ void lf_plan_cache_clear(void) {
 uint64_t lf_launch_count(void) { return g_launches.load(); }
 
 void lf_profile_enable(int on) { g_trace_on.store(on ? 1 : 0); }
+
+void lf_profile_only(const char* name) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_only = name ? name : "";
+}
 
 void lf_profile_reset(void) {
   std::lock_guard<std::mutex> lk(g_trace_mu);
