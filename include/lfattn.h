@@ -87,6 +87,44 @@ LF_API lf_status lf_attn_fwd(const void* q, const void* k, const void* v, void* 
                       int n_global, float scale, lf_stream_t stream);
 
 /*
+ * lf_attn_fwd_lse — lf_attn_fwd that also writes each row's log-sum-exp,
+ *   lse[b,h,i] = ln( sum_{j in K(i)} exp(scale * q_i . k_j) )   (fp32),
+ * the normaliser a backward pass needs (p_ij = exp(scale q_i.k_j - lse_i)).
+ *   lse  device, fp32 [B,H,L], written (every element), 16-byte aligned.
+ * Other arguments and errors as lf_attn_fwd.
+ */
+LF_API lf_status lf_attn_fwd_lse(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int B, int H, int L, int D, int w,
+                                 const int32_t* dilation, const int32_t* global_idx, int n_global,
+                                 float scale, lf_stream_t stream);
+
+/*
+ * lf_attn_bwd — gradients of sum(out * dout) for out = lf_attn_fwd(q, k, v).
+ *
+ * With s_ij = scale q_i . k_j over K(i), p_ij = exp(s_ij - lse_i):
+ *   dv_j = sum_i p_ij dout_i
+ *   ds_ij = p_ij (dout_i . v_j - dout_i . out_i)
+ *   dq_i = scale sum_j ds_ij k_j,   dk_j = scale sum_i ds_ij q_i
+ * (the derivative of the forward's definition; the pages give no backward).
+ *
+ *   q, k, v, out, dout  device, bf16 [B,H,L,D], read only (out and lse from
+ *                 the forward on the same q, k, v: lf_attn_fwd_lse).
+ *   lse           device, fp32 [B,H,L], read only.
+ *   dq, dk, dv    device, fp32 [B,H,L,D], written (every element).
+ *   Other arguments and errors as lf_attn_fwd.
+ *
+ * Products in bf16 (p and ds are rounded to bf16 before their products) with
+ * fp32 accumulation; contributions are summed with fp32 atomics, so the
+ * low bits of the result depend on the order the hardware applies them.
+ * Scratch: B*H*L*4 bytes in a third grow-only buffer per (device, stream).
+ */
+LF_API lf_status lf_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                             const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                             int B, int H, int L, int D, int w, const int32_t* dilation,
+                             const int32_t* global_idx, int n_global, float scale,
+                             lf_stream_t stream);
+
+/*
  * lf_attn_fwd_f32 — same operation with fp32 q/k/v/out.  q, k and v are
  * rounded to bf16 (nearest even) on the device first; the output is written
  * in fp32 without the final bf16 rounding.  Same arguments and errors as

@@ -78,6 +78,12 @@ def load_library() -> ctypes.CDLL:
     lib.lf_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip, ip,
                                  i32, f32, f32, vp]
     lib.lf_layer_fwd.restype = i32
+    lib.lf_attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip, ip, i32,
+                                    f32, vp]
+    lib.lf_attn_fwd_lse.restype = i32
+    lib.lf_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip,
+                                ip, i32, f32, vp]
+    lib.lf_attn_bwd.restype = i32
     _lib = lib
     return lib
 
@@ -326,3 +332,39 @@ def lf_layer_fwd(x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, out, H: int, w: int,
                             B, L, hidden, H, int(w), _i32_array(dilation),
                             _i32_array(global_idx), len(global_idx), float(scale), float(eps),
                             _stream_handle(stream)))
+
+
+def lf_attn_fwd_lse(q, k, v, out, lse, w: int, dilation: Sequence[int],
+                    global_idx: Sequence[int], scale: float, stream=None):
+    """bf16 forward that also writes lse (fp32 cuda [B,H,L]), the row's
+    log-sum-exp of the scaled scores over its key set."""
+    _check_qkv(q, k, v, out, torch.bfloat16, "cuda")
+    B, H, L, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, L) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,L]")
+    lib = load_library()
+    _check(lib.lf_attn_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), B, H, L, D, int(w), _i32_array(dilation),
+                               _i32_array(global_idx), len(global_idx), float(scale),
+                               _stream_handle(stream)))
+
+
+def lf_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, w: int, dilation: Sequence[int],
+                global_idx: Sequence[int], scale: float, stream=None):
+    """Gradients dq, dk, dv (fp32 cuda [B,H,L,D]) of sum(out * dout); q, k,
+    v, out, dout bf16 cuda [B,H,L,D]; lse from lf_attn_fwd_lse."""
+    _check_qkv(q, k, v, out, torch.bfloat16, "cuda")
+    B, H, L, D = q.shape
+    if dout.dtype != torch.bfloat16 or dout.shape != q.shape or not dout.is_contiguous():
+        raise ValueError("dout must be a contiguous bf16 tensor like q")
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.dtype != torch.float32 or t.shape != q.shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 tensor like q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, L) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B,H,L]")
+    lib = load_library()
+    _check(lib.lf_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dv.data_ptr(), B, H, L, D, int(w), _i32_array(dilation),
+                           _i32_array(global_idx), len(global_idx), float(scale),
+                           _stream_handle(stream)))

@@ -28,6 +28,7 @@
 #include "lf_attn_kernel.cuh"
 #include "lf_aux_kernels.cuh"
 #include "lf_common.cuh"
+#include "lf_bwd_kernels.cuh"
 #include "lf_layer_kernels.cuh"
 
 namespace {
@@ -551,7 +552,7 @@ lf_status get_workspace(int dev, cudaStream_t stream, size_t bytes, uint8_t** ou
 // plan and every device address they embed, so that a repeated call encodes
 // nothing.
 using ParamKey = std::tuple<const Plan*, const void*, const void*, const void*, void*, bool,
-                            const uint8_t*, float>;
+                            const uint8_t*, float, float*>;
 std::map<ParamKey, std::unique_ptr<MainParams>> g_params;
 constexpr size_t kMaxCachedParams = 256;
 
@@ -560,7 +561,7 @@ constexpr size_t kMaxCachedParams = 256;
 // addresses.
 lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, const void* qb,
                        const void* kb, const void* vb, void* out, bool f32, uint8_t* ws,
-                       size_t off_g, size_t off_po, size_t off_pm, float scale,
+                       size_t off_g, size_t off_po, size_t off_pm, float scale, float* lse,
                        MainParams* prm_out) {
   lf_status s = LF_OK;
   const Plan* pl = &plan;
@@ -605,6 +606,7 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
   P.L = L;
   P.w = w;
   P.sl2 = scale * 1.4426950408889634f;
+  P.lse = lse;
   P.status = ds->status;
   P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
@@ -613,7 +615,7 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
 
 lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool f32, int B, int H,
                    int L, int D, int w, const int32_t* dilation, const int32_t* gidx, int n_g,
-                   float scale, cudaStream_t stream) {
+                   float scale, cudaStream_t stream, float* lse = nullptr) {
   t_last_error.clear();
   if (B < 1) return fail(LF_ERR_INVALID_ARG, "B=%d must be >= 1", B);
   lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
@@ -673,7 +675,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
     vb = cq + 2 * elems;
   }
 
-  const ParamKey pkey{pl, qb, kb, vb, out, f32, ws, scale};
+  const ParamKey pkey{pl, qb, kb, vb, out, f32, ws, scale, lse};
   MainParams* cached = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -686,7 +688,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   if (cached == nullptr) {
     auto fresh = std::make_unique<MainParams>();
     if ((s = build_params(ds, *pl, *pat, qb, kb, vb, out, f32, ws, off_g, off_po, off_pm, scale,
-                          fresh.get())) != LF_OK)
+                          lse, fresh.get())) != LF_OK)
       return s;
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_params.size() >= kMaxCachedParams) g_params.clear();
@@ -725,11 +727,11 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
       if (D == 64)
         lf::lf_combine_globals_kernel<64><<<blocks, threads, 0, stream>>>(
             prm.part_o, prm.part_ml, pat->d_G, out, prm.out_f32, n_g, pl->NGQ, pl->n_chunks, L,
-            BH);
+            BH, lse);
       else
         lf::lf_combine_globals_kernel<128><<<blocks, threads, 0, stream>>>(
             prm.part_o, prm.part_ml, pat->d_G, out, prm.out_f32, n_g, pl->NGQ, pl->n_chunks, L,
-            BH);
+            BH, lse);
     });
   }
   LF_CUDA(cudaGetLastError());
@@ -937,10 +939,10 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
     const int blocks = (int)((warps + threads / 32 - 1) / (threads / 32));
     if (D == 64)
       lf::lf_combine_globals_kernel<64><<<blocks, threads, 0, stream>>>(
-          prm.part_o, prm.part_ml, d_gidx, out, 0, n_g, pl.NGQ, pl.n_chunks, L, BH);
+          prm.part_o, prm.part_ml, d_gidx, out, 0, n_g, pl.NGQ, pl.n_chunks, L, BH, nullptr);
     else
       lf::lf_combine_globals_kernel<128><<<blocks, threads, 0, stream>>>(
-          prm.part_o, prm.part_ml, d_gidx, out, 0, n_g, pl.NGQ, pl.n_chunks, L, BH);
+          prm.part_o, prm.part_ml, d_gidx, out, 0, n_g, pl.NGQ, pl.n_chunks, L, BH, nullptr);
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   LF_CUDA(cudaGetLastError());
@@ -1158,6 +1160,152 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   return LF_OK;
 }
 
+
+// ------------------------------------------------------------ backward
+
+// Band tiles of the backward (bh, residue r, first key t0, dilation d), per
+// batch size and pattern; plus the backward's own scratch (delta).
+struct BwdPlan {
+  int4* d_tiles = nullptr;
+  int n_tiles = 0;
+};
+std::map<PlanKey, BwdPlan> g_bwd_plans;
+std::map<std::pair<int, cudaStream_t>, LayerWorkspace> g_bwd_ws;
+bool g_bwd_smem_set[64] = {false};
+
+lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   const void* dout, float* dq, float* dk, float* dv, int B, int H, int L, int D,
+                   int w, const int32_t* dilation, const int32_t* gidx, int n_g, float scale,
+                   cudaStream_t stream) {
+  t_last_error.clear();
+  if (B < 1) return fail(LF_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  const void* ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
+  for (const void* x : ptrs) {
+    if (x == nullptr) return fail(LF_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned16(x)) return fail(LF_ERR_INVALID_ARG, "a tensor pointer is not 16-byte aligned");
+  }
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(LF_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (D != 64 && D != 128) return fail(LF_ERR_UNSUPPORTED, "D=%d (supported: 64, 128)", D);
+  for (int h = 0; h < H; ++h)
+    if (dilation[h] > 1 && L % dilation[h] != 0)
+      return fail(LF_ERR_UNSUPPORTED, "L=%d is not a multiple of dilation[%d]=%d", L, h, dilation[h]);
+  if ((long long)B * H * L > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "B*H*L too large");
+  DevState* ds = nullptr;
+  int dev = 0;
+  if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
+  std::shared_ptr<Pattern> pat;
+  if ((s = get_pattern(dev, H, L, w, dilation, gidx, n_g, &pat)) != LF_OK) return s;
+  BwdPlan* bp = nullptr;
+  {
+    PatKey pk{dev, H, L, w, pat->dil, pat->G};
+    PlanKey key{dev, B, D, pk};
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_bwd_plans.find(key);
+    if (it == g_bwd_plans.end()) {
+      std::vector<int4> tiles;
+      for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+          const int d = dilation[h];
+          for (int r = 0; r < d; ++r) {
+            const int Lr = lf::residue_len(L, d, r);
+            for (int t0 = 0; t0 < Lr; t0 += lf::kBwdB) tiles.push_back(make_int4(b * H + h, r, t0, d));
+          }
+        }
+      BwdPlan np;
+      np.n_tiles = (int)tiles.size();
+      LF_CUDA(cudaMalloc(&np.d_tiles, sizeof(int4) * std::max<size_t>(tiles.size(), 1)));
+      LF_CUDA(cudaMemcpy(np.d_tiles, tiles.data(), sizeof(int4) * tiles.size(), cudaMemcpyHostToDevice));
+      it = g_bwd_plans.emplace(key, np).first;
+    }
+    bp = &it->second;
+  }
+  const long long rows = (long long)B * H * L;
+  uint8_t* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    LayerWorkspace& wsp = g_bwd_ws[{dev, stream}];
+    const size_t need = align_up((size_t)rows * 4, 256);
+    if (wsp.bytes < need) {
+      if (wsp.ptr) LF_CUDA(cudaFreeAsync(wsp.ptr, stream));
+      wsp.ptr = nullptr;
+      wsp.bytes = 0;
+      LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&wsp.ptr), align_up(need, size_t(1) << 20), stream));
+      wsp.bytes = align_up(need, size_t(1) << 20);
+    }
+    ws = wsp.ptr;
+  }
+  float* delta = reinterpret_cast<float*>(ws);
+  const size_t grad_bytes = (size_t)rows * D * 4;
+  LF_CUDA(cudaMemsetAsync(dq, 0, grad_bytes, stream));
+  LF_CUDA(cudaMemsetAsync(dk, 0, grad_bytes, stream));
+  LF_CUDA(cudaMemsetAsync(dv, 0, grad_bytes, stream));
+
+  lf::BwdParams P;
+  P.q = static_cast<const __nv_bfloat16*>(q);
+  P.k = static_cast<const __nv_bfloat16*>(k);
+  P.v = static_cast<const __nv_bfloat16*>(v);
+  P.dout = static_cast<const __nv_bfloat16*>(dout);
+  P.lse = lse;
+  P.delta = delta;
+  P.dq = dq;
+  P.dk = dk;
+  P.dv = dv;
+  P.gidx = pat->d_G;
+  P.is_glob = pat->d_isg;
+  P.tiles = bp->d_tiles;
+  P.n_tiles = bp->n_tiles;
+  P.head_dil = pat->d_dil;
+  P.H = H;
+  P.L = L;
+  P.w = w;
+  P.n_g = n_g;
+  P.scale = scale;
+
+  const int dthreads = 256;
+  const unsigned dblocks = (unsigned)((rows + dthreads / 32 - 1) / (dthreads / 32));
+  const int gt = (n_g + lf::kBwdB - 1) / lf::kBwdB;
+  const long long gunits = (long long)B * H * gt;
+  auto launch_all = [&](auto dc) -> lf_status {
+    constexpr int DD = decltype(dc)::value;
+    const int smem = (int)sizeof(lf::BwdSmem<DD>);
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      const int slot = dev * 2 + (DD == 128 ? 1 : 0);
+      if (slot < 64 && !g_bwd_smem_set[slot]) {
+        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        g_bwd_smem_set[slot] = true;
+      }
+    }
+    traced("bwd_delta", stream, [&] {
+      lf::lf_bwd_delta_kernel<DD><<<dblocks, dthreads, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(out), P.dout, delta, rows);
+    });
+    if (P.n_tiles > 0)
+      traced("bwd_band", stream, [&] {
+        lf::lf_bwd_kernel<DD, 0><<<(unsigned)P.n_tiles, lf::kBwdThreads, smem, stream>>>(P);
+      });
+    if (gunits > 0) {
+      if (gunits > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "too many global tiles");
+      traced("bwd_global_keys", stream, [&] {
+        lf::lf_bwd_kernel<DD, 1><<<(unsigned)gunits, lf::kBwdThreads, smem, stream>>>(P);
+      });
+      traced("bwd_global_rows", stream, [&] {
+        lf::lf_bwd_kernel<DD, 2><<<(unsigned)gunits, lf::kBwdThreads, smem, stream>>>(P);
+      });
+    }
+    return LF_OK;
+  };
+  if (D == 64) s = launch_all(std::integral_constant<int, 64>{});
+  else s = launch_all(std::integral_constant<int, 128>{});
+  if (s != LF_OK) return s;
+  LF_CUDA(cudaGetLastError());
+  return LF_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -1170,6 +1318,36 @@ lf_status lf_attn_fwd(const void* q, const void* k, const void* v, void* out, in
   try {
     return fwd_impl(q, k, v, out, false, B, H, L, D, w, dilation, global_idx, n_global, scale,
                     static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int B, int H, int L, int D, int w, const int32_t* dilation,
+                          const int32_t* global_idx, int n_global, float scale,
+                          lf_stream_t stream) {
+  try {
+    if (lse == nullptr || (reinterpret_cast<uintptr_t>(lse) & 15u) != 0)
+      return fail(LF_ERR_INVALID_ARG, "lse must be a 16-byte aligned device pointer");
+    return fwd_impl(q, k, v, out, false, B, H, L, D, w, dilation, global_idx, n_global, scale,
+                    static_cast<cudaStream_t>(stream), lse);
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                      const float* lse, const void* dout, float* dq, float* dk, float* dv, int B,
+                      int H, int L, int D, int w, const int32_t* dilation,
+                      const int32_t* global_idx, int n_global, float scale, lf_stream_t stream) {
+  try {
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, B, H, L, D, w, dilation, global_idx,
+                    n_global, scale, static_cast<cudaStream_t>(stream));
   } catch (const std::exception& e) {
     return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
   } catch (...) {
@@ -1317,6 +1495,11 @@ void lf_plan_cache_clear(void) {
   for (auto& kv : g_layer_ws)
     if (kv.second.ptr) cudaFree(kv.second.ptr);
   g_layer_ws.clear();
+  for (auto& kv : g_bwd_ws)
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+  g_bwd_ws.clear();
+  for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tiles);
+  g_bwd_plans.clear();
   for (auto& kv : g_gemms) {
     cublasLtMatmulDescDestroy(kv.second.op);
     cublasLtMatrixLayoutDestroy(kv.second.a);

@@ -761,6 +761,9 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       if (band) {
         const bool store = rowvalid && !row_glob;
         const float inv = l > 0.f ? 1.0f / l : 0.f;
+        // the row's log-sum-exp, for a backward pass: l sums 2^(s log2e - m_ref)
+        if (store && p.lse != nullptr)
+          p.lse[static_cast<size_t>(wi.bh) * p.L + i] = (m_ref + __log2f(l)) * 0.69314718f;
         const size_t base = (static_cast<size_t>(wi.bh) * p.L + i) * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {

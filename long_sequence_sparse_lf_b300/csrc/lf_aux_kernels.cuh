@@ -58,13 +58,18 @@ __global__ void lf_gather_globals_kernel(const uint4* __restrict__ q, const uint
 // ---------------------------------------------------------------- combine
 // One warp per (bh, g < n_g): merges the key-chunk partials of a global row,
 //   m = max_c m_c,  l = sum_c l_c 2^(m_c - m),  o = sum_c o_c 2^(m_c - m) / l
-// (m in log2 units), and writes the row of the output at position G[g].
+// (m in log2 units), and writes the row of the output at position G[g] (and
+// its log-sum-exp (m + log2 l) ln 2, if lse is given).  Lane c reads chunk c's (m_c, l_c) (32 chunks at a time), the weights are
+// shared by shuffles, and every O load of the chunk loop is independent of
+// the others, so the warp has all its loads in flight at once.
 template <int D>
 __global__ void lf_combine_globals_kernel(const float* __restrict__ part_o,
                                           const float* __restrict__ part_ml,
                                           const int32_t* __restrict__ gidx, void* out, int out_f32,
-                                          int n_g, int NGQ, int n_chunks, int L, int BH) {
+                                          int n_g, int NGQ, int n_chunks, int L, int BH,
+                                          float* __restrict__ lse) {
   constexpr int PER = D / 32;
+  const float NEG_INF = -__int_as_float(0x7f800000);
   const int warps_per_block = blockDim.x / 32;
   const long long wid = (long long)blockIdx.x * warps_per_block + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -72,22 +77,38 @@ __global__ void lf_combine_globals_kernel(const float* __restrict__ part_o,
   const int g = (int)(wid % n_g);
   const long long bh = wid / n_g;
   const size_t base = ((size_t)bh * NGQ + g) * n_chunks;
-  float m = -__int_as_float(0x7f800000);
-  for (int c = 0; c < n_chunks; ++c) m = fmaxf(m, part_ml[(base + c) * 2]);
+  float m = NEG_INF;
+  for (int c0 = 0; c0 < n_chunks; c0 += 32)
+    if (c0 + lane < n_chunks) m = fmaxf(m, part_ml[(base + c0 + lane) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int c = 0; c < n_chunks; ++c) {
-    const float mc = part_ml[(base + c) * 2];
-    const float wgt = (mc == m) ? 1.f : exp2f(mc - m);
-    l += part_ml[(base + c) * 2 + 1] * wgt;
-    const float* src = part_o + (base + c) * D;
+  for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+    // this lane's chunk: its weight 2^(m_c - m) (0 for an empty chunk)
+    float wgt = 0.f, lc = 0.f;
+    if (c0 + lane < n_chunks) {
+      const float mc = part_ml[(base + c0 + lane) * 2];
+      lc = part_ml[(base + c0 + lane) * 2 + 1];
+      wgt = (mc == m) ? 1.f : exp2f(mc - m);
+    }
+    l += wgt * lc;
+    const int nc = min(32, n_chunks - c0);
+#pragma unroll 4
+    for (int c = 0; c < nc; ++c) {
+      const float wc = __shfl_sync(0xffffffffu, wgt, c);
+      const float* src = part_o + (base + c0 + c) * D;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += src[lane + 32 * e] * wgt;
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(src[lane + 32 * e], wc, acc[e]);
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const size_t orow = ((size_t)bh * L + gidx[g]) * D;
+  if (lse != nullptr && lane == 0) lse[(size_t)bh * L + gidx[g]] = (m + __log2f(l)) * 0.69314718f;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
     const float val = acc[e] * inv;

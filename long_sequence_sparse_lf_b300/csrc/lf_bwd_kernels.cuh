@@ -1,0 +1,267 @@
+// Backward of the Longformer sparse attention: dq, dk, dv of sum(out * dout).
+//
+// With s_ij = scale q_i.k_j over the key set K(i) (band(i) ∪ G, or every key
+// for a global row i), p_ij = exp(s_ij - lse_i) (lse from the forward) and
+// out_i = sum_j p_ij v_j, the chain rule gives per attended pair (i, j):
+//   dv_j += p_ij dout_i,   dp_ij = dout_i . v_j,
+//   ds_ij = p_ij (dp_ij - delta_i),   delta_i = dout_i . out_i,
+//   dq_i += scale ds_ij k_j,   dk_j += scale ds_ij q_i.
+// (The pages give only the forward; this is the derivative of its plain
+// definition: "Longformer explained" §2, §4.)
+//
+// The attended pairs split into three classes, each a kernel over 64 x 64
+// blocks of (query rows, key rows):
+//   band        i not global, j in band(i): per 64-key tile of one residue
+//               class (the band is symmetric, so the queries are those of
+//               the key's own window), over the query blocks it reaches;
+//   global keys j global, i not global, j not in band(i): per 64 gathered
+//               global keys, over every query block;
+//   global rows i global, every j: per 64 gathered global rows, over every
+//               key block.
+// Each block pair computes S = Q K^T and dP = dO V^T with WMMA (bf16 in, fp32
+// accumulation) into shared memory, forms P and dS (bf16) element by element
+// with the class's mask, then dV += P^T dO, dK += dS^T Q and dQ += dS K, added
+// into fp32 dq, dk, dv (zeroed first) with atomics.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <mma.h>
+#include <type_traits>
+
+namespace lf {
+
+constexpr int kBwdB = 64;        // rows of a query block and of a key block
+constexpr int kBwdThreads = 128; // four warps
+
+struct BwdParams {
+  const __nv_bfloat16* q;        // [B*H, L, D]
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* dout;
+  const float* lse;              // [B*H, L]
+  const float* delta;            // [B*H, L]
+  float* dq;                     // [B*H, L, D], accumulated
+  float* dk;
+  float* dv;
+  const int32_t* gidx;           // [n_g] sorted global positions
+  const uint8_t* is_glob;        // [L]
+  const int4* tiles;             // band tiles: (bh, residue r, first key t0, dilation d)
+  int n_tiles;
+  const int32_t* head_dil;       // [H]
+  int H, L, w, n_g;
+  float scale;
+};
+
+// delta[bh, i] = dout_i . out_i (bf16 rows, fp32 sum); one warp per row.
+template <int D>
+__global__ void lf_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
+                                    const __nv_bfloat16* __restrict__ dout,
+                                    float* __restrict__ delta, long long rows) {
+  const long long r = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float s = 0.f;
+#pragma unroll
+  for (int e = lane; e < D; e += 32)
+    s += __bfloat162float(out[r * D + e]) * __bfloat162float(dout[r * D + e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) delta[r] = s;
+}
+
+template <int D>
+struct BwdSmem {
+  __nv_bfloat16 q[kBwdB * D], k[kBwdB * D], v[kBwdB * D], dout[kBwdB * D];
+  float s[kBwdB * kBwdB];        // S, then dP
+  float dp[kBwdB * kBwdB];
+  __nv_bfloat16 p[kBwdB * kBwdB], ds[kBwdB * kBwdB];
+  float acc[kBwdB * D];          // product tile before it is added to global memory
+  float lse[kBwdB], delta[kBwdB];
+  int qpos[kBwdB], kpos[kBwdB];  // positions of the block's rows (-1: none)
+  int qglob[kBwdB];              // the query row is a global token
+};
+
+// rows[c] (positions, -1 = none) of X [B*H, L, D] into shared memory (zeros
+// for missing rows); 16 bytes per thread and step
+template <int D>
+__device__ __forceinline__ void bwd_load_rows(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                              size_t bh, int L, const int* rows) {
+  constexpr int PCS = D / 8;
+  for (int x = threadIdx.x; x < kBwdB * PCS; x += blockDim.x) {
+    const int c = x / PCS, pc = x - c * PCS;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (rows[c] >= 0)
+      val = reinterpret_cast<const uint4*>(src + (bh * L + rows[c]) * D)[pc];
+    reinterpret_cast<uint4*>(dst)[x] = val;
+  }
+}
+
+// C[64 x N] (= A[64 x K] B) into shared memory, fp32; A row-major (lda), B
+// row-major [K x N] (b_rowmajor, ldb) or B = X^T for X row-major [N x K]
+// (ldb = K); a_colmajor reads A as the transpose of a row-major [K x 64].
+template <int N, int K, bool A_COL, bool B_ROW>
+__device__ __forceinline__ void bwd_gemm(float* C, int ldc, const __nv_bfloat16* A, int lda,
+                                         const __nv_bfloat16* B, int ldb) {
+  using namespace nvcuda;
+  const int warp = threadIdx.x >> 5;
+  constexpr int TN = N / 16;
+  for (int t = warp; t < 4 * TN; t += kBwdThreads / 32) {
+    const int mi = t / TN, ni = t - mi * TN;
+    wmma::fragment<wmma::accumulator, 16, 16, 16, float> c;
+    wmma::fill_fragment(c, 0.f);
+#pragma unroll
+    for (int kk = 0; kk < K / 16; ++kk) {
+      using ALay = typename std::conditional<A_COL, wmma::col_major, wmma::row_major>::type;
+      using BLay = typename std::conditional<B_ROW, wmma::row_major, wmma::col_major>::type;
+      wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, ALay> a;
+      wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, BLay> b;
+      const __nv_bfloat16* ap = A_COL ? A + (size_t)kk * 16 * lda + mi * 16
+                                      : A + (size_t)mi * 16 * lda + kk * 16;
+      const __nv_bfloat16* bp = B_ROW ? B + (size_t)kk * 16 * ldb + ni * 16
+                                      : B + (size_t)ni * 16 * ldb + kk * 16;
+      wmma::load_matrix_sync(a, ap, lda);
+      wmma::load_matrix_sync(b, bp, ldb);
+      wmma::mma_sync(c, a, b, c);
+    }
+    wmma::store_matrix_sync(C + (size_t)mi * 16 * ldc + ni * 16, c, ldc, wmma::mem_row_major);
+  }
+}
+
+// acc [64 x D] (scaled) added to X[bh, rows[c], :] with atomics
+template <int D>
+__device__ __forceinline__ void bwd_add_rows(float* X, const float* acc, float scale, size_t bh,
+                                             int L, const int* rows) {
+  for (int x = threadIdx.x; x < kBwdB * D; x += blockDim.x) {
+    const int c = x / D, e = x - c * D;
+    if (rows[c] >= 0) atomicAdd(X + (bh * L + rows[c]) * D + e, acc[x] * scale);
+  }
+}
+
+// kind 0: band tile; 1: global keys; 2: global rows.  One CTA per unit.
+template <int D, int KIND>
+__global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) {
+  extern __shared__ __align__(128) uint8_t bwd_smem_raw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(bwd_smem_raw);
+  const float log2e = 1.4426950408889634f;
+  size_t bh;
+  int d = 1, r = 0, Lr = p.L;
+  int n_blocks;                  // blocks of the streamed side
+  int fixed0 = 0;                // first fixed row (residue space / gathered index)
+  if (KIND == 0) {
+    const int4 t = p.tiles[blockIdx.x];
+    bh = (size_t)t.x;
+    r = t.y;
+    fixed0 = t.z;
+    d = t.w;
+    Lr = (p.L - 1 - r) / d + 1;
+    const int s_lo = max(fixed0 - p.w, 0), s_hi = min(fixed0 + kBwdB - 1 + p.w, Lr - 1);
+    n_blocks = (s_hi - s_lo) / kBwdB + 1;
+  } else {
+    const int n_gt = (p.n_g + kBwdB - 1) / kBwdB;
+    bh = blockIdx.x / n_gt;
+    fixed0 = (int)(blockIdx.x % n_gt) * kBwdB;
+    d = p.head_dil[bh % p.H];
+    n_blocks = (p.L + kBwdB - 1) / kBwdB;
+  }
+  // the fixed side: keys (band, global keys) or queries (global rows)
+  int* fixed_pos = (KIND == 2) ? sm.qpos : sm.kpos;
+  for (int c = threadIdx.x; c < kBwdB; c += blockDim.x) {
+    int pos = -1;
+    if (KIND == 0) {
+      if (fixed0 + c < Lr) pos = r + d * (fixed0 + c);
+    } else if (fixed0 + c < p.n_g) {
+      pos = p.gidx[fixed0 + c];
+    }
+    fixed_pos[c] = pos;
+  }
+  __syncthreads();
+  if (KIND == 2) {
+    bwd_load_rows<D>(sm.q, p.q, bh, p.L, sm.qpos);
+    bwd_load_rows<D>(sm.dout, p.dout, bh, p.L, sm.qpos);
+    for (int c = threadIdx.x; c < kBwdB; c += blockDim.x) {
+      sm.lse[c] = sm.qpos[c] >= 0 ? p.lse[bh * p.L + sm.qpos[c]] * log2e : 0.f;
+      sm.delta[c] = sm.qpos[c] >= 0 ? p.delta[bh * p.L + sm.qpos[c]] : 0.f;
+      sm.qglob[c] = 1;
+    }
+  } else {
+    bwd_load_rows<D>(sm.k, p.k, bh, p.L, sm.kpos);
+    bwd_load_rows<D>(sm.v, p.v, bh, p.L, sm.kpos);
+  }
+  const int s_lo = (KIND == 0) ? max(fixed0 - p.w, 0) : 0;
+  const float sl2 = p.scale * log2e;
+
+  for (int blk = 0; blk < n_blocks; ++blk) {
+    __syncthreads();
+    // the streamed side's rows
+    int* str_pos = (KIND == 2) ? sm.kpos : sm.qpos;
+    for (int c = threadIdx.x; c < kBwdB; c += blockDim.x) {
+      int pos = -1;
+      if (KIND == 0) {
+        const int s = s_lo + blk * kBwdB + c;
+        if (s < Lr) pos = r + d * s;
+      } else {
+        const int i = blk * kBwdB + c;
+        if (i < p.L) pos = i;
+      }
+      str_pos[c] = pos;
+    }
+    __syncthreads();
+    if (KIND == 2) {
+      bwd_load_rows<D>(sm.k, p.k, bh, p.L, sm.kpos);
+      bwd_load_rows<D>(sm.v, p.v, bh, p.L, sm.kpos);
+    } else {
+      bwd_load_rows<D>(sm.q, p.q, bh, p.L, sm.qpos);
+      bwd_load_rows<D>(sm.dout, p.dout, bh, p.L, sm.qpos);
+      for (int c = threadIdx.x; c < kBwdB; c += blockDim.x) {
+        sm.lse[c] = sm.qpos[c] >= 0 ? p.lse[bh * p.L + sm.qpos[c]] * log2e : 0.f;
+        sm.delta[c] = sm.qpos[c] >= 0 ? p.delta[bh * p.L + sm.qpos[c]] : 0.f;
+        sm.qglob[c] = sm.qpos[c] >= 0 ? p.is_glob[sm.qpos[c]] : 0;
+      }
+    }
+    __syncthreads();
+    // S = Q K^T, dP = dO V^T   [64 queries x 64 keys]
+    bwd_gemm<kBwdB, D, false, false>(sm.s, kBwdB, sm.q, D, sm.k, D);
+    bwd_gemm<kBwdB, D, false, false>(sm.dp, kBwdB, sm.dout, D, sm.v, D);
+    __syncthreads();
+    // P and dS of the pairs this class owns (0 elsewhere)
+    for (int x = threadIdx.x; x < kBwdB * kBwdB; x += blockDim.x) {
+      const int a = x / kBwdB, b = x - a * kBwdB;   // query row a, key row b
+      const int i = sm.qpos[a], j = sm.kpos[b];
+      bool ok = i >= 0 && j >= 0;
+      if (ok) {
+        if (KIND == 0) {
+          // same residue class by construction; the window in residue space
+          const int ts = (i - r) / d, tk = (j - r) / d;
+          ok = abs(ts - tk) <= p.w && sm.qglob[a] == 0;
+        } else if (KIND == 1) {
+          const int diff = i - j;
+          const bool in_band = abs(diff) <= d * p.w && diff % d == 0;
+          ok = sm.qglob[a] == 0 && !in_band;
+        }
+      }
+      float pv = 0.f, dsv = 0.f;
+      if (ok) {
+        pv = exp2f(sm.s[x] * sl2 - sm.lse[a]);
+        dsv = pv * (sm.dp[x] - sm.delta[a]);
+      }
+      sm.p[x] = __float2bfloat16_rn(pv);
+      sm.ds[x] = __float2bfloat16_rn(dsv);
+    }
+    __syncthreads();
+    // dV_keys += P^T dO, dK_keys += scale dS^T Q, dQ_queries += scale dS K
+    bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.p, kBwdB, sm.dout, D);
+    __syncthreads();
+    bwd_add_rows<D>(p.dv, sm.acc, 1.f, bh, p.L, sm.kpos);
+    __syncthreads();
+    bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.ds, kBwdB, sm.q, D);
+    __syncthreads();
+    bwd_add_rows<D>(p.dk, sm.acc, p.scale, bh, p.L, sm.kpos);
+    __syncthreads();
+    bwd_gemm<D, kBwdB, false, true>(sm.acc, D, sm.ds, kBwdB, sm.k, D);
+    __syncthreads();
+    bwd_add_rows<D>(p.dq, sm.acc, p.scale, bh, p.L, sm.qpos);
+  }
+}
+
+}  // namespace lf

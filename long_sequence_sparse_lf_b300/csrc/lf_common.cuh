@@ -136,6 +136,7 @@ struct MainParams {
   int out_f32;
   float* part_o;                   // [(bh*NGQ + g)*n_chunks + c][D] fp32
   float* part_ml;                  // [(bh*NGQ + g)*n_chunks + c][2] (m, l)
+  float* lse;                      // [B*H, L]: ln sum_{K(i)} exp(scale q.k), or null
   int H, L, w;
   float sl2;                       // scale * log2(e)
   unsigned* status;                // device status word

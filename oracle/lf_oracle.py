@@ -325,3 +325,64 @@ def longformer_layer(x: np.ndarray, w_qkv: np.ndarray, b_qkv: np.ndarray,
     x1 = rnd(layer_norm(xr + a, ln1[0], ln1[1], eps))
     f = x1 @ np.asarray(w_ff, np.float64).T + np.asarray(b_ff, np.float64)
     return rnd(layer_norm(x1 + f, ln2[0], ln2[1], eps))
+
+
+# --------------------------------------------------------------------------
+# Backward of the attention
+# --------------------------------------------------------------------------
+
+def attention_lse(q: np.ndarray, k: np.ndarray, w: int, dilation: Sequence[int],
+                  G: Sequence[int], scale: float, chunk: int = 256) -> np.ndarray:
+    """lse[b, h, i] = ln sum_{j in K(i)} exp(scale * q_i . k_j), float64: the
+    normaliser of the softmax of ``attention``, so that its weights are
+    p_ij = exp(scale q_i.k_j - lse_i)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    B, H, L, D = q.shape
+    out = np.empty((B, H, L), dtype=np.float64)
+    for h in range(H):
+        d = int(dilation[h])
+        for c0 in range(0, L, chunk):
+            r = np.arange(c0, min(L, c0 + chunk))
+            m = mask_rows(r, L, w, d, G)
+            for b in range(B):
+                s = np.where(m, (q[b, h, r, :] @ k[b, h].T) * scale, -np.inf)
+                mx = s.max(axis=1, keepdims=True)
+                out[b, h, r] = (mx + np.log(np.exp(s - mx).sum(axis=1, keepdims=True)))[:, 0]
+    return out
+
+
+def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
+                       w: int, dilation: Sequence[int], G: Sequence[int], scale: float,
+                       chunk: int = 256):
+    """Gradients (dq, dk, dv) of sum(out * dout) for out = attention(q, k, v),
+    float64, dense-masked.  With s_ij = scale q_i.k_j over K(i), the softmax
+    p_ij and out_i = sum_j p_ij v_j (the definition of ``attention``), the
+    chain rule gives, row by row:
+        dv_j  += p_ij dout_i                   (out is linear in v)
+        dp_ij  = dout_i . v_j
+        ds_ij  = p_ij (dp_ij - sum_j' p_ij' dp_ij')   (the softmax's Jacobian)
+        dq_i   = scale sum_j ds_ij k_j,   dk_j += scale ds_ij q_i
+    with p_ij = 0 for j outside K(i).  This is the derivative of the plain
+    definition, written out; the pages give no backward of their own."""
+    q, k, v, dout = (np.asarray(t, dtype=np.float64) for t in (q, k, v, dout))
+    B, H, L, D = q.shape
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(H):
+        d = int(dilation[h])
+        for c0 in range(0, L, chunk):
+            r = np.arange(c0, min(L, c0 + chunk))
+            m = mask_rows(r, L, w, d, G)
+            for b in range(B):
+                s = np.where(m, (q[b, h, r, :] @ k[b, h].T) * scale, -np.inf)
+                s = s - s.max(axis=1, keepdims=True)
+                p = np.exp(s)
+                p /= p.sum(axis=1, keepdims=True)
+                dp = dout[b, h, r, :] @ v[b, h].T
+                ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+                dq[b, h, r, :] = scale * (ds @ k[b, h])
+                dk[b, h] += scale * (ds.T @ q[b, h, r, :])
+                dv[b, h] += p.T @ dout[b, h, r, :]
+    return dq, dk, dv
