@@ -558,6 +558,143 @@ def run_layer(args):
     print(json.dumps(line), flush=True)
     return 0
 
+
+def band_class_pairs(wl) -> int:
+    """Attended pairs (i, j) with i not global and j in band(i), summed over
+    heads and batch: the pairs the backward's band kernel owns.  Per head,
+    sum_i |band(i)| = L + 2 sum_{t=1..w} max(0, L - t d), less the window
+    sizes of the global rows."""
+    G = set(wl.global_idx)
+    total = 0
+    for d in wl.dilation:
+        all_rows = wl.L + 2 * sum(max(0, wl.L - t * d) for t in range(1, wl.w + 1))
+        glob = sum(1 + min(wl.w, g // d) + min(wl.w, (wl.L - 1 - g) // d) for g in G)
+        total += all_rows - glob
+    return total * wl.B
+
+
+def run_backward(args, wl):
+    """The backward (lf_attn_bwd) on a workload: useful FLOPs = 10*B*D*pairs
+    (recomputed S, dP, dV, dK, dQ products per attended pair)."""
+    import long_sequence_sparse_lf_b300 as lf
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lf.load_library()
+    q, k, v = W.make_qkv(wl)
+    g = torch.Generator("cpu").manual_seed(wl.seed + 1000)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, dout))
+    out = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lf.lf_attn_fwd_lse(qd, kd, vd, out, lse, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+    grads = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    _, _, pairs = lf.lf_attn_pairs(wl.H, wl.L, wl.w, wl.dilation, wl.global_idx,
+                                   count_only=True, device=dev)
+    flops = 10 * wl.B * wl.D * pairs
+    band_flops = 10 * wl.D * band_class_pairs(wl)
+
+    def step(bufs):
+        lf.lf_attn_bwd(*bufs, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+
+    bufs = (qd, kd, vd, out, lse, dod, *grads)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(bufs)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    lf.lf_profile_reset()
+    lf.lf_profile_only("bwd_band")
+    lf.lf_profile_enable(True)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = lf.lf_launch_count()
+    for s_ in range(args.steps):
+        flush.zero_()
+        evs[s_][0].record(stream)
+        step(bufs)
+        evs[s_][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = lf.lf_launch_count() - launches0
+    clocks = sampler.stop()
+    lf.lf_profile_enable(False)
+    lf.lf_profile_only(None)
+    total_ms = float(sum(a.elapsed_time(b) for a, b in evs))
+    band_ms, band_n = lf.lf_profile_query("bwd_band")
+    lf.lf_profile_reset()
+    if lf.lf_attn_get_status(stream) != 0:
+        raise SystemExit("device status error in timed region: " + lf.lf_last_error())
+    value = flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: inputs from pinned host memory, gradients back
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    host_in = [t.cpu().pin_memory() for t in (qd, kd, vd, out, lse, dod)]
+    host_out = [torch.empty(q.shape, dtype=torch.float32).pin_memory() for _ in range(3)]
+    dev_in = [torch.empty_like(t) for t in (qd, kd, vd, out, lse, dod)]
+    dev_out = [torch.empty_like(t) for t in grads]
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for dd, hh in zip(dev_in, host_in):
+            dd.copy_(hh, non_blocking=True)
+        step((*dev_in, *dev_out))
+        for hh, dd in zip(host_out, dev_out):
+            hh.copy_(dd, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    peaks, peak_src = load_peaks()
+    band_s = band_ms / max(band_n, 1) * 1e-3
+    ach = band_flops / band_s / 1e12
+    line = {
+        "metric": "banded+global attention backward useful TFLOP/s (10*D per attended pair; "
+                  "1 B300)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; dout from seed+1000)",
+        "config": dict(wl.describe(), l2="flushed between timed steps (256 MiB memset)",
+                       pairs=pairs * wl.B),
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": "bwd_band", "kernel_ms": band_s * 1e3,
+                     "kernel_useful_flops": band_flops,
+                     "peak_source": "measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback"},
+        "gpu_launches": launches,
+        "e2e": {"value": flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "lf_attn_bwd with inputs copied from pinned host memory and the "
+                       "gradients copied back"},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle as O
+        heads = max(1, min(wl.H, 2))
+        qf, kf, vf, df = (t[:1, :heads].double().numpy() for t in (q, k, v, dout))
+        t0 = time.perf_counter()
+        O.attention_backward(qf, kf, vf, df, wl.w, wl.dilation[:heads], wl.global_idx, wl.scale)
+        secs = time.perf_counter() - t0
+        sample_pairs = pairs * heads / wl.H
+        line["cpu_baseline"] = {
+            "value": 10 * wl.D * sample_pairs / secs / 1e12, "unit": "TFLOP/s",
+            "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 dense-masked backward oracle over {heads} (b,h) heads of the "
+                      f"{wl.name} workload"}
+    print(json.dumps(line), flush=True)
+    return 0
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -568,12 +705,20 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward (lf_attn_bwd) on --config instead of the forward")
     ap.add_argument("--layer", default=None, choices=sorted(W.LAYER_CONFIGS),
                     help="time one Longformer layer forward (lf_layer_fwd) instead of the "
                          "attention alone")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.backward:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the backward line has no "
+                              "reference arm"}))
+            return 0
+        return run_backward(args, W.CONFIGS[args.config])
     if args.layer is not None:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the layer line has no "

@@ -1266,7 +1266,8 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   const int dthreads = 256;
   const unsigned dblocks = (unsigned)((rows + dthreads / 32 - 1) / (dthreads / 32));
   const int gt = (n_g + lf::kBwdB - 1) / lf::kBwdB;
-  const long long gunits = (long long)B * H * gt;
+  const int n_sc = ((L + lf::kBwdB - 1) / lf::kBwdB + lf::kBwdChunk - 1) / lf::kBwdChunk;
+  const long long gunits = (long long)B * H * gt * n_sc;
   auto launch_all = [&](auto dc) -> lf_status {
     constexpr int DD = decltype(dc)::value;
     const int smem = (int)sizeof(lf::BwdSmem<DD>);

@@ -18,10 +18,14 @@
 //               global keys, over every query block;
 //   global rows i global, every j: per 64 gathered global rows, over every
 //               key block.
+// The two global classes split their streamed side into chunks of kBwdChunk
+// blocks, one CTA each, so that a few global tokens still fill the GPU.
 // Each block pair computes S = Q K^T and dP = dO V^T with WMMA (bf16 in, fp32
 // accumulation) into shared memory, forms P and dS (bf16) element by element
-// with the class's mask, then dV += P^T dO, dK += dS^T Q and dQ += dS K, added
-// into fp32 dq, dk, dv (zeroed first) with atomics.
+// with the class's mask, then dV += P^T dO, dK += dS^T Q and dQ += dS K.  The
+// CTA's fixed rows (keys, or global rows) sum in shared memory and are added
+// to the fp32 gradients (zeroed first) once, with atomics; the streamed rows'
+// sums are added with atomics after every block pair.
 #pragma once
 
 #include <cstdint>
@@ -32,7 +36,8 @@
 namespace lf {
 
 constexpr int kBwdB = 64;        // rows of a query block and of a key block
-constexpr int kBwdThreads = 128; // four warps
+constexpr int kBwdThreads = 256; // eight warps
+constexpr int kBwdChunk = 8;     // streamed blocks per CTA of the global kernels
 
 struct BwdParams {
   const __nv_bfloat16* q;        // [B*H, L, D]
@@ -77,6 +82,7 @@ struct BwdSmem {
   float dp[kBwdB * kBwdB];
   __nv_bfloat16 p[kBwdB * kBwdB], ds[kBwdB * kBwdB];
   float acc[kBwdB * D];          // product tile before it is added to global memory
+  float st0[kBwdB * D], st1[kBwdB * D];   // the fixed rows' sums over the streamed blocks
   float lse[kBwdB], delta[kBwdB];
   int qpos[kBwdB], kpos[kBwdB];  // positions of the block's rows (-1: none)
   int qglob[kBwdB];              // the query row is a global token
@@ -97,10 +103,10 @@ __device__ __forceinline__ void bwd_load_rows(__nv_bfloat16* dst, const __nv_bfl
   }
 }
 
-// C[64 x N] (= A[64 x K] B) into shared memory, fp32; A row-major (lda), B
+// C[64 x N] (= A[64 x K] B, or C += A B with ACCUM) in shared memory, fp32; A row-major (lda), B
 // row-major [K x N] (b_rowmajor, ldb) or B = X^T for X row-major [N x K]
 // (ldb = K); a_colmajor reads A as the transpose of a row-major [K x 64].
-template <int N, int K, bool A_COL, bool B_ROW>
+template <int N, int K, bool A_COL, bool B_ROW, bool ACCUM = false>
 __device__ __forceinline__ void bwd_gemm(float* C, int ldc, const __nv_bfloat16* A, int lda,
                                          const __nv_bfloat16* B, int ldb) {
   using namespace nvcuda;
@@ -109,7 +115,10 @@ __device__ __forceinline__ void bwd_gemm(float* C, int ldc, const __nv_bfloat16*
   for (int t = warp; t < 4 * TN; t += kBwdThreads / 32) {
     const int mi = t / TN, ni = t - mi * TN;
     wmma::fragment<wmma::accumulator, 16, 16, 16, float> c;
-    wmma::fill_fragment(c, 0.f);
+    if (ACCUM)   // C += A B (C already holds the running sum)
+      wmma::load_matrix_sync(c, C + (size_t)mi * 16 * ldc + ni * 16, ldc, wmma::mem_row_major);
+    else
+      wmma::fill_fragment(c, 0.f);
 #pragma unroll
     for (int kk = 0; kk < K / 16; ++kk) {
       using ALay = typename std::conditional<A_COL, wmma::col_major, wmma::row_major>::type;
@@ -147,6 +156,7 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
   size_t bh;
   int d = 1, r = 0, Lr = p.L;
   int n_blocks;                  // blocks of the streamed side
+  int blk0 = 0;                  // first of them (global classes: this CTA's chunk)
   int fixed0 = 0;                // first fixed row (residue space / gathered index)
   if (KIND == 0) {
     const int4 t = p.tiles[blockIdx.x];
@@ -159,10 +169,15 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
     n_blocks = (s_hi - s_lo) / kBwdB + 1;
   } else {
     const int n_gt = (p.n_g + kBwdB - 1) / kBwdB;
-    bh = blockIdx.x / n_gt;
-    fixed0 = (int)(blockIdx.x % n_gt) * kBwdB;
+    const int all_blocks = (p.L + kBwdB - 1) / kBwdB;
+    const int n_sc = (all_blocks + kBwdChunk - 1) / kBwdChunk;
+    const int sc = (int)(blockIdx.x % n_sc);
+    const size_t unit = blockIdx.x / n_sc;
+    bh = unit / n_gt;
+    fixed0 = (int)(unit % n_gt) * kBwdB;
     d = p.head_dil[bh % p.H];
-    n_blocks = (p.L + kBwdB - 1) / kBwdB;
+    blk0 = sc * kBwdChunk;
+    n_blocks = min(all_blocks, blk0 + kBwdChunk);
   }
   // the fixed side: keys (band, global keys) or queries (global rows)
   int* fixed_pos = (KIND == 2) ? sm.qpos : sm.kpos;
@@ -174,6 +189,10 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
       pos = p.gidx[fixed0 + c];
     }
     fixed_pos[c] = pos;
+  }
+  for (int x = threadIdx.x; x < kBwdB * D; x += blockDim.x) {
+    sm.st0[x] = 0.f;
+    sm.st1[x] = 0.f;
   }
   __syncthreads();
   if (KIND == 2) {
@@ -191,7 +210,7 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
   const int s_lo = (KIND == 0) ? max(fixed0 - p.w, 0) : 0;
   const float sl2 = p.scale * log2e;
 
-  for (int blk = 0; blk < n_blocks; ++blk) {
+  for (int blk = blk0; blk < n_blocks; ++blk) {
     __syncthreads();
     // the streamed side's rows
     int* str_pos = (KIND == 2) ? sm.kpos : sm.qpos;
@@ -249,18 +268,32 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
       sm.ds[x] = __float2bfloat16_rn(dsv);
     }
     __syncthreads();
-    // dV_keys += P^T dO, dK_keys += scale dS^T Q, dQ_queries += scale dS K
-    bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.p, kBwdB, sm.dout, D);
-    __syncthreads();
-    bwd_add_rows<D>(p.dv, sm.acc, 1.f, bh, p.L, sm.kpos);
-    __syncthreads();
-    bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.ds, kBwdB, sm.q, D);
-    __syncthreads();
-    bwd_add_rows<D>(p.dk, sm.acc, p.scale, bh, p.L, sm.kpos);
-    __syncthreads();
-    bwd_gemm<D, kBwdB, false, true>(sm.acc, D, sm.ds, kBwdB, sm.k, D);
-    __syncthreads();
-    bwd_add_rows<D>(p.dq, sm.acc, p.scale, bh, p.L, sm.qpos);
+    // dV_keys += P^T dO, dK_keys += scale dS^T Q, dQ_queries += scale dS K:
+    // the fixed side's rows sum in shared memory over the streamed blocks,
+    // the streamed side's go to global memory with atomics
+    if (KIND == 2) {
+      bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.p, kBwdB, sm.dout, D);
+      __syncthreads();
+      bwd_add_rows<D>(p.dv, sm.acc, 1.f, bh, p.L, sm.kpos);
+      __syncthreads();
+      bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.ds, kBwdB, sm.q, D);
+      __syncthreads();
+      bwd_add_rows<D>(p.dk, sm.acc, p.scale, bh, p.L, sm.kpos);
+      bwd_gemm<D, kBwdB, false, true, true>(sm.st0, D, sm.ds, kBwdB, sm.k, D);
+    } else {
+      bwd_gemm<D, kBwdB, true, true, true>(sm.st0, D, sm.p, kBwdB, sm.dout, D);
+      bwd_gemm<D, kBwdB, true, true, true>(sm.st1, D, sm.ds, kBwdB, sm.q, D);
+      bwd_gemm<D, kBwdB, false, true>(sm.acc, D, sm.ds, kBwdB, sm.k, D);
+      __syncthreads();
+      bwd_add_rows<D>(p.dq, sm.acc, p.scale, bh, p.L, sm.qpos);
+    }
+  }
+  __syncthreads();
+  if (KIND == 2) {
+    bwd_add_rows<D>(p.dq, sm.st0, p.scale, bh, p.L, sm.qpos);
+  } else {
+    bwd_add_rows<D>(p.dv, sm.st0, 1.f, bh, p.L, sm.kpos);
+    bwd_add_rows<D>(p.dk, sm.st1, p.scale, bh, p.L, sm.kpos);
   }
 }
 
