@@ -75,14 +75,25 @@ __global__ void lf_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
   if (lane == 0) delta[r] = s;
 }
 
+// Row strides of the shared-memory tiles, padded by 16 bytes so that the
+// column-wise fragment loads of a tile (P^T, dS^T) do not fall on one bank.
+template <int D>
+struct BwdLd {
+  static constexpr int X = D + 8;       // bf16 [64 x D] tiles (q, k, v, dout)
+  static constexpr int SQ = kBwdB + 4;  // fp32 [64 x 64] (S, dP)
+  static constexpr int PQ = kBwdB + 8;  // bf16 [64 x 64] (P, dS)
+  static constexpr int A = D + 4;       // fp32 [64 x D] (products, sums)
+};
+
 template <int D>
 struct BwdSmem {
-  __nv_bfloat16 q[kBwdB * D], k[kBwdB * D], v[kBwdB * D], dout[kBwdB * D];
-  float s[kBwdB * kBwdB];        // S, then dP
-  float dp[kBwdB * kBwdB];
-  __nv_bfloat16 p[kBwdB * kBwdB], ds[kBwdB * kBwdB];
-  float acc[kBwdB * D];          // product tile before it is added to global memory
-  float st0[kBwdB * D], st1[kBwdB * D];   // the fixed rows' sums over the streamed blocks
+  using LD = BwdLd<D>;
+  __nv_bfloat16 q[kBwdB * LD::X], k[kBwdB * LD::X], v[kBwdB * LD::X], dout[kBwdB * LD::X];
+  float s[kBwdB * LD::SQ];
+  float dp[kBwdB * LD::SQ];
+  __nv_bfloat16 p[kBwdB * LD::PQ], ds[kBwdB * LD::PQ];
+  float acc[kBwdB * LD::A];      // product tile before it is added to global memory
+  float st0[kBwdB * LD::A], st1[kBwdB * LD::A];   // the fixed rows' sums over the streamed blocks
   float lse[kBwdB], delta[kBwdB];
   int qpos[kBwdB], kpos[kBwdB];  // positions of the block's rows (-1: none)
   int qglob[kBwdB];              // the query row is a global token
@@ -99,7 +110,7 @@ __device__ __forceinline__ void bwd_load_rows(__nv_bfloat16* dst, const __nv_bfl
     uint4 val = make_uint4(0, 0, 0, 0);
     if (rows[c] >= 0)
       val = reinterpret_cast<const uint4*>(src + (bh * L + rows[c]) * D)[pc];
-    reinterpret_cast<uint4*>(dst)[x] = val;
+    reinterpret_cast<uint4*>(dst + c * BwdLd<D>::X)[pc] = val;
   }
 }
 
@@ -137,13 +148,15 @@ __device__ __forceinline__ void bwd_gemm(float* C, int ldc, const __nv_bfloat16*
   }
 }
 
-// acc [64 x D] (scaled) added to X[bh, rows[c], :] with atomics
+// acc [64 x D] (row stride BwdLd::A, scaled) added to X[bh, rows[c], :]
+// with atomics
 template <int D>
 __device__ __forceinline__ void bwd_add_rows(float* X, const float* acc, float scale, size_t bh,
                                              int L, const int* rows) {
   for (int x = threadIdx.x; x < kBwdB * D; x += blockDim.x) {
     const int c = x / D, e = x - c * D;
-    if (rows[c] >= 0) atomicAdd(X + (bh * L + rows[c]) * D + e, acc[x] * scale);
+    if (rows[c] >= 0)
+      atomicAdd(X + (bh * L + rows[c]) * D + e, acc[c * BwdLd<D>::A + e] * scale);
   }
 }
 
@@ -152,6 +165,7 @@ template <int D, int KIND>
 __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) {
   extern __shared__ __align__(128) uint8_t bwd_smem_raw[];
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(bwd_smem_raw);
+  using LD = BwdLd<D>;
   const float log2e = 1.4426950408889634f;
   size_t bh;
   int d = 1, r = 0, Lr = p.L;
@@ -190,7 +204,7 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
     }
     fixed_pos[c] = pos;
   }
-  for (int x = threadIdx.x; x < kBwdB * D; x += blockDim.x) {
+  for (int x = threadIdx.x; x < kBwdB * LD::A; x += blockDim.x) {
     sm.st0[x] = 0.f;
     sm.st1[x] = 0.f;
   }
@@ -240,8 +254,8 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
     }
     __syncthreads();
     // S = Q K^T, dP = dO V^T   [64 queries x 64 keys]
-    bwd_gemm<kBwdB, D, false, false>(sm.s, kBwdB, sm.q, D, sm.k, D);
-    bwd_gemm<kBwdB, D, false, false>(sm.dp, kBwdB, sm.dout, D, sm.v, D);
+    bwd_gemm<kBwdB, D, false, false>(sm.s, LD::SQ, sm.q, LD::X, sm.k, LD::X);
+    bwd_gemm<kBwdB, D, false, false>(sm.dp, LD::SQ, sm.dout, LD::X, sm.v, LD::X);
     __syncthreads();
     // P and dS of the pairs this class owns (0 elsewhere)
     for (int x = threadIdx.x; x < kBwdB * kBwdB; x += blockDim.x) {
@@ -261,29 +275,29 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
       }
       float pv = 0.f, dsv = 0.f;
       if (ok) {
-        pv = exp2f(sm.s[x] * sl2 - sm.lse[a]);
-        dsv = pv * (sm.dp[x] - sm.delta[a]);
+        pv = exp2f(sm.s[a * LD::SQ + b] * sl2 - sm.lse[a]);
+        dsv = pv * (sm.dp[a * LD::SQ + b] - sm.delta[a]);
       }
-      sm.p[x] = __float2bfloat16_rn(pv);
-      sm.ds[x] = __float2bfloat16_rn(dsv);
+      sm.p[a * LD::PQ + b] = __float2bfloat16_rn(pv);
+      sm.ds[a * LD::PQ + b] = __float2bfloat16_rn(dsv);
     }
     __syncthreads();
     // dV_keys += P^T dO, dK_keys += scale dS^T Q, dQ_queries += scale dS K:
     // the fixed side's rows sum in shared memory over the streamed blocks,
     // the streamed side's go to global memory with atomics
     if (KIND == 2) {
-      bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.p, kBwdB, sm.dout, D);
+      bwd_gemm<D, kBwdB, true, true>(sm.acc, LD::A, sm.p, LD::PQ, sm.dout, LD::X);
       __syncthreads();
       bwd_add_rows<D>(p.dv, sm.acc, 1.f, bh, p.L, sm.kpos);
       __syncthreads();
-      bwd_gemm<D, kBwdB, true, true>(sm.acc, D, sm.ds, kBwdB, sm.q, D);
+      bwd_gemm<D, kBwdB, true, true>(sm.acc, LD::A, sm.ds, LD::PQ, sm.q, LD::X);
       __syncthreads();
       bwd_add_rows<D>(p.dk, sm.acc, p.scale, bh, p.L, sm.kpos);
-      bwd_gemm<D, kBwdB, false, true, true>(sm.st0, D, sm.ds, kBwdB, sm.k, D);
+      bwd_gemm<D, kBwdB, false, true, true>(sm.st0, LD::A, sm.ds, LD::PQ, sm.k, LD::X);
     } else {
-      bwd_gemm<D, kBwdB, true, true, true>(sm.st0, D, sm.p, kBwdB, sm.dout, D);
-      bwd_gemm<D, kBwdB, true, true, true>(sm.st1, D, sm.ds, kBwdB, sm.q, D);
-      bwd_gemm<D, kBwdB, false, true>(sm.acc, D, sm.ds, kBwdB, sm.k, D);
+      bwd_gemm<D, kBwdB, true, true, true>(sm.st0, LD::A, sm.p, LD::PQ, sm.dout, LD::X);
+      bwd_gemm<D, kBwdB, true, true, true>(sm.st1, LD::A, sm.ds, LD::PQ, sm.q, LD::X);
+      bwd_gemm<D, kBwdB, false, true>(sm.acc, LD::A, sm.ds, LD::PQ, sm.k, LD::X);
       __syncthreads();
       bwd_add_rows<D>(p.dq, sm.acc, p.scale, bh, p.L, sm.qpos);
     }
