@@ -172,7 +172,8 @@ def key_lists(L: int, w: int, dilation: Sequence[int], G: Sequence[int],
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
               dilation: Sequence[int], G: Sequence[int], scale: float,
               rows: Optional[Sequence[int]] = None,
-              chunk: int = 256) -> np.ndarray:
+              chunk: int = 256,
+              rel_bias: Optional[np.ndarray] = None) -> np.ndarray:
     """Longformer sparse self-attention forward, dense-masked, float64.
 
     q, k, v: arrays [B, H, L, D] (any float type; promoted to float64).
@@ -184,6 +185,14 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
     (exact exclusion: the reading of "attends only to" in [LF-explained] §2),
     one row softmax ([LF-explained] §4: the patterns share one normalisation),
     then the product with V.
+
+    rel_bias ([H, 2w+1] or None): a relative-position bias on the window's
+    scores.  [LF-explained] §5 (position-encoding adaptations) says local
+    attention is strengthened by a relative position bias but gives no
+    formula.  The form chosen here: for a non-global row i and a key
+    j = i + d*t of its window (|t| <= w), s_ij += rel_bias[h, t + w];
+    scores of global keys outside the window, and of global rows, carry no
+    bias.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -199,8 +208,18 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
         for c0 in range(0, rows_arr.size, chunk):
             r = rows_arr[c0:c0 + chunk]
             m = mask_rows(r, L, w, d, G)
+            bias = None
+            if rel_bias is not None:
+                # the window's offsets t = (j - i) / d of each (row, key)
+                diff = np.arange(L)[None, :] - r[:, None]
+                in_band = (np.abs(diff) <= d * w) & (diff % d == 0)
+                in_band &= ~np.isin(r, np.asarray(G, dtype=np.int64))[:, None]
+                t = np.clip(diff // d + w, 0, 2 * w)
+                bias = np.where(in_band, np.asarray(rel_bias, np.float64)[h][t], 0.0)
             for b in range(B):
                 s = (q[b, h, r, :] @ k[b, h].T) * scale
+                if bias is not None:
+                    s = s + bias
                 s = np.where(m, s, -np.inf)
                 s = s - s.max(axis=1, keepdims=True)
                 p = np.exp(s)
