@@ -699,6 +699,124 @@ def run_backward(args, wl):
     print(json.dumps(line), flush=True)
     return 0
 
+def run_bias(args, wl):
+    """The relative-position-bias forward (lf_attn_fwd_bias) on a workload:
+    useful FLOPs = 4*B*D*pairs, as the plain forward's.  The bias table is
+    N(0,1) fp32 [H, 2w+1], seeded."""
+    import long_sequence_sparse_lf_b300 as lf
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lf.load_library()
+    q, k, v = W.make_qkv(wl)
+    g = torch.Generator("cpu").manual_seed(wl.seed + 2000)
+    rb = torch.randn((wl.H, 2 * wl.w + 1), generator=g)
+    qd, kd, vd, rbd = (t.to(dev) for t in (q, k, v, rb))
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    _, _, pairs = lf.lf_attn_pairs(wl.H, wl.L, wl.w, wl.dilation, wl.global_idx,
+                                   count_only=True, device=dev)
+    flops = 4 * wl.B * wl.D * pairs
+
+    def step(a, b, c, t, o):
+        lf.lf_attn_fwd_bias(a, b, c, o, t, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(qd, kd, vd, rbd, out)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    lf.lf_profile_reset()
+    lf.lf_profile_only("attn_main")
+    lf.lf_profile_enable(True)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = lf.lf_launch_count()
+    for s_ in range(args.steps):
+        flush.zero_()
+        evs[s_][0].record(stream)
+        step(qd, kd, vd, rbd, out)
+        evs[s_][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = lf.lf_launch_count() - launches0
+    clocks = sampler.stop()
+    lf.lf_profile_enable(False)
+    lf.lf_profile_only(None)
+    total_ms = float(sum(a.elapsed_time(b) for a, b in evs))
+    main_ms, main_n = lf.lf_profile_query("attn_main")
+    lf.lf_profile_reset()
+    if lf.lf_attn_get_status(stream) != 0:
+        raise SystemExit("device status error in timed region: " + lf.lf_last_error())
+    value = flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: q, k, v and the table from pinned host memory, out back
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    host_in = [t.pin_memory() for t in (q, k, v, rb)]
+    host_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    dev_in = [torch.empty_like(t) for t in (qd, kd, vd, rbd)]
+    dev_out = torch.empty_like(out)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for dd, hh in zip(dev_in, host_in):
+            dd.copy_(hh, non_blocking=True)
+        step(*dev_in, dev_out)
+        host_out.copy_(dev_out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    peaks, peak_src = load_peaks()
+    main_s = main_ms / max(main_n, 1) * 1e-3
+    ach = flops / main_s / 1e12
+    line = {
+        "metric": "banded+global attention forward with relative position bias, useful "
+                  "TFLOP/s (4*D per attended pair; 1 B300)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; bias N(0,1) fp32 from seed+2000)",
+        "config": dict(wl.describe(), l2="flushed between timed steps (256 MiB memset)",
+                       pairs=pairs * wl.B, rel_bias="[H, 2w+1] fp32"),
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": "attn_main (bias build)", "kernel_ms": main_s * 1e3,
+                     "peak_source": "measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback"},
+        "gpu_launches": launches,
+        "e2e": {"value": flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "lf_attn_fwd_bias with q, k, v and the table copied from pinned host "
+                       "memory and the output copied back"},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle as O
+        rows = list(range(0, wl.L, max(1, wl.L // 256)))
+        qf, kf, vf = (t[:1].double().numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        O.attention(qf, kf, vf, wl.w, wl.dilation, wl.global_idx, wl.scale, rows=rows,
+                    rel_bias=rb.double().numpy())
+        secs = time.perf_counter() - t0
+        sample_pairs = pairs * len(rows) / wl.L
+        line["cpu_baseline"] = {
+            "value": 4 * wl.D * sample_pairs / secs / 1e12, "unit": "TFLOP/s",
+            "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 dense-masked oracle with the bias, {len(rows)} evenly spaced rows of "
+                      f"every head of one batch element of the {wl.name} workload"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,6 +832,8 @@ def main():
     ap.add_argument("--layer", default=None, choices=sorted(W.LAYER_CONFIGS),
                     help="time one Longformer layer forward (lf_layer_fwd) instead of the "
                          "attention alone")
+    ap.add_argument("--rel-bias", action="store_true",
+                    help="time the relative-position-bias forward (lf_attn_fwd_bias) on --config")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -723,6 +843,12 @@ def main():
                               "reference arm"}))
             return 0
         return run_backward(args, W.CONFIGS[args.config])
+    if args.rel_bias:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the bias line has no "
+                              "reference arm"}))
+            return 0
+        return run_bias(args, W.CONFIGS[args.config])
     if args.layer is not None:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the layer line has no "

@@ -87,6 +87,32 @@ LF_API lf_status lf_attn_fwd(const void* q, const void* k, const void* v, void* 
                       int n_global, float scale, lf_stream_t stream);
 
 /*
+ * lf_attn_fwd_bias — lf_attn_fwd with a relative-position bias on the
+ * window's scores.  Longformer explained, §5 (position-encoding adaptations), says
+ * local attention is strengthened by a relative position bias but gives no
+ * formula.  The form implemented: for a non-global row i and a key
+ * j = i + d*t of its window (|t| <= w),
+ *   s_ij = scale * q_i . k_j + rel_bias[h, t + w];
+ * global keys outside the window and global rows carry no bias.
+ *   rel_bias  device, fp32 [H, 2w+1], row-major, read only; values of
+ *             magnitude up to 1e4 (-1e4 already removes a key: its weight
+ *             falls below 2^-125).  Larger magnitudes are not checked and
+ *             not supported: the exponentials take s*scale*log2(e) minus a
+ *             rounded copy of the row maximum, and beyond about 2^30 the
+ *             rounding alone overflows them.
+ * Other arguments and errors as lf_attn_fwd; LF_ERR_INVALID_ARG also for a
+ * null or misaligned rel_bias.  Two launches on `stream`: a copy of the table
+ * scaled by 1/scale and zero-padded on both sides (into a workspace the
+ * library keeps per device and stream, freed by lf_plan_cache_clear), then a
+ * separate build of the attention kernel that adds it to the window's
+ * scores; lf_attn_fwd's kernel is unchanged.
+ */
+LF_API lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v, void* out,
+                                  const float* rel_bias, int B, int H, int L, int D, int w,
+                                  const int32_t* dilation, const int32_t* global_idx,
+                                  int n_global, float scale, lf_stream_t stream);
+
+/*
  * lf_attn_fwd_lse — lf_attn_fwd that also writes each row's log-sum-exp,
  *   lse[b,h,i] = ln( sum_{j in K(i)} exp(scale * q_i . k_j) )   (fp32),
  * the normaliser a backward pass needs (p_ij = exp(scale q_i.k_j - lse_i)).

@@ -84,6 +84,9 @@ def load_library() -> ctypes.CDLL:
     lib.lf_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip,
                                 ip, i32, f32, vp]
     lib.lf_attn_bwd.restype = i32
+    lib.lf_attn_fwd_bias.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip, ip, i32,
+                                     f32, vp]
+    lib.lf_attn_fwd_bias.restype = i32
     _lib = lib
     return lib
 
@@ -347,6 +350,23 @@ def lf_attn_fwd_lse(q, k, v, out, lse, w: int, dilation: Sequence[int],
                                lse.data_ptr(), B, H, L, D, int(w), _i32_array(dilation),
                                _i32_array(global_idx), len(global_idx), float(scale),
                                _stream_handle(stream)))
+
+
+def lf_attn_fwd_bias(q, k, v, out, rel_bias, w: int, dilation: Sequence[int],
+                     global_idx: Sequence[int], scale: float, stream=None):
+    """bf16 forward with a relative-position bias on the window's scores:
+    rel_bias is fp32 cuda [H, 2w+1] with |values| <= 1e4; a non-global row i
+    gains rel_bias[h, t + w] on the score of its window key i + d*t."""
+    _check_qkv(q, k, v, out, torch.bfloat16, "cuda")
+    B, H, L, D = q.shape
+    if (rel_bias.dtype != torch.float32 or rel_bias.device.type != "cuda"
+            or tuple(rel_bias.shape) != (H, 2 * int(w) + 1) or not rel_bias.is_contiguous()):
+        raise ValueError("rel_bias must be a contiguous fp32 cuda tensor [H, 2w+1]")
+    lib = load_library()
+    _check(lib.lf_attn_fwd_bias(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                rel_bias.data_ptr(), B, H, L, D, int(w), _i32_array(dilation),
+                                _i32_array(global_idx), len(global_idx), float(scale),
+                                _stream_handle(stream)))
 
 
 def lf_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, w: int, dilation: Sequence[int],

@@ -152,7 +152,9 @@ lf_status get_dev(DevState** out, int* dev_out) {
     // The attention kernel hands registers between its warpgroups
     // (setmaxnreg); the split assumes the launch allocation kRegsLaunch.
     for (const void* fn : {reinterpret_cast<const void*>(lf::lf_attn_main_kernel<64>),
-                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128>)}) {
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128>),
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<64, true>),
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128, true>)}) {
       cudaFuncAttributes fa;
       LF_CUDA(cudaFuncGetAttributes(&fa, fn));
       if (fa.numRegs != (int)lf::kRegsLaunch)
@@ -164,6 +166,12 @@ lf_status get_dev(DevState** out, int* dev_out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)lf::KCfg<64>::SMEM_BYTES));
     LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)lf::KCfg<128>::SMEM_BYTES));
+    LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<64, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)lf::KCfg<64>::SMEM_BYTES));
+    LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<128, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)lf::KCfg<128>::SMEM_BYTES));
     ds.ready = true;
@@ -552,7 +560,7 @@ lf_status get_workspace(int dev, cudaStream_t stream, size_t bytes, uint8_t** ou
 // plan and every device address they embed, so that a repeated call encodes
 // nothing.
 using ParamKey = std::tuple<const Plan*, const void*, const void*, const void*, void*, bool,
-                            const uint8_t*, float, float*>;
+                            const uint8_t*, float, float*, const float*>;
 std::map<ParamKey, std::unique_ptr<MainParams>> g_params;
 constexpr size_t kMaxCachedParams = 256;
 
@@ -562,7 +570,7 @@ constexpr size_t kMaxCachedParams = 256;
 lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, const void* qb,
                        const void* kb, const void* vb, void* out, bool f32, uint8_t* ws,
                        size_t off_g, size_t off_po, size_t off_pm, float scale, float* lse,
-                       MainParams* prm_out) {
+                       const float* rel_bias, MainParams* prm_out) {
   lf_status s = LF_OK;
   const Plan* pl = &plan;
   const Pattern* pat = &pattern;
@@ -607,6 +615,7 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
   P.w = w;
   P.sl2 = scale * 1.4426950408889634f;
   P.lse = lse;
+  P.rel_bias = rel_bias;
   P.status = ds->status;
   P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
@@ -615,7 +624,8 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
 
 lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool f32, int B, int H,
                    int L, int D, int w, const int32_t* dilation, const int32_t* gidx, int n_g,
-                   float scale, cudaStream_t stream, float* lse = nullptr) {
+                   float scale, cudaStream_t stream, float* lse = nullptr,
+                   const float* rel_bias = nullptr) {
   t_last_error.clear();
   if (B < 1) return fail(LF_ERR_INVALID_ARG, "B=%d must be >= 1", B);
   lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
@@ -675,7 +685,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
     vb = cq + 2 * elems;
   }
 
-  const ParamKey pkey{pl, qb, kb, vb, out, f32, ws, scale, lse};
+  const ParamKey pkey{pl, qb, kb, vb, out, f32, ws, scale, lse, rel_bias};
   MainParams* cached = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -688,7 +698,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   if (cached == nullptr) {
     auto fresh = std::make_unique<MainParams>();
     if ((s = build_params(ds, *pl, *pat, qb, kb, vb, out, f32, ws, off_g, off_po, off_pm, scale,
-                          lse, fresh.get())) != LF_OK)
+                          lse, rel_bias, fresh.get())) != LF_OK)
       return s;
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_params.size() >= kMaxCachedParams) g_params.clear();
@@ -713,8 +723,12 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   if (prm.n_items > 0) {
     const int grid = pl->grid;
     traced("attn_main", stream, [&] {
-      if (D == 64)
+      if (D == 64 && rel_bias)
+        lf::lf_attn_main_kernel<64, true><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
+      else if (D == 64)
         lf::lf_attn_main_kernel<64><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
+      else if (rel_bias)
+        lf::lf_attn_main_kernel<128, true><<<grid, lf::KCfg<128>::THREADS, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
       else
         lf::lf_attn_main_kernel<128><<<grid, lf::KCfg<128>::THREADS, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
     });
@@ -1307,6 +1321,50 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   return LF_OK;
 }
 
+// lf_attn_fwd_bias: the zero-padded, 1/scale-scaled, four-way shifted copy
+// of the bias table (lf_bias_pad_kernel, into a per-(device, stream)
+// workspace), then the forward with the BIAS attention kernel.
+std::map<std::pair<int, cudaStream_t>, LayerWorkspace> g_bias_ws;
+
+lf_status bias_fwd_impl(const void* q, const void* k, const void* v, void* out,
+                        const float* rel_bias, int B, int H, int L, int D, int w,
+                        const int32_t* dilation, const int32_t* gidx, int n_g, float scale,
+                        cudaStream_t stream) {
+  t_last_error.clear();
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  if (rel_bias == nullptr || (reinterpret_cast<uintptr_t>(rel_bias) & 3u) != 0)
+    return fail(LF_ERR_INVALID_ARG, "rel_bias must be a 4-byte aligned device pointer");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(LF_ERR_INVALID_ARG, "scale=%g must be positive and finite", (double)scale);
+  int dev = 0;
+  LF_CUDA(cudaGetDevice(&dev));
+  if (w > (1 << 24)) return fail(LF_ERR_UNSUPPORTED, "w=%d too large for the bias table", w);
+  const size_t rs = 4 * (size_t)lf::bias_row_len(w);
+  if ((size_t)H * rs > (size_t)INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "bias table too large");
+  float* tbl = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    LayerWorkspace& wsp = g_bias_ws[{dev, stream}];
+    const size_t need = align_up((size_t)H * rs * 4, 256);
+    if (wsp.bytes < need) {
+      if (wsp.ptr) LF_CUDA(cudaFreeAsync(wsp.ptr, stream));
+      wsp.ptr = nullptr;
+      wsp.bytes = 0;
+      LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&wsp.ptr), need, stream));
+      wsp.bytes = need;
+    }
+    tbl = reinterpret_cast<float*>(wsp.ptr);
+  }
+  const int n = H * (int)rs;
+  traced("bias_pad", stream, [&] {
+    lf::lf_bias_pad_kernel<<<(n + 255) / 256, 256, 0, stream>>>(rel_bias, tbl, H, w, 1.0f / scale);
+  });
+  LF_CUDA(cudaGetLastError());
+  return fwd_impl(q, k, v, out, false, B, H, L, D, w, dilation, gidx, n_g, scale, stream, nullptr,
+                  tbl);
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -1319,6 +1377,20 @@ lf_status lf_attn_fwd(const void* q, const void* k, const void* v, void* out, in
   try {
     return fwd_impl(q, k, v, out, false, B, H, L, D, w, dilation, global_idx, n_global, scale,
                     static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v, void* out,
+                           const float* rel_bias, int B, int H, int L, int D, int w,
+                           const int32_t* dilation, const int32_t* global_idx, int n_global,
+                           float scale, lf_stream_t stream) {
+  try {
+    return bias_fwd_impl(q, k, v, out, rel_bias, B, H, L, D, w, dilation, global_idx, n_global,
+                         scale, static_cast<cudaStream_t>(stream));
   } catch (const std::exception& e) {
     return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
   } catch (...) {
@@ -1499,6 +1571,9 @@ void lf_plan_cache_clear(void) {
   for (auto& kv : g_bwd_ws)
     if (kv.second.ptr) cudaFree(kv.second.ptr);
   g_bwd_ws.clear();
+  for (auto& kv : g_bias_ws)
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+  g_bias_ws.clear();
   for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tiles);
   g_bwd_plans.clear();
   for (auto& kv : g_gemms) {

@@ -200,7 +200,10 @@ __device__ __noinline__ bool issue_pv_block(uint32_t b0, int X, uint32_t sV, uin
   return true;
 }
 
-template <int D>
+// BIAS: the relative-position-bias variant (p.rel_bias): each window key
+// j = i + d*t of a non-global row gains rel_bias[h][t + w] on its scaled
+// score.  A separate instantiation, so the kernel without it is unchanged.
+template <int D, bool BIAS = false>
 __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_constant__ MainParams p) {
   using C = KCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -632,6 +635,30 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             tmem_ld64(tS + 64 * hf, r);
 #pragma unroll
             for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
+          }
+          if (BIAS && band && j < wi.nkb) {
+            // rel_bias / scale added to the raw score, so that everything
+            // after (max, rescale, exponentials) sees scale*q.k + rel_bias.
+            // The row's 64 values start at I = kBiasPad + w + kpos0 - t in
+            // the zero-padded table (t the row's residue index; the columns
+            // outside the window read padding or neighbours and are masked
+            // below).  Copy I % 4 of the table is shifted so that this start
+            // is 16-byte aligned: sixteen 16-byte loads.
+            const int I = kBiasPad + p.w + wi.kb0 + kBN * j + 64 * hf - (wi.t0 + kBM * X + row);
+            const int sft = I & 3;
+            const float4* tp = reinterpret_cast<const float4*>(
+                p.rel_bias + static_cast<size_t>((wi.bh % p.H) * 4 + sft) * bias_row_len(p.w) +
+                (I - sft));
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float4 bv = __ldg(tp + e);
+              const float2 lo = add2(make_float2(s[4 * e], s[4 * e + 1]), make_float2(bv.x, bv.y));
+              const float2 hi = add2(make_float2(s[4 * e + 2], s[4 * e + 3]), make_float2(bv.z, bv.w));
+              s[4 * e] = lo.x;
+              s[4 * e + 1] = lo.y;
+              s[4 * e + 2] = hi.x;
+              s[4 * e + 3] = hi.y;
+            }
           }
           if (!C::P_ALIAS && (hf == 1 || !live1)) {
             tc_fence_before();

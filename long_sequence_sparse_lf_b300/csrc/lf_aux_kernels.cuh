@@ -217,4 +217,19 @@ __global__ void lf_pairs_fill_kernel(const int32_t* __restrict__ dil, const int3
   }
 }
 
+// The bias table as the BIAS attention kernel reads it: four copies per
+// head, copy c of head h at (4h + c) * bias_row_len(w), whose entry x holds
+// rel_bias[h, x + c - kBiasPad] * inv_scale where that index is in [0, 2w]
+// and 0 elsewhere.  A row whose values start at index I of the padded table
+// reads copy I % 4 from I - I % 4, a 16-byte aligned address.
+__global__ void lf_bias_pad_kernel(const float* __restrict__ rb, float* __restrict__ out, int H,
+                                   int w, float inv_scale) {
+  const int rl = bias_row_len(w);
+  const int n = 4 * H * rl;
+  for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < n; x += gridDim.x * blockDim.x) {
+    const int row = x / rl, h = row >> 2, c = (x - row * rl) + (row & 3) - kBiasPad;
+    out[x] = (c >= 0 && c <= 2 * w) ? rb[static_cast<size_t>(h) * (2 * w + 1) + c] * inv_scale : 0.f;
+  }
+}
+
 }  // namespace lf

@@ -19,6 +19,15 @@ namespace lf {
 constexpr int kMaxDilSlots = 8;     // distinct dilation values per call
 constexpr int kBM = 128;            // query rows per tile (MMA M)
 constexpr int kBN = 128;            // keys per band block (MMA N)
+// Zero padding on each side of a head's row of the bias table: a band
+// block's column offsets kpos - t stay within +-(w + kBM + kBN - 2).
+constexpr int kBiasPad = 256;
+static_assert(kBiasPad >= kBM + kBN - 2, "bias padding too small");
+// Length (floats, a multiple of 4) of one shifted copy of a head's padded
+// bias row: 2w+1 values and kBiasPad zeros on each side.
+__host__ __device__ __forceinline__ int bias_row_len(int w) {
+  return (2 * w + 1 + 2 * kBiasPad + 3) & ~3;
+}
 
 enum : uint32_t { kStatusTimeout = 1u, kStatusBadItem = 2u };
 
@@ -137,6 +146,8 @@ struct MainParams {
   float* part_o;                   // [(bh*NGQ + g)*n_chunks + c][D] fp32
   float* part_ml;                  // [(bh*NGQ + g)*n_chunks + c][2] (m, l)
   float* lse;                      // [B*H, L]: ln sum_{K(i)} exp(scale q.k), or null
+  const float* rel_bias;           // [H, 4, bias_row_len(w)]: rel_bias/scale, zero-padded,
+                                   // copy c shifted by c (the BIAS kernel only)
   int H, L, w;
   float sl2;                       // scale * log2(e)
   unsigned* status;                // device status word
