@@ -11,7 +11,8 @@ Sources (web pages; cited by title and section):
                   至O(n)的实现" (block-sparse Longformer), sections 2-4.
   [Reformer-hash] "Reformer哈希", section "核心原理" (the attention formula).
   [Eff-survey]    the commentary on "Efficient Transformers: A Survey",
-                  section 2.1 (where the cost of dense attention comes from).
+                  section 2.1 (where the cost of dense attention comes from),
+                  sections 3.1-3.2 (strided and BigBird random patterns).
   [LF-blocksparse] §6 "Longformer的整体架构" also defines the layer around the
                   attention (``longformer_layer`` below).
 
@@ -24,6 +25,8 @@ in the repository's design notes and repeated at each function):
                   ([LF-explained] §2 sliding window; §2 dilated window)
     K(i)    = [0, L)          if i in G      ([LF-explained] §2 global attention)
             = band(i) ∪ G     otherwise      (the union, each key once)
+            (∪ X(i), the tile's extra key blocks, when a random / strided
+             block table is given: ``extra_block_keys``)
     s_ij    = scale * <q_i, k_j>             ([Reformer-hash] 核心原理 formula)
     p_ij    = exp(s_ij - max_{K(i)} s) / sum_{j' in K(i)} exp(s_ij' - max)
     out_i   = sum_{j in K(i)} p_ij v_j       (one softmax over all of K(i):
@@ -66,19 +69,60 @@ def band_offsets(i: int, L: int, w: int, d: int) -> List[int]:
     return keys
 
 
-def key_set(i: int, L: int, w: int, d: int, G: Sequence[int]) -> List[int]:
-    """K(i) as a sorted list (see the module docstring)."""
+XBLOCK = 128   # keys per extra block and queries per tile (residue space)
+
+
+def tiles_per_class(L: int, d: int) -> int:
+    """Query tiles of XBLOCK rows in the longest residue class of a head."""
+    return -(-(-(-L // d)) // XBLOCK)
+
+
+def extra_block_keys(i: int, L: int, d: int, xb_h) -> List[int]:
+    """X(i): the extra key blocks of query i's tile, as positions.
+
+    BigBird adds random key blocks to window + global attention; the survey
+    commentary also names a fixed-stride pattern as the deterministic
+    alternative ([Eff-survey] §3.1 fixed patterns, §3.2 combined patterns).
+    Neither gives a block size or an indexing, so the reading taken here:
+    with r = i mod d and t = i div d (the residue space of the dilated
+    window), the row belongs to tile qt = t div 128 of class r, and
+    xb_h[r * tiles_per_class(L, d) + qt] lists key blocks kb (-1 = none);
+    block kb holds the keys r + d*t' for 128*kb <= t' < 128*kb + 128 of the
+    same class, clipped to [0, L).  A random table gives BigBird's random
+    blocks, a table listing every s-th block the strided pattern.
+    """
+    r, t = i % d, i // d
+    nqt = tiles_per_class(L, d)
+    keys = set()
+    for kb in np.asarray(xb_h[r * nqt + t // XBLOCK]).ravel():
+        kb = int(kb)
+        if kb < 0:
+            continue
+        for tt in range(kb * XBLOCK, kb * XBLOCK + XBLOCK):
+            j = r + d * tt
+            if j < L:
+                keys.add(j)
+    return sorted(keys)
+
+
+def key_set(i: int, L: int, w: int, d: int, G: Sequence[int], xb_h=None) -> List[int]:
+    """K(i) as a sorted list (see the module docstring); ``xb_h`` (one head's
+    extra-block table, see :func:`extra_block_keys`) adds X(i) to a
+    non-global row."""
     Gs = set(int(g) for g in G)
     if i in Gs:
         # [LF-explained] §2 global attention: a global token sees the whole
         # sequence.
         return list(range(L))
     # Every token also attends to the global tokens ([LF-blocksparse] §4).
-    return sorted(set(band_offsets(i, L, w, d)) | Gs)
+    keys = set(band_offsets(i, L, w, d)) | Gs
+    if xb_h is not None:
+        keys |= set(extra_block_keys(i, L, d, xb_h))
+    return sorted(keys)
 
 
 def mask_rows(rows: np.ndarray, L: int, w: int, d: int,
-              G: Sequence[int]) -> np.ndarray:
+              G: Sequence[int], xb_h=None) -> np.ndarray:
     """Boolean [len(rows), L] mask, True where key j is in K(row).
 
     Vectorised form of :func:`key_set`: j is in band(i) iff |i-j| <= d*w and
@@ -89,6 +133,9 @@ def mask_rows(rows: np.ndarray, L: int, w: int, d: int,
     i = rows[:, None]
     diff = j - i
     m = (np.abs(diff) <= d * w) & (diff % d == 0)
+    if xb_h is not None:
+        for n, row in enumerate(rows.tolist()):
+            m[n, extra_block_keys(row, L, d, xb_h)] = True
     G = np.asarray(G, dtype=np.int64)
     if G.size:
         m[:, G] = True
@@ -173,7 +220,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
               dilation: Sequence[int], G: Sequence[int], scale: float,
               rows: Optional[Sequence[int]] = None,
               chunk: int = 256,
-              rel_bias: Optional[np.ndarray] = None) -> np.ndarray:
+              rel_bias: Optional[np.ndarray] = None,
+              xblocks: Optional[np.ndarray] = None) -> np.ndarray:
     """Longformer sparse self-attention forward, dense-masked, float64.
 
     q, k, v: arrays [B, H, L, D] (any float type; promoted to float64).
@@ -193,6 +241,10 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
     j = i + d*t of its window (|t| <= w), s_ij += rel_bias[h, t + w];
     scores of global keys outside the window, and of global rows, carry no
     bias.
+
+    xblocks ([H, T, R] integer table or None): extra key blocks per query
+    tile (BigBird random / strided blocks, see :func:`extra_block_keys`),
+    added to K(i) of every non-global row.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -207,7 +259,7 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, w: int,
         d = int(dilation[h])
         for c0 in range(0, rows_arr.size, chunk):
             r = rows_arr[c0:c0 + chunk]
-            m = mask_rows(r, L, w, d, G)
+            m = mask_rows(r, L, w, d, G, None if xblocks is None else xblocks[h])
             bias = None
             if rel_bias is not None:
                 # the window's offsets t = (j - i) / d of each (row, key)
