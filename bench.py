@@ -699,10 +699,41 @@ def run_backward(args, wl):
     print(json.dumps(line), flush=True)
     return 0
 
-def run_bias(args, wl):
-    """The relative-position-bias forward (lf_attn_fwd_bias) on a workload:
-    useful FLOPs = 4*B*D*pairs, as the plain forward's.  The bias table is
-    N(0,1) fp32 [H, 2w+1], seeded."""
+def extra_block_pairs(wl, tab) -> int:
+    """Attended pairs that a table of extra key blocks adds, summed over heads
+    and batch: per tile, its listed blocks' keys (deduplicated, clipped to the
+    class) that are not global, times its non-global rows whose window does
+    not already hold them (|t' - t| > w in residue space)."""
+    tab = np.asarray(tab)
+    L, w = wl.L, wl.w
+    isg = np.zeros(L, dtype=bool)
+    isg[list(wl.global_idx)] = True
+    total = 0
+    for h, d in enumerate(wl.dilation):
+        nqt = W.tiles_per_class(L, d)
+        for r in range(d):
+            pos = np.arange(r, L, d)
+            Lr = pos.size
+            for qt in range(nqt):
+                rows = np.arange(qt * W.TILE, min(qt * W.TILE + W.TILE, Lr))
+                kbs = sorted(set(int(x) for x in tab[h, r * nqt + qt] if x >= 0))
+                if rows.size == 0 or not kbs:
+                    continue
+                keys = np.concatenate([np.arange(kb * W.TILE, min(kb * W.TILE + W.TILE, Lr))
+                                       for kb in kbs])
+                keys = keys[~isg[pos[keys]]]
+                rows = rows[~isg[pos[rows]]]
+                total += int((np.abs(keys[None, :] - rows[:, None]) > w).sum())
+    return total * wl.B
+
+
+def run_variant(args, wl, variant: str):
+    """A forward variant on a workload, timed like the plain forward:
+      "bias"           lf_attn_fwd_bias, table N(0,1) fp32 [H, 2w+1];
+      "blocks-random"  lf_attn_fwd_blocks, 3 random key blocks per tile
+                       (BigBird-style), seeded;
+      "blocks-strided" lf_attn_fwd_blocks, key blocks 0, 8, 16, ... per tile.
+    Useful FLOPs = 4*D per attended pair (the variant's own key sets)."""
     import long_sequence_sparse_lf_b300 as lf
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
@@ -713,22 +744,53 @@ def run_bias(args, wl):
     dev = torch.device("cuda", local)
     lf.load_library()
     q, k, v = W.make_qkv(wl)
-    g = torch.Generator("cpu").manual_seed(wl.seed + 2000)
-    rb = torch.randn((wl.H, 2 * wl.w + 1), generator=g)
-    qd, kd, vd, rbd = (t.to(dev) for t in (q, k, v, rb))
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
     out = torch.empty_like(qd)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     _, _, pairs = lf.lf_attn_pairs(wl.H, wl.L, wl.w, wl.dilation, wl.global_idx,
                                    count_only=True, device=dev)
-    flops = 4 * wl.B * wl.D * pairs
+    pairs *= wl.B
+    extra_host = []        # host inputs copied each e2e step (besides q, k, v)
+    if variant == "bias":
+        g = torch.Generator("cpu").manual_seed(wl.seed + 2000)
+        rb = torch.randn((wl.H, 2 * wl.w + 1), generator=g)
+        rbd = rb.to(dev)
+        extra_host = [rb]
 
-    def step(a, b, c, t, o):
-        lf.lf_attn_fwd_bias(a, b, c, o, t, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
+        def step(a, b, c, o, dev_extra):
+            lf.lf_attn_fwd_bias(a, b, c, o, dev_extra[0], wl.w, wl.dilation, wl.global_idx,
+                                wl.scale, stream)
+        dev_extra = [rbd]
+        metric = ("banded+global attention forward with relative position bias, useful "
+                  "TFLOP/s (4*D per attended pair; 1 B300)")
+        data = "synthetic (seeded N(0,1), bf16-rounded; bias N(0,1) fp32 from seed+2000)"
+        cfg_extra = {"rel_bias": "[H, 2w+1] fp32"}
+        kernel = "attn_main (bias build)"
+    else:
+        if variant == "blocks-random":
+            tab = W.random_blocks(wl.L, wl.dilation, 3, wl.seed + 3000)
+            cfg_extra = {"extra_blocks": "3 random key blocks of 128 per 128-query tile "
+                                         "(seed+3000)"}
+        else:
+            tab = W.strided_blocks(wl.L, wl.dilation, 8)
+            cfg_extra = {"extra_blocks": "key blocks 0, 8, 16, ... of 128 per 128-query tile"}
+        pairs += extra_block_pairs(wl, tab)
+        # the table is a host argument of the call: it is read on the host every step
+
+        def step(a, b, c, o, dev_extra):
+            lf.lf_attn_fwd_blocks(a, b, c, o, wl.w, wl.dilation, wl.global_idx, tab, wl.scale,
+                                  stream)
+        dev_extra = []
+        metric = ("banded+global attention forward with extra key blocks per tile (BigBird "
+                  "random / strided), useful TFLOP/s (4*D per attended pair; 1 B300)")
+        data = "synthetic (seeded N(0,1), bf16-rounded; block table seeded)"
+        kernel = "attn_main (extra-block build)"
+    flops = 4 * wl.D * pairs
 
     for _ in range(args.warmup):
         flush.zero_()
-        step(qd, kd, vd, rbd, out)
+        step(qd, kd, vd, out, dev_extra)
     torch.cuda.synchronize(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
@@ -743,7 +805,7 @@ def run_bias(args, wl):
     for s_ in range(args.steps):
         flush.zero_()
         evs[s_][0].record(stream)
-        step(qd, kd, vd, rbd, out)
+        step(qd, kd, vd, out, dev_extra)
         evs[s_][1].record(stream)
     torch.cuda.synchronize(dev)
     launches = lf.lf_launch_count() - launches0
@@ -757,18 +819,18 @@ def run_bias(args, wl):
         raise SystemExit("device status error in timed region: " + lf.lf_last_error())
     value = flops * args.steps / (total_ms * 1e-3) / 1e12
 
-    # ---- end to end: q, k, v and the table from pinned host memory, out back
+    # ---- end to end: q, k, v (and a bias table) from pinned host memory, out back
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    host_in = [t.pin_memory() for t in (q, k, v, rb)]
+    host_in = [t.pin_memory() for t in (q, k, v, *extra_host)]
     host_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
-    dev_in = [torch.empty_like(t) for t in (qd, kd, vd, rbd)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
     dev_out = torch.empty_like(out)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         for dd, hh in zip(dev_in, host_in):
             dd.copy_(hh, non_blocking=True)
-        step(*dev_in, dev_out)
+        step(dev_in[0], dev_in[1], dev_in[2], dev_out, dev_in[3:])
         host_out.copy_(dev_out, non_blocking=True)
     torch.cuda.synchronize(dev)
     e2e_s = time.perf_counter() - t0
@@ -779,40 +841,40 @@ def run_bias(args, wl):
     main_s = main_ms / max(main_n, 1) * 1e-3
     ach = flops / main_s / 1e12
     line = {
-        "metric": "banded+global attention forward with relative position bias, useful "
-                  "TFLOP/s (4*D per attended pair; 1 B300)",
+        "metric": metric,
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1), bf16-rounded; bias N(0,1) fp32 from seed+2000)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": data,
         "config": dict(wl.describe(), l2="flushed between timed steps (256 MiB memset)",
-                       pairs=pairs * wl.B, rel_bias="[H, 2w+1] fp32"),
+                       pairs=pairs, **cfg_extra),
         "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
-                     "kernel": "attn_main (bias build)", "kernel_ms": main_s * 1e3,
+                     "kernel": kernel, "kernel_ms": main_s * 1e3,
                      "peak_source": "measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback"},
         "gpu_launches": launches,
         "e2e": {"value": flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "api": "lf_attn_fwd_bias with q, k, v and the table copied from pinned host "
-                       "memory and the output copied back"},
+                "api": f"the {variant} forward with its inputs copied from pinned host memory "
+                       "and the output copied back"},
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
         import oracle as O
         rows = list(range(0, wl.L, max(1, wl.L // 256)))
         qf, kf, vf = (t[:1].double().numpy() for t in (q, k, v))
+        kw = {"rel_bias": rb.double().numpy()} if variant == "bias" else \
+             {"xblocks": np.asarray(tab)}
         t0 = time.perf_counter()
-        O.attention(qf, kf, vf, wl.w, wl.dilation, wl.global_idx, wl.scale, rows=rows,
-                    rel_bias=rb.double().numpy())
+        O.attention(qf, kf, vf, wl.w, wl.dilation, wl.global_idx, wl.scale, rows=rows, **kw)
         secs = time.perf_counter() - t0
-        sample_pairs = pairs * len(rows) / wl.L
+        sample_pairs = pairs / wl.B * len(rows) / wl.L
         line["cpu_baseline"] = {
             "value": 4 * wl.D * sample_pairs / secs / 1e12, "unit": "TFLOP/s",
             "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"fp64 dense-masked oracle with the bias, {len(rows)} evenly spaced rows of "
-                      f"every head of one batch element of the {wl.name} workload"}
+            "sample": f"fp64 dense-masked oracle of the {variant} forward, {len(rows)} evenly "
+                      f"spaced rows of every head of one batch element of the {wl.name} "
+                      "workload"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -834,6 +896,9 @@ def main():
                          "attention alone")
     ap.add_argument("--rel-bias", action="store_true",
                     help="time the relative-position-bias forward (lf_attn_fwd_bias) on --config")
+    ap.add_argument("--blocks", default=None, choices=["random", "strided"],
+                    help="time the forward with extra key blocks per tile (lf_attn_fwd_blocks): "
+                         "3 random blocks, or blocks 0, 8, 16, ...")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -843,12 +908,13 @@ def main():
                               "reference arm"}))
             return 0
         return run_backward(args, W.CONFIGS[args.config])
-    if args.rel_bias:
+    if args.rel_bias or args.blocks:
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the bias line has no "
+            print(json.dumps({"impl": "reference", "unavailable": "the variant lines have no "
                               "reference arm"}))
             return 0
-        return run_bias(args, W.CONFIGS[args.config])
+        variant = "bias" if args.rel_bias else "blocks-" + args.blocks
+        return run_variant(args, W.CONFIGS[args.config], variant)
     if args.layer is not None:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the layer line has no "

@@ -113,6 +113,32 @@ LF_API lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v, v
                                   int n_global, float scale, lf_stream_t stream);
 
 /*
+ * lf_attn_fwd_blocks — lf_attn_fwd with extra key blocks per query tile:
+ * BigBird's random blocks added to window + global attention, or a fixed
+ * strided choice of blocks (the commentary on "Efficient Transformers: A
+ * Survey", §3.1 fixed patterns and §3.2 combined patterns; neither gives a
+ * block size or an indexing).  The form implemented, per head h with
+ * dilation d: a query i with r = i mod d, t = i div d lies in tile
+ * qt = t div 128 of residue class r; nqt = ceil(ceil(L/d) / 128) tiles per
+ * class.  Row r*nqt + qt of xblocks[h] lists up to R key blocks kb (-1 for
+ * none; duplicates allowed); block kb holds the keys r + d*t' with
+ * 128*kb <= t' < 128*kb + 128 (clipped to [0, L)).  They join K(i) of every
+ * non-global row of the tile, each key counted once (keys of the row's
+ * window and global keys are not added twice).  Global rows still see all
+ * keys.
+ *   xblocks  host, int32 [H, T, R] row-major, read during the call only;
+ *            T >= d*nqt for every head; entries in [-1, nqt).
+ * Other arguments and errors as lf_attn_fwd; LF_ERR_INVALID_ARG for a table
+ * of the wrong shape or an entry out of range.  The table is part of the
+ * cached plan: a new table builds (and keeps) a new plan.
+ */
+LF_API lf_status lf_attn_fwd_blocks(const void* q, const void* k, const void* v, void* out,
+                                    int B, int H, int L, int D, int w,
+                                    const int32_t* dilation, const int32_t* global_idx,
+                                    int n_global, const int32_t* xblocks, int T, int R,
+                                    float scale, lf_stream_t stream);
+
+/*
  * lf_attn_fwd_lse — lf_attn_fwd that also writes each row's log-sum-exp,
  *   lse[b,h,i] = ln( sum_{j in K(i)} exp(scale * q_i . k_j) )   (fp32),
  * the normaliser a backward pass needs (p_ij = exp(scale q_i.k_j - lse_i)).

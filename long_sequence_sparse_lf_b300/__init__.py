@@ -6,7 +6,7 @@ its ctypes binding, the build script and the seeded workload generators.
 """
 from ._binding import (  # noqa: F401
     LfError, attention, lf_attn_bwd, lf_attn_fwd, lf_attn_fwd_f32, lf_attn_fwd_host,
-    lf_attn_fwd_bias, lf_attn_fwd_lse, lf_attn_fwd_noalloc,
+    lf_attn_fwd_bias, lf_attn_fwd_blocks, lf_attn_fwd_lse, lf_attn_fwd_noalloc,
     lf_attn_get_status, lf_attn_pairs, lf_last_error, lf_launch_count, lf_layer_fwd,
     lf_selftest_wait_timeout,
     lf_plan_cache_clear, lf_profile_enable, lf_profile_only, lf_profile_query, lf_profile_reset,

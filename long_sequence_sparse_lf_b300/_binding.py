@@ -87,6 +87,9 @@ def load_library() -> ctypes.CDLL:
     lib.lf_attn_fwd_bias.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ip, ip, i32,
                                      f32, vp]
     lib.lf_attn_fwd_bias.restype = i32
+    lib.lf_attn_fwd_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, ip, ip, i32, vp,
+                                       i32, i32, f32, vp]
+    lib.lf_attn_fwd_blocks.restype = i32
     _lib = lib
     return lib
 
@@ -367,6 +370,25 @@ def lf_attn_fwd_bias(q, k, v, out, rel_bias, w: int, dilation: Sequence[int],
                                 rel_bias.data_ptr(), B, H, L, D, int(w), _i32_array(dilation),
                                 _i32_array(global_idx), len(global_idx), float(scale),
                                 _stream_handle(stream)))
+
+
+def lf_attn_fwd_blocks(q, k, v, out, w: int, dilation: Sequence[int],
+                       global_idx: Sequence[int], xblocks, scale: float, stream=None):
+    """bf16 forward with extra key blocks per 128-query tile (BigBird random
+    or strided blocks): xblocks is an integer table [H, T, R] (host; -1 for
+    none) whose row r*nqt + qt lists the key blocks of tile qt of residue
+    class r, nqt = ceil(ceil(L/d) / 128)."""
+    _check_qkv(q, k, v, out, torch.bfloat16, "cuda")
+    B, H, L, D = q.shape
+    tab = torch.as_tensor(xblocks).to(dtype=torch.int32, device="cpu").contiguous()
+    if tab.dim() != 3 or tab.shape[0] != H:
+        raise ValueError(f"xblocks must be [H, T, R] with H={H}, got {tuple(tab.shape)}")
+    lib = load_library()
+    _check(lib.lf_attn_fwd_blocks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  B, H, L, D, int(w), _i32_array(dilation),
+                                  _i32_array(global_idx), len(global_idx), tab.data_ptr(),
+                                  int(tab.shape[1]), int(tab.shape[2]), float(scale),
+                                  _stream_handle(stream)))
 
 
 def lf_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, w: int, dilation: Sequence[int],

@@ -35,6 +35,7 @@ namespace {
 
 using lf::MainParams;
 using lf::WorkItem;
+using lf::XBlock;
 
 __device__ unsigned g_status_word;
 
@@ -154,7 +155,9 @@ lf_status get_dev(DevState** out, int* dev_out) {
     for (const void* fn : {reinterpret_cast<const void*>(lf::lf_attn_main_kernel<64>),
                            reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128>),
                            reinterpret_cast<const void*>(lf::lf_attn_main_kernel<64, true>),
-                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128, true>)}) {
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128, true>),
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<64, false, true>),
+                           reinterpret_cast<const void*>(lf::lf_attn_main_kernel<128, false, true>)}) {
       cudaFuncAttributes fa;
       LF_CUDA(cudaFuncGetAttributes(&fa, fn));
       if (fa.numRegs != (int)lf::kRegsLaunch)
@@ -172,6 +175,12 @@ lf_status get_dev(DevState** out, int* dev_out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)lf::KCfg<64>::SMEM_BYTES));
     LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<128, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)lf::KCfg<128>::SMEM_BYTES));
+    LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<64, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)lf::KCfg<64>::SMEM_BYTES));
+    LF_CUDA(cudaFuncSetAttribute(lf::lf_attn_main_kernel<128, false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)lf::KCfg<128>::SMEM_BYTES));
     ds.ready = true;
@@ -214,6 +223,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Pattern {
   int H = 0, L = 0, w = 0, n_g = 0;
   std::vector<int32_t> dil, G;
+  // extra key blocks per query tile: {T, R, table [H][T][R]}, or empty
+  std::vector<int32_t> xkey;
   int32_t* d_G = nullptr;
   uint8_t* d_isg = nullptr;
   int32_t* d_gcnt = nullptr;
@@ -240,21 +251,39 @@ struct Plan {
   std::vector<int> head_slot;
   int NGB = 16, NGQ = 0, n_gblk = 0, n_chunks = 0;
   std::vector<WorkItem> items;     // grouped by CTA (see cta_begin)
+  std::vector<int4> xitem;         // per item {xo, nx0, nx1, 0} (extra blocks; else empty)
+  std::vector<XBlock> xlist;       // the extra blocks
   std::vector<int> cta_begin;      // [grid + 1] item ranges per CTA
   int grid = 0;                    // CTAs of the attention kernel
-  WorkItem* d_items = nullptr;     // device copy of items, then cta_begin
-  int* d_cta = nullptr;
+  WorkItem* d_items = nullptr;     // device copy of items, then cta_begin (one allocation,
+  int* d_cta = nullptr;            // freed through d_items), then xitem and xlist
+  int4* d_xitem = nullptr;
+  XBlock* d_xlist = nullptr;
 };
 
-using PatKey = std::tuple<int, int, int, int, std::vector<int32_t>, std::vector<int32_t>>;
+using PatKey = std::tuple<int, int, int, int, std::vector<int32_t>, std::vector<int32_t>,
+                          std::vector<int32_t>>;
 using PlanKey = std::tuple<int, int, int, PatKey>;   // dev, B, D, pattern
 std::map<PatKey, std::shared_ptr<Pattern>> g_patterns;
 std::map<PlanKey, std::unique_ptr<Plan>> g_plans;
 
+// The extra-block key of a pattern: {T, R, table}, or empty for none.
+std::vector<int32_t> xblock_key(int H, const int32_t* xb, int T, int R) {
+  std::vector<int32_t> k;
+  if (xb == nullptr || T <= 0 || R <= 0) return k;
+  k.reserve(2 + (size_t)H * T * R);
+  k.push_back(T);
+  k.push_back(R);
+  k.insert(k.end(), xb, xb + (size_t)H * T * R);
+  return k;
+}
+
 lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const int32_t* gidx,
-                      int n_g, std::shared_ptr<Pattern>* out) {
+                      int n_g, std::shared_ptr<Pattern>* out, const int32_t* xb = nullptr,
+                      int T = 0, int R = 0) {
   PatKey key{dev, H, L, w, std::vector<int32_t>(dil, dil + H),
-             std::vector<int32_t>(gidx ? gidx : dil, gidx ? gidx + n_g : dil)};
+             std::vector<int32_t>(gidx ? gidx : dil, gidx ? gidx + n_g : dil),
+             xblock_key(H, xb, T, R)};
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_patterns.find(key);
   if (it != g_patterns.end()) {
@@ -268,6 +297,7 @@ lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const in
   pat->n_g = n_g;
   pat->dil.assign(dil, dil + H);
   if (n_g) pat->G.assign(gidx, gidx + n_g);
+  pat->xkey = std::get<6>(key);
   fill_global_tables(*pat);
   LF_CUDA(cudaMalloc(&pat->d_isg, L));
   LF_CUDA(cudaMemcpy(pat->d_isg, pat->isg.data(), L, cudaMemcpyHostToDevice));
@@ -294,16 +324,47 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // each to the least-loaded CTA (a cost per item = the blocks of its busier
 // slot, gathered blocks weighted by their width, plus one for the item's
 // own loads and epilogue), and stored grouped by CTA.
-int item_cost(const WorkItem& wi, int NGB) {
+int item_cost(const WorkItem& wi, int NGB, const int4& xi) {
   int c[2];
   for (int X = 0; X < 2; ++X) {
     const int n = lf::blk_count(wi, X);
     if (wi.kind == 0 && n > 0)
-      c[X] = 8 * (n - wi.ngb) + (wi.ngb * NGB + 15) / 16;   // eighths of a block
+      c[X] = 8 * (n - wi.ngb) + (wi.ngb * NGB + 15) / 16 + 8 * (X ? xi.z : xi.y);   // eighths
     else
       c[X] = 8 * n;
   }
   return std::max(c[0], c[1]) + 8;
+}
+
+// The extra key blocks of one query tile (rows ta..tb of residue class r of
+// head h, class length Lr): the table's row for the tile, without -1,
+// duplicates and blocks that every row already holds in its window;
+// appended to xlist with the bits of their global columns.  Returns how many.
+int tile_extra_blocks(const Pattern& pt, int h, int d, int r, int Lr, int ta, int tb,
+                      std::vector<XBlock>& xlist) {
+  if (pt.xkey.empty()) return 0;
+  const int T = pt.xkey[0], R = pt.xkey[1];
+  const int nqt = ceil_div(ceil_div(pt.L, d), lf::kBM);
+  const int rho = r * nqt + ta / lf::kBM;
+  const int32_t* row = pt.xkey.data() + 2 + ((size_t)h * T + rho) * R;
+  std::vector<int> kbs;
+  for (int e = 0; e < R; ++e)
+    if (row[e] >= 0) kbs.push_back(row[e]);
+  std::sort(kbs.begin(), kbs.end());
+  kbs.erase(std::unique(kbs.begin(), kbs.end()), kbs.end());
+  int n = 0;
+  for (int kb : kbs) {
+    const int k0 = kb * lf::kBN, k1 = std::min(k0 + lf::kBN, Lr) - 1;
+    if (k0 > k1) continue;
+    if (k0 >= tb - pt.w && k1 <= ta + pt.w) continue;   // inside every row's window
+    XBlock xb{};
+    xb.kpos0 = k0;
+    for (int c = 0; c <= k1 - k0; ++c)
+      if (pt.isg[r + d * (k0 + c)]) xb.gm[c >> 5] |= 1u << (c & 31);
+    xlist.push_back(xb);
+    ++n;
+  }
+  return n;
 }
 
 void build_items(Plan& pl, int num_sms) {
@@ -339,6 +400,8 @@ void build_items(Plan& pl, int num_sms) {
     pl.n_chunks = 0;
   }
   std::vector<WorkItem> order;
+  std::vector<int4> order_x;   // extra blocks of each item, parallel to order
+  pl.xlist.clear();
   for (int b = 0; b < pl.B; ++b) {
     for (int h = 0; h < H; ++h) {
       const int bh = b * H + h;
@@ -373,16 +436,21 @@ void build_items(Plan& pl, int num_sms) {
           wi.nkb = ceil_div(phi - plo + 1, lf::kBN);
           wi.ngb = pl.n_gblk;
           wi.slot = pl.head_slot[h];
+          int4 xi = make_int4((int)pl.xlist.size(), 0, 0, 0);
           for (int X = 0; X < 2; ++X) {
             if (present[X]) {
               wi.jlo[X] = (lo[X] - plo) / lf::kBN;
               wi.jhi[X] = (hi[X] - plo) / lf::kBN;
+              const int ta = t0 + X * lf::kBM, tb = std::min(ta + lf::kBM - 1, Lr - 1);
+              const int nx = tile_extra_blocks(pt, h, d, r, Lr, ta, tb, pl.xlist);
+              if (X) xi.z = nx; else xi.y = nx;
             } else {
               wi.jlo[X] = 1;
               wi.jhi[X] = 0;
             }
           }
           order.push_back(wi);
+          order_x.push_back(xi);
         }
       }
       for (int gt = 0; gt < pl.NGQ / lf::kBM; ++gt)
@@ -399,6 +467,7 @@ void build_items(Plan& pl, int num_sms) {
           wi.jlo[0] = wi.jlo[1] = 0;
           wi.jhi[0] = wi.jhi[1] = -1;
           order.push_back(wi);
+          order_x.push_back(make_int4(0, 0, 0, 0));
         }
     }
   }
@@ -409,7 +478,7 @@ void build_items(Plan& pl, int num_sms) {
   std::vector<int> cost(n);
   for (int x = 0; x < n; ++x) {
     idx[x] = x;
-    cost[x] = item_cost(order[x], pl.NGB);
+    cost[x] = item_cost(order[x], pl.NGB, order_x[x]);
   }
   std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return cost[a] > cost[b]; });
   std::vector<std::vector<int>> per_cta(pl.grid);
@@ -425,11 +494,16 @@ void build_items(Plan& pl, int num_sms) {
   }
   pl.items.clear();
   pl.items.reserve(n);
+  pl.xitem.clear();
   pl.cta_begin.assign(pl.grid + 1, 0);
+  const bool extra = !pt.xkey.empty();
   for (int c = 0; c < pl.grid; ++c) {
     // keep each CTA's items in list order (head by head, along the keys)
     std::sort(per_cta[c].begin(), per_cta[c].end());
-    for (int x : per_cta[c]) pl.items.push_back(order[x]);
+    for (int x : per_cta[c]) {
+      pl.items.push_back(order[x]);
+      if (extra) pl.xitem.push_back(order_x[x]);
+    }
     pl.cta_begin[c + 1] = (int)pl.items.size();
   }
 }
@@ -437,17 +511,22 @@ void build_items(Plan& pl, int num_sms) {
 // Every block of an item must have a user: the kernel releases a K/V stage
 // after its users' products (checked once per plan).
 bool items_consistent(const Plan& pl) {
-  for (const WorkItem& wi : pl.items) {
-    for (int j = 0; j < wi.nkb + wi.ngb; ++j)
-      if (!lf::blk_uses(wi, 0, j) && !lf::blk_uses(wi, 1, j)) return false;
+  for (size_t x = 0; x < pl.items.size(); ++x) {
+    const WorkItem& wi = pl.items[x];
+    const int4 xi = pl.xitem.empty() ? make_int4(0, 0, 0, 0) : pl.xitem[x];
+    const lf::SlotBlocks s0(wi, 0, xi.y, xi.z), s1(wi, 1, xi.y, xi.z);
+    for (int j = 0; j < wi.nkb + wi.ngb + xi.y + xi.z; ++j)
+      if (!s0.uses(j) && !s1.uses(j)) return false;
     if (wi.nkb < 1) return false;
+    if (xi.y + xi.z > 0 && (wi.kind != 0 || xi.x < 0 || (size_t)xi.x + xi.y + xi.z > pl.xlist.size()))
+      return false;
   }
   return true;
 }
 
 lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pattern>& pat,
                    Plan** out) {
-  PatKey pk{dev, pat->H, pat->L, pat->w, pat->dil, pat->G};
+  PatKey pk{dev, pat->H, pat->L, pat->w, pat->dil, pat->G, pat->xkey};
   PlanKey key{dev, B, D, pk};
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_plans.find(key);
@@ -475,15 +554,28 @@ lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pat
   if (!items_consistent(*pl)) return fail(LF_ERR_INVALID_ARG, "internal: inconsistent work list");
   {
     const size_t ib = align_up(sizeof(WorkItem) * std::max<size_t>(pl->items.size(), 1), 256);
-    const size_t cb = sizeof(int) * pl->cta_begin.size();
+    const size_t cb = align_up(sizeof(int) * pl->cta_begin.size(), 256);
+    const size_t xib = align_up(sizeof(int4) * pl->xitem.size(), 256);
+    const size_t xlb = align_up(sizeof(XBlock) * pl->xlist.size(), 256);
     uint8_t* dev_mem = nullptr;
-    LF_CUDA(cudaMalloc(reinterpret_cast<void**>(&dev_mem), ib + cb));
+    LF_CUDA(cudaMalloc(reinterpret_cast<void**>(&dev_mem), ib + cb + xib + xlb));
     pl->d_items = reinterpret_cast<WorkItem*>(dev_mem);
     pl->d_cta = reinterpret_cast<int*>(dev_mem + ib);
     if (!pl->items.empty())
       LF_CUDA(cudaMemcpy(pl->d_items, pl->items.data(), sizeof(WorkItem) * pl->items.size(),
                          cudaMemcpyHostToDevice));
-    LF_CUDA(cudaMemcpy(pl->d_cta, pl->cta_begin.data(), cb, cudaMemcpyHostToDevice));
+    LF_CUDA(cudaMemcpy(pl->d_cta, pl->cta_begin.data(), sizeof(int) * pl->cta_begin.size(),
+                       cudaMemcpyHostToDevice));
+    if (!pl->xitem.empty()) {
+      pl->d_xitem = reinterpret_cast<int4*>(dev_mem + ib + cb);
+      LF_CUDA(cudaMemcpy(pl->d_xitem, pl->xitem.data(), sizeof(int4) * pl->xitem.size(),
+                         cudaMemcpyHostToDevice));
+    }
+    if (!pl->xlist.empty()) {
+      pl->d_xlist = reinterpret_cast<XBlock*>(dev_mem + ib + cb + xib);
+      LF_CUDA(cudaMemcpy(pl->d_xlist, pl->xlist.data(), sizeof(XBlock) * pl->xlist.size(),
+                         cudaMemcpyHostToDevice));
+    }
   }
   *out = pl.get();
   g_plans[key] = std::move(pl);
@@ -616,6 +708,8 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
   P.sl2 = scale * 1.4426950408889634f;
   P.lse = lse;
   P.rel_bias = rel_bias;
+  P.xitem = pl->d_xitem;
+  P.xlist = pl->d_xlist;
   P.status = ds->status;
   P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
@@ -625,7 +719,8 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
 lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool f32, int B, int H,
                    int L, int D, int w, const int32_t* dilation, const int32_t* gidx, int n_g,
                    float scale, cudaStream_t stream, float* lse = nullptr,
-                   const float* rel_bias = nullptr) {
+                   const float* rel_bias = nullptr, const int32_t* xblocks = nullptr, int xT = 0,
+                   int xR = 0) {
   t_last_error.clear();
   if (B < 1) return fail(LF_ERR_INVALID_ARG, "B=%d must be >= 1", B);
   lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
@@ -646,9 +741,12 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   int dev = 0;
   if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
   std::shared_ptr<Pattern> pat;
-  if ((s = get_pattern(dev, H, L, w, dilation, gidx, n_g, &pat)) != LF_OK) return s;
+  if ((s = get_pattern(dev, H, L, w, dilation, gidx, n_g, &pat, xblocks, xT, xR)) != LF_OK)
+    return s;
   Plan* pl = nullptr;
   if ((s = get_plan(dev, ds->num_sms, B, D, pat, &pl)) != LF_OK) return s;
+  const bool xb = !pat->xkey.empty();
+  if (xb && rel_bias) return fail(LF_ERR_UNSUPPORTED, "extra blocks with a bias table");
 
   const int BH = B * H;
   const size_t elems = (size_t)BH * L * D;
@@ -723,7 +821,11 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   if (prm.n_items > 0) {
     const int grid = pl->grid;
     traced("attn_main", stream, [&] {
-      if (D == 64 && rel_bias)
+      if (D == 64 && xb)
+        lf::lf_attn_main_kernel<64, false, true><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
+      else if (D == 128 && xb)
+        lf::lf_attn_main_kernel<128, false, true><<<grid, lf::KCfg<128>::THREADS, lf::KCfg<128>::SMEM_BYTES, stream>>>(prm);
+      else if (D == 64 && rel_bias)
         lf::lf_attn_main_kernel<64, true><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
       else if (D == 64)
         lf::lf_attn_main_kernel<64><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
@@ -1213,7 +1315,7 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   if ((s = get_pattern(dev, H, L, w, dilation, gidx, n_g, &pat)) != LF_OK) return s;
   BwdPlan* bp = nullptr;
   {
-    PatKey pk{dev, H, L, w, pat->dil, pat->G};
+    PatKey pk{dev, H, L, w, pat->dil, pat->G, pat->xkey};
     PlanKey key{dev, B, D, pk};
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_bwd_plans.find(key);
@@ -1365,6 +1467,35 @@ lf_status bias_fwd_impl(const void* q, const void* k, const void* v, void* out,
                   tbl);
 }
 
+// lf_attn_fwd_blocks: the table's shape and entries are checked here; the
+// planner turns each tile's row into extra blocks of its band items.
+lf_status blocks_fwd_impl(const void* q, const void* k, const void* v, void* out, int B, int H,
+                          int L, int D, int w, const int32_t* dilation, const int32_t* gidx,
+                          int n_g, const int32_t* xblocks, int T, int R, float scale,
+                          cudaStream_t stream) {
+  t_last_error.clear();
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  if (xblocks == nullptr || T < 1 || R < 1)
+    return fail(LF_ERR_INVALID_ARG, "xblocks must be a host table [H, T, R] with T, R >= 1");
+  if ((long long)H * T * R > (1LL << 28))
+    return fail(LF_ERR_UNSUPPORTED, "extra-block table too large (H*T*R=%lld)",
+                (long long)H * T * R);
+  for (int h = 0; h < H; ++h) {
+    const int d = dilation[h];
+    const int nqt = ceil_div(ceil_div(L, d), lf::kBM);
+    if ((long long)d * nqt > T)
+      return fail(LF_ERR_INVALID_ARG, "T=%d < %d tiles of head %d (dilation %d)", T, d * nqt, h, d);
+    const int32_t* tab = xblocks + (size_t)h * T * R;
+    for (size_t e = 0; e < (size_t)T * R; ++e)
+      if (tab[e] < -1 || tab[e] >= nqt)
+        return fail(LF_ERR_INVALID_ARG, "xblocks[%d][%zu]=%d not in [-1, %d)", h, e / R, tab[e],
+                    nqt);
+  }
+  return fwd_impl(q, k, v, out, false, B, H, L, D, w, dilation, gidx, n_g, scale, stream, nullptr,
+                  nullptr, xblocks, T, R);
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -1391,6 +1522,20 @@ lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v, void* ou
   try {
     return bias_fwd_impl(q, k, v, out, rel_bias, B, H, L, D, w, dilation, global_idx, n_global,
                          scale, static_cast<cudaStream_t>(stream));
+  } catch (const std::exception& e) {
+    return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
+  } catch (...) {
+    return fail(LF_ERR_NOMEM, "host exception");
+  }
+}
+
+lf_status lf_attn_fwd_blocks(const void* q, const void* k, const void* v, void* out, int B,
+                             int H, int L, int D, int w, const int32_t* dilation,
+                             const int32_t* global_idx, int n_global, const int32_t* xblocks,
+                             int T, int R, float scale, lf_stream_t stream) {
+  try {
+    return blocks_fwd_impl(q, k, v, out, B, H, L, D, w, dilation, global_idx, n_global, xblocks,
+                           T, R, scale, static_cast<cudaStream_t>(stream));
   } catch (const std::exception& e) {
     return fail(LF_ERR_NOMEM, "host exception: %s", e.what());
   } catch (...) {

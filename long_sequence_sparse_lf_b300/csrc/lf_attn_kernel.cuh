@@ -202,8 +202,10 @@ __device__ __noinline__ bool issue_pv_block(uint32_t b0, int X, uint32_t sV, uin
 
 // BIAS: the relative-position-bias variant (p.rel_bias): each window key
 // j = i + d*t of a non-global row gains rel_bias[h][t + w] on its scaled
-// score.  A separate instantiation, so the kernel without it is unchanged.
-template <int D, bool BIAS = false>
+// score.  XB: band items carry extra key blocks per tile slot (random /
+// strided block patterns, p.xitem / p.xlist).  Separate instantiations, so
+// the kernel without them is unchanged.
+template <int D, bool BIAS = false, bool XB = false>
 __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_constant__ MainParams p) {
   using C = KCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -280,6 +282,12 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       bool ok = true;
       for (int it = it_begin; it < it_end && ok; ++it) {
         const WorkItem wi = p.items[it];
+        int xo = 0, nxt = 0;
+        if (XB && wi.kind == 0) {
+          const int4 xi = p.xitem[it];
+          xo = xi.x;
+          nxt = xi.y + xi.z;
+        }
 #pragma unroll
         for (int X = 0; X < 2; ++X) {
           if (!ok || blk_count(wi, X) == 0) continue;
@@ -301,14 +309,17 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           ++qn[X];
         }
         if (!ok) break;
-        const int nbt = wi.nkb + wi.ngb;
+        const int nbt = wi.nkb + wi.ngb + nxt;
         for (int j = 0; j < nbt; ++j) {
           const int st = nb % C::NST;
           const uint32_t su = nb / C::NST;
           if (su > 0 && !bwait(BAR(C::B_KE + st), (su - 1) & 1, W)) { ok = false; break; }
           const uint32_t kd = sK + st * C::KVB, vd = sV + st * C::KVB;
-          if (j < wi.nkb) {
-            const int kpos = wi.kb0 + kBN * j;
+          const bool gblk = XB ? (j >= wi.nkb && j < wi.nkb + wi.ngb) : j >= wi.nkb;
+          if (!gblk) {
+            // band block, or an extra block (band-type, from the list)
+            const int kpos = (XB && j >= wi.nkb) ? p.xlist[xo + j - wi.nkb - wi.ngb].kpos0
+                                                 : wi.kb0 + kBN * j;
             mbar_arrive_expect_tx(BAR(C::B_KF + st), 2u * C::KVB);
 #pragma unroll
             for (int hh = 0; hh < C::NH; ++hh) {
@@ -382,8 +393,14 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
       };
       for (int it = it_begin; it < it_end && ok; ++it) {
         const WorkItem wi = p.items[it];
-        const SlotBlocks sb(wi, X);
-        const int nbt = wi.nkb + wi.ngb;
+        int nx0 = 0, nx1 = 0;
+        if (XB && wi.kind == 0) {
+          const int4 xi = p.xitem[it];
+          nx0 = xi.y;
+          nx1 = xi.z;
+        }
+        const SlotBlocks sb(wi, X, nx0, nx1);
+        const int nbt = wi.nkb + wi.ngb + nx0 + nx1;
         const int cnt = sb.count();
         const bool present = sb.jlo <= sb.jhi;
         int seen = 0;
@@ -392,8 +409,10 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           // block nb reuses the stage of block nb - NST, which the producer
           // refills only after that block's PVs
           if (pend && p_nb + C::NST <= nb && !issue_pv()) { ok = false; break; }
-          const bool use = wi.kind == 0 ? present && (j >= wi.nkb || (j >= sb.jlo && j <= sb.jhi))
-                                        : (j < wi.nkb && (j & 1) == X);
+          const bool use =
+              XB ? sb.uses(j)
+                 : (wi.kind == 0 ? present && (j >= wi.nkb || (j >= sb.jlo && j <= sb.jhi))
+                                 : (j < wi.nkb && (j & 1) == X));
           if (!use) {
             if (!bwait(BAR(C::B_KF + st), (nb / C::NST) & 1, W)) { ok = false; break; }
             mbar_arrive(BAR(C::B_KE + st));
@@ -408,7 +427,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          const bool gblk = j >= wi.nkb;
+          const bool gblk = XB ? (j >= wi.nkb && j < wi.nkb + wi.ngb) : j >= wi.nkb;
           const uint32_t qa = sQ + bi * C::QB, ka = sK + st * C::KVB;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
@@ -470,7 +489,13 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
     for (int it = it_begin; it < it_end && ok; ++it) {
       const WorkItem wi = p.items[it];
       const bool band = wi.kind == 0;
-      const SlotBlocks sb(wi, X);
+      int nx0 = 0, nx1 = 0;
+      if (XB && band) {
+        const int4 xi = p.xitem[it];
+        nx0 = xi.y;
+        nx1 = xi.z;
+      }
+      const SlotBlocks sb(wi, X, nx0, nx1);
       if (sb.count() == 0) {
         if (!band) {
           // the slot had no block of this chunk: an empty partial
@@ -553,6 +578,19 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             v1 = range_bits(clo, chi1, 32);
             v2 = range_bits(clo, chi1, 64);
             v3 = range_bits(clo, chi1, 96);
+          } else if (XB && j >= wi.nkb + wi.ngb) {
+            // extra block: its keys inside [0, Lr), minus the row's window
+            // (the band blocks hold those) and the global positions (the
+            // gathered blocks hold those)
+            const XBlock& xb = p.xlist[p.xitem[it].x + j - wi.nkb - wi.ngb];
+            const uint4 gm = *reinterpret_cast<const uint4*>(xb.gm);
+            const int kpos0 = xb.kpos0;
+            const int nv = residue_len(p.L, d, wi.r) - kpos0;
+            const int clo = wlo - kpos0, chi1 = whi - kpos0 + 1;
+            v0 = range_bits(0, nv, 0) & ~range_bits(clo, chi1, 0) & ~gm.x;
+            v1 = range_bits(0, nv, 32) & ~range_bits(clo, chi1, 32) & ~gm.y;
+            v2 = range_bits(0, nv, 64) & ~range_bits(clo, chi1, 64) & ~gm.z;
+            v3 = range_bits(0, nv, 96) & ~range_bits(clo, chi1, 96) & ~gm.w;
           } else {
             // gathered globals G[gbase + c]: not the padding, and not a global
             // already in the row's window (columns [c_lo, c_hi) hold

@@ -63,18 +63,37 @@ struct WorkItem {
   int jhi[2];    // band: last band block used by each tile slot (inclusive)
 };
 
+// Extra key blocks (the random / strided block patterns, built by the
+// kernel instance with extra blocks): a band item may carry, after its band
+// and gathered blocks, nx[0] blocks of slot 0 and then nx[1] blocks of slot
+// 1, described by XBlock records xlist[xo ..] (xitem[item] = {xo, nx[0],
+// nx[1], 0}).  Block j = nkb + ngb + n holds keys kpos0 .. kpos0+127 of the
+// item's residue class (residue space); gm marks the columns that are global
+// positions (their keys come from the gathered blocks).
+struct __align__(16) XBlock {
+  uint32_t gm[4];
+  int kpos0;
+  int pad_[3];
+};
+
 // The blocks one tile slot uses in an item, with the slot fixed (its range
-// is taken out of the item once, so that walking it needs no indexing).
+// is taken out of the item once, so that walking it needs no indexing):
+// band blocks jlo..jhi, the gathered blocks, then the slot's extra blocks
+// xa .. xa+xn-1 (none unless given).
 struct SlotBlocks {
-  int kind, nkb, ngb, jlo, jhi, X;
+  int kind, nkb, ngb, jlo, jhi, X, xa, xn;
   __host__ __device__ __forceinline__ SlotBlocks(int kind_, int nkb_, int ngb_, int jlo_, int jhi_,
                                                  int x)
-      : kind(kind_), nkb(nkb_), ngb(ngb_), jlo(jlo_), jhi(jhi_), X(x) {}
+      : kind(kind_), nkb(nkb_), ngb(ngb_), jlo(jlo_), jhi(jhi_), X(x), xa(nkb_ + ngb_), xn(0) {}
   __host__ __device__ __forceinline__ SlotBlocks(const WorkItem& wi, int x)
       : kind(wi.kind), nkb(wi.nkb), ngb(wi.ngb), jlo(x ? wi.jlo[1] : wi.jlo[0]),
-        jhi(x ? wi.jhi[1] : wi.jhi[0]), X(x) {}
+        jhi(x ? wi.jhi[1] : wi.jhi[0]), X(x), xa(wi.nkb + wi.ngb), xn(0) {}
+  __host__ __device__ __forceinline__ SlotBlocks(const WorkItem& wi, int x, int nx0, int nx1)
+      : kind(wi.kind), nkb(wi.nkb), ngb(wi.ngb), jlo(x ? wi.jlo[1] : wi.jlo[0]),
+        jhi(x ? wi.jhi[1] : wi.jhi[0]), X(x), xa(wi.nkb + wi.ngb + (x ? nx0 : 0)),
+        xn(x ? nx1 : nx0) {}
   __host__ __device__ __forceinline__ int count() const {
-    if (kind == 0) return jlo <= jhi ? jhi - jlo + 1 + ngb : 0;
+    if (kind == 0) return jlo <= jhi ? jhi - jlo + 1 + ngb + xn : 0;
     return nkb > X ? (nkb - X + 1) / 2 : 0;
   }
   __host__ __device__ __forceinline__ int first() const {
@@ -84,10 +103,17 @@ struct SlotBlocks {
   __host__ __device__ __forceinline__ int next(int j) const {
     if (kind == 0) {
       if (j < jhi) return j + 1;
-      if (j < nkb) return ngb > 0 ? nkb : -1;
-      return j + 1 < nkb + ngb ? j + 1 : -1;
+      if (j < nkb) return ngb > 0 ? nkb : (xn > 0 ? xa : -1);
+      if (j < nkb + ngb) return j + 1 < nkb + ngb ? j + 1 : (xn > 0 ? xa : -1);
+      return j + 1 < xa + xn ? j + 1 : -1;
     }
     return j + 2 < nkb ? j + 2 : -1;
+  }
+  __host__ __device__ __forceinline__ bool uses(int j) const {
+    if (kind == 0)
+      return jlo <= jhi && ((j >= jlo && j <= jhi) || (j >= nkb && j < nkb + ngb) ||
+                            (j >= xa && j < xa + xn));
+    return j < nkb && (j & 1) == X;
   }
 };
 
@@ -146,6 +172,8 @@ struct MainParams {
   float* part_o;                   // [(bh*NGQ + g)*n_chunks + c][D] fp32
   float* part_ml;                  // [(bh*NGQ + g)*n_chunks + c][2] (m, l)
   float* lse;                      // [B*H, L]: ln sum_{K(i)} exp(scale q.k), or null
+  const int4* xitem;               // [n_items] {xo, nx0, nx1, 0} (extra-block kernel only)
+  const XBlock* xlist;             // extra blocks of all items
   const float* rel_bias;           // [H, 4, bias_row_len(w)]: rel_bias/scale, zero-padded,
                                    // copy c shifted by c (the BIAS kernel only)
   int H, L, w;

@@ -113,6 +113,51 @@ def random_globals(L: int, n: int, seed: int) -> tuple:
     return tuple(sorted(torch.randperm(L, generator=g)[:n].tolist()))
 
 
+# ------------------------------------------------- extra key-block tables
+# Tables [H, T, R] of extra key blocks per 128-query tile (BigBird random
+# blocks, or a fixed strided choice).  Head h with dilation d has
+# nqt = ceil(ceil(L / d) / 128) tiles per residue class and d classes; its
+# rows r*nqt + qt are used, the rest are -1.  Only indices are drawn here.
+
+TILE = 128
+
+
+def tiles_per_class(L: int, d: int) -> int:
+    return -(-(-(-L // d)) // TILE)
+
+
+def block_table_rows(L: int, dilation: Sequence[int]) -> int:
+    """T: the table rows that every head's tiles fit in."""
+    return max(int(d) * tiles_per_class(L, int(d)) for d in dilation)
+
+
+def random_blocks(L: int, dilation: Sequence[int], R: int, seed: int) -> torch.Tensor:
+    """R distinct key blocks per tile, uniform over the tile's class (fewer,
+    padded with -1, when the class has fewer blocks); int32 [H, T, R]."""
+    H, T = len(dilation), block_table_rows(L, dilation)
+    g = torch.Generator().manual_seed(seed)
+    tab = torch.full((H, T, R), -1, dtype=torch.int32)
+    for h, d in enumerate(dilation):
+        nqt = tiles_per_class(L, int(d))
+        for row in range(int(d) * nqt):
+            pick = torch.randperm(nqt, generator=g)[:R]
+            tab[h, row, :pick.numel()] = pick.to(torch.int32)
+    return tab
+
+
+def strided_blocks(L: int, dilation: Sequence[int], stride: int) -> torch.Tensor:
+    """Every tile lists the key blocks 0, stride, 2*stride, ... of its class;
+    int32 [H, T, R] with R the longest such list."""
+    H, T = len(dilation), block_table_rows(L, dilation)
+    lists = [list(range(0, tiles_per_class(L, int(d)), stride)) for d in dilation]
+    R = max(len(x) for x in lists)
+    tab = torch.full((H, T, R), -1, dtype=torch.int32)
+    for h, d in enumerate(dilation):
+        nqt = tiles_per_class(L, int(d))
+        tab[h, :int(d) * nqt, :len(lists[h])] = torch.tensor(lists[h], dtype=torch.int32)
+    return tab
+
+
 # ------------------------------------------------------------ layer inputs
 # Synthetic inputs of one Longformer layer (random-init weights of the
 # page's layer shape; no trained weights exist here).  Only random numbers:
