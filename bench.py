@@ -289,6 +289,13 @@ def run_ours(args, wl):
     # the forward with its arguments marshalled once (lf_attn_fwd through the C ABI)
     step = lf.prepare_fwd(qd, kd, vd, out, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
 
+    # the clock sampler starts (and is given time to take its first sample)
+    # before the warm-up, so that the warm-up steps come right before the
+    # timed ones: an idle gap there leaves the first timed steps slow
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -298,7 +305,6 @@ def run_ours(args, wl):
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    sampler = ClockSampler(local) if rank == 0 else None
     lf.lf_profile_reset()
     # events around attn_main only: every traced launch costs the stream an
     # event pair, and only attn_main's duration is used below
@@ -307,9 +313,6 @@ def run_ours(args, wl):
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     launches0 = lf.lf_launch_count()
     for s in range(args.steps):
         flush.zero_()
@@ -449,6 +452,12 @@ def run_layer(args):
         lf.lf_layer_fwd(xin, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, yout, lw.H, lw.w,
                         lw.dilation, lw.global_idx, lw.scale, lw.eps, stream)
 
+    # the clock sampler starts (and is given time to take its first sample)
+    # before the warm-up, so that the warm-up steps come right before the
+    # timed ones: an idle gap there leaves the first timed steps slow
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         flush.zero_()
         step(x, out)
@@ -457,15 +466,12 @@ def run_layer(args):
         raise SystemExit("device status error after warm-up: " + lf.lf_last_error())
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    sampler = ClockSampler(local)
     lf.lf_profile_reset()
     # in the timed loop only attn_main (the roofline's kernel) is bracketed by
     # events: each traced launch costs the stream an event pair
     lf.lf_profile_only("attn_main")
     lf.lf_profile_enable(True)
     torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.3)
     launches0 = lf.lf_launch_count()
     for s_ in range(args.steps):
         flush.zero_()
@@ -608,19 +614,22 @@ def run_backward(args, wl):
         lf.lf_attn_bwd(*bufs, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
 
     bufs = (qd, kd, vd, out, lse, dod, *grads)
+    # the clock sampler starts (and is given time to take its first sample)
+    # before the warm-up, so that the warm-up steps come right before the
+    # timed ones: an idle gap there leaves the first timed steps slow
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         flush.zero_()
         step(bufs)
     torch.cuda.synchronize(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    sampler = ClockSampler(local)
     lf.lf_profile_reset()
     lf.lf_profile_only("bwd_band")
     lf.lf_profile_enable(True)
     torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.3)
     launches0 = lf.lf_launch_count()
     for s_ in range(args.steps):
         flush.zero_()
@@ -788,19 +797,22 @@ def run_variant(args, wl, variant: str):
         kernel = "attn_main (extra-block build)"
     flops = 4 * wl.D * pairs
 
+    # the clock sampler starts (and is given time to take its first sample)
+    # before the warm-up, so that the warm-up steps come right before the
+    # timed ones: an idle gap there leaves the first timed steps slow
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         flush.zero_()
         step(qd, kd, vd, out, dev_extra)
     torch.cuda.synchronize(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    sampler = ClockSampler(local)
     lf.lf_profile_reset()
     lf.lf_profile_only("attn_main")
     lf.lf_profile_enable(True)
     torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.3)
     launches0 = lf.lf_launch_count()
     for s_ in range(args.steps):
         flush.zero_()

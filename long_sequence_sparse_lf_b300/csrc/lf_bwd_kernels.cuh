@@ -23,9 +23,10 @@
 // Each block pair computes S = Q K^T and dP = dO V^T with WMMA (bf16 in, fp32
 // accumulation) into shared memory, forms P and dS (bf16) element by element
 // with the class's mask, then dV += P^T dO, dK += dS^T Q and dQ += dS K.  The
-// CTA's fixed rows (keys, or global rows) sum in shared memory and are added
-// to the fp32 gradients (zeroed first) once, with atomics; the streamed rows'
-// sums are added with atomics after every block pair.
+// CTA's fixed rows (keys, or global rows) sum in WMMA accumulator fragments,
+// each warp holding its share of the tiles for the CTA's whole life, and are
+// added to the fp32 gradients (zeroed first) once, with atomics; the streamed
+// rows' sums are added with atomics after every block pair.
 #pragma once
 
 #include <cstdint>
@@ -93,7 +94,6 @@ struct BwdSmem {
   float dp[kBwdB * LD::SQ];
   __nv_bfloat16 p[kBwdB * LD::PQ], ds[kBwdB * LD::PQ];
   float acc[kBwdB * LD::A];      // product tile before it is added to global memory
-  float st0[kBwdB * LD::A], st1[kBwdB * LD::A];   // the fixed rows' sums over the streamed blocks
   float lse[kBwdB], delta[kBwdB];
   int qpos[kBwdB], kpos[kBwdB];  // positions of the block's rows (-1: none)
   int qglob[kBwdB];              // the query row is a global token
@@ -148,6 +148,58 @@ __device__ __forceinline__ void bwd_gemm(float* C, int ldc, const __nv_bfloat16*
   }
 }
 
+// A [64 x N] fp32 sum held in registers: warp w keeps the accumulator
+// fragments of tiles w, w + 8, ... of the 4 x N/16 grid of 16 x 16 tiles.
+// mma() adds A B with bwd_gemm's operand conventions; store() writes the sum
+// to shared memory (row stride ldc).
+template <int N>
+struct BwdFragAcc {
+  static constexpr int TN = N / 16;
+  static constexpr int NF = 4 * TN / (kBwdThreads / 32);
+  static_assert(NF * (kBwdThreads / 32) == 4 * TN, "tiles must split evenly over the warps");
+  nvcuda::wmma::fragment<nvcuda::wmma::accumulator, 16, 16, 16, float> f[NF];
+
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int m = 0; m < NF; ++m) nvcuda::wmma::fill_fragment(f[m], 0.f);
+  }
+  template <int K, bool A_COL, bool B_ROW>
+  __device__ __forceinline__ void mma(const __nv_bfloat16* A, int lda, const __nv_bfloat16* B,
+                                      int ldb) {
+    using namespace nvcuda;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m = 0; m < NF; ++m) {
+      const int t = warp + m * (kBwdThreads / 32);
+      const int mi = t / TN, ni = t - mi * TN;
+#pragma unroll
+      for (int kk = 0; kk < K / 16; ++kk) {
+        using ALay = typename std::conditional<A_COL, wmma::col_major, wmma::row_major>::type;
+        using BLay = typename std::conditional<B_ROW, wmma::row_major, wmma::col_major>::type;
+        wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, ALay> a;
+        wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, BLay> b;
+        const __nv_bfloat16* ap = A_COL ? A + (size_t)kk * 16 * lda + mi * 16
+                                        : A + (size_t)mi * 16 * lda + kk * 16;
+        const __nv_bfloat16* bp = B_ROW ? B + (size_t)kk * 16 * ldb + ni * 16
+                                        : B + (size_t)ni * 16 * ldb + kk * 16;
+        wmma::load_matrix_sync(a, ap, lda);
+        wmma::load_matrix_sync(b, bp, ldb);
+        wmma::mma_sync(f[m], a, b, f[m]);
+      }
+    }
+  }
+  __device__ __forceinline__ void store(float* C, int ldc) const {
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m = 0; m < NF; ++m) {
+      const int t = warp + m * (kBwdThreads / 32);
+      const int mi = t / TN, ni = t - mi * TN;
+      nvcuda::wmma::store_matrix_sync(C + (size_t)mi * 16 * ldc + ni * 16, f[m], ldc,
+                                      nvcuda::wmma::mem_row_major);
+    }
+  }
+};
+
 // acc [64 x D] (row stride BwdLd::A, scaled) added to X[bh, rows[c], :]
 // with atomics
 template <int D>
@@ -160,9 +212,10 @@ __device__ __forceinline__ void bwd_add_rows(float* X, const float* acc, float s
   }
 }
 
-// kind 0: band tile; 1: global keys; 2: global rows.  One CTA per unit.
+// kind 0: band tile; 1: global keys; 2: global rows.  One CTA per unit (two
+// per SM for D = 64, whose shared memory allows it).
 template <int D, int KIND>
-__global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1) lf_bwd_kernel(const BwdParams p) {
   extern __shared__ __align__(128) uint8_t bwd_smem_raw[];
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(bwd_smem_raw);
   using LD = BwdLd<D>;
@@ -204,10 +257,11 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
     }
     fixed_pos[c] = pos;
   }
-  for (int x = threadIdx.x; x < kBwdB * LD::A; x += blockDim.x) {
-    sm.st0[x] = 0.f;
-    sm.st1[x] = 0.f;
-  }
+  // the fixed rows' sums over the streamed blocks: dV, dK of the keys, or
+  // dQ of the global rows (fix0 only)
+  BwdFragAcc<D> fix0, fix1;
+  fix0.zero();
+  fix1.zero();
   __syncthreads();
   if (KIND == 2) {
     bwd_load_rows<D>(sm.q, p.q, bh, p.L, sm.qpos);
@@ -293,21 +347,26 @@ __global__ void __launch_bounds__(kBwdThreads) lf_bwd_kernel(const BwdParams p) 
       bwd_gemm<D, kBwdB, true, true>(sm.acc, LD::A, sm.ds, LD::PQ, sm.q, LD::X);
       __syncthreads();
       bwd_add_rows<D>(p.dk, sm.acc, p.scale, bh, p.L, sm.kpos);
-      bwd_gemm<D, kBwdB, false, true, true>(sm.st0, LD::A, sm.ds, LD::PQ, sm.k, LD::X);
+      fix0.template mma<kBwdB, false, true>(sm.ds, LD::PQ, sm.k, LD::X);
     } else {
-      bwd_gemm<D, kBwdB, true, true, true>(sm.st0, LD::A, sm.p, LD::PQ, sm.dout, LD::X);
-      bwd_gemm<D, kBwdB, true, true, true>(sm.st1, LD::A, sm.ds, LD::PQ, sm.q, LD::X);
+      fix0.template mma<kBwdB, true, true>(sm.p, LD::PQ, sm.dout, LD::X);
+      fix1.template mma<kBwdB, true, true>(sm.ds, LD::PQ, sm.q, LD::X);
       bwd_gemm<D, kBwdB, false, true>(sm.acc, LD::A, sm.ds, LD::PQ, sm.k, LD::X);
       __syncthreads();
       bwd_add_rows<D>(p.dq, sm.acc, p.scale, bh, p.L, sm.qpos);
     }
   }
   __syncthreads();
+  fix0.store(sm.acc, LD::A);
+  __syncthreads();
   if (KIND == 2) {
-    bwd_add_rows<D>(p.dq, sm.st0, p.scale, bh, p.L, sm.qpos);
+    bwd_add_rows<D>(p.dq, sm.acc, p.scale, bh, p.L, sm.qpos);
   } else {
-    bwd_add_rows<D>(p.dv, sm.st0, 1.f, bh, p.L, sm.kpos);
-    bwd_add_rows<D>(p.dk, sm.st1, p.scale, bh, p.L, sm.kpos);
+    bwd_add_rows<D>(p.dv, sm.acc, 1.f, bh, p.L, sm.kpos);
+    __syncthreads();
+    fix1.store(sm.acc, LD::A);
+    __syncthreads();
+    bwd_add_rows<D>(p.dk, sm.acc, p.scale, bh, p.L, sm.kpos);
   }
 }
 
