@@ -215,6 +215,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, pg=None, device="cpu") -> float:
+    """The maximum of x over the ranks of the default process group (x itself
+    without one): the job's time is its slowest replica's."""
+    if pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(flops_per_step: float, steps: int, world_size: int, total_ms: float) -> float:
+    """Whole-job useful TFLOP/s of `world_size` replicas, each running `steps`
+    steps of the same workload in `total_ms` (the maximum over ranks)."""
+    return flops_per_step * world_size * steps / (total_ms * 1e-3) / 1e12
+
+
 def run_reference(args, wl):
     ws, rank, local = dist_env()
     if rank != 0:
@@ -332,13 +348,8 @@ def run_ours(args, wl):
     lf.lf_profile_reset()
     if lf.lf_attn_get_status(stream) != 0:
         raise SystemExit("device status error in timed region: " + lf.lf_last_error())
-    if pg:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
-
-    n_units = ws * args.steps
-    value = flops * n_units / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms, pg, dev)
+    value = replica_value(flops, args.steps, ws, total_ms)
     ms_per_step = total_ms / args.steps
 
     # ---- end to end through the host-buffer entry point (pinned memory)
@@ -352,12 +363,8 @@ def run_ours(args, wl):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         lf.lf_attn_fwd_host(qh, kh, vh, oh, wl.w, wl.dilation, wl.global_idx, wl.scale, stream)
-    e2e_s = time.perf_counter() - t0
-    if pg:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = flops * ws * e2e_steps / e2e_s / 1e12
+    e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
+    e2e_value = replica_value(flops, e2e_steps, ws, e2e_s * 1e3)
     io_bytes = qh.numel() * qh.element_size()
 
     if rank != 0:

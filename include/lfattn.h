@@ -130,7 +130,10 @@ LF_API lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v, v
  *            T >= d*nqt for every head; entries in [-1, nqt).
  * Other arguments and errors as lf_attn_fwd; LF_ERR_INVALID_ARG for a table
  * of the wrong shape or an entry out of range.  The table is part of the
- * cached plan: a new table builds (and keeps) a new plan.
+ * cached plan: a new table builds (and keeps) a new plan.  When 32 tables are
+ * cached, the next new one first frees them all (their plans included), after
+ * a cudaDeviceSynchronize; tables drawn anew every step therefore cost a
+ * plan build per call and a device synchronization every 32 calls.
  */
 LF_API lf_status lf_attn_fwd_blocks(const void* q, const void* k, const void* v, void* out,
                                     int B, int H, int L, int D, int w,

@@ -278,6 +278,12 @@ std::vector<int32_t> xblock_key(int H, const int32_t* xb, int T, int R) {
   return k;
 }
 
+// Patterns with extra-block tables are cached like the others, but a
+// caller may draw a new table every step: past kMaxExtraPatterns of them the
+// next new one first evicts them all (see evict_extra_patterns).
+constexpr size_t kMaxExtraPatterns = 32;
+void evict_extra_patterns();   // needs g_mu held
+
 lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const int32_t* gidx,
                       int n_g, std::shared_ptr<Pattern>* out, const int32_t* xb = nullptr,
                       int T = 0, int R = 0) {
@@ -289,6 +295,11 @@ lf_status get_pattern(int dev, int H, int L, int w, const int32_t* dil, const in
   if (it != g_patterns.end()) {
     *out = it->second;
     return LF_OK;
+  }
+  if (!std::get<6>(key).empty()) {
+    size_t n_extra = 0;
+    for (const auto& kv : g_patterns) n_extra += kv.second->xkey.empty() ? 0 : 1;
+    if (n_extra >= kMaxExtraPatterns) evict_extra_patterns();
   }
   auto pat = std::make_shared<Pattern>();
   pat->H = H;
@@ -655,6 +666,40 @@ using ParamKey = std::tuple<const Plan*, const void*, const void*, const void*, 
                             const uint8_t*, float, float*, const float*>;
 std::map<ParamKey, std::unique_ptr<MainParams>> g_params;
 constexpr size_t kMaxCachedParams = 256;
+
+// Frees every cached pattern that has an extra-block table, with its plans
+// and their kernel parameters, after the device has finished all work
+// queued so far (an in-flight kernel may still read a plan's work list).
+void evict_extra_patterns() {
+  cudaDeviceSynchronize();
+  for (auto it = g_params.begin(); it != g_params.end();) {
+    const Plan* pl = std::get<0>(it->first);
+    if (pl != nullptr && !pl->pat->xkey.empty())
+      it = g_params.erase(it);
+    else
+      ++it;
+  }
+  for (auto it = g_plans.begin(); it != g_plans.end();) {
+    if (!it->second->pat->xkey.empty()) {
+      if (it->second->d_items) cudaFree(it->second->d_items);
+      it = g_plans.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  for (auto it = g_patterns.begin(); it != g_patterns.end();) {
+    Pattern& pt = *it->second;
+    if (!pt.xkey.empty()) {
+      cudaFree(pt.d_G);
+      cudaFree(pt.d_isg);
+      cudaFree(pt.d_gcnt);
+      cudaFree(pt.d_dil);
+      it = g_patterns.erase(it);
+    } else {
+      ++it;
+    }
+  }
+}
 
 // Kernel parameters of one call: tensor maps of q, k, v (one residue view
 // per dilation value) and of the gathered global rows, and the scratch

@@ -143,6 +143,21 @@ def test_base_config_random_blocks_sampled_rows(lf):
     assert np.isfinite(got).all()
 
 
+def test_many_tables_evict_and_stay_correct(lf):
+    """40 distinct random tables in a row (past the 32 the library caches, so
+    the cached ones are freed once on the way); outputs stay right, and an
+    evicted table works again when it comes back."""
+    B, H, L, D, w, dil, G = 1, 2, 768, 64, 24, (1, 2), (5,)
+    q, k, v = _inputs((B, H, L, D), 12)
+    tabs = [W.random_blocks(L, dil, 2, 100 + n) for n in range(40)]
+    outs = [_run(lf, q, k, v, w, dil, G, t, 0.125).float().cpu().double().numpy()
+            for t in tabs]
+    for n in (0, 31, 32, 39):
+        _assert_close(outs[n], _ref(q, k, v, w, dil, G, tabs[n], 0.125), f"table {n}")
+    again = _run(lf, q, k, v, w, dil, G, tabs[0], 0.125).float().cpu().double().numpy()
+    assert np.array_equal(again, outs[0])
+
+
 def test_table_errors(lf):
     q, k, v = _inputs((1, 2, 512, 64), 1)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
