@@ -1280,10 +1280,11 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   if ((s = fwd_impl(qkv, qkv + act, qkv + 2 * act, a, false, B, H, L, D, w, dilation, gidx, n_g,
                     scale, stream)) != LF_OK)
     return s;
-  const int threads = 256;
+  // the LayerNorm kernels, one warp per row, four rows per CTA (small CTAs
+  // pack into the register file with less of a tail wave), with the widest
+  // vector (VW columns, NJ steps per lane) the width allows
+  const int threads = 128;
   const unsigned rows_blocks = (unsigned)((M + threads / 32 - 1) / (threads / 32));
-  // the LayerNorm kernels, with the widest vector (VW columns, NJ steps per
-  // lane) the width allows
   auto launch_ln1 = [&](auto vw, auto nj) {
     constexpr int VW = decltype(vw)::value, NJ = decltype(nj)::value;
     traced("layer_merge_ln1", stream, [&] {

@@ -87,6 +87,26 @@ __device__ __forceinline__ void layer_store_bf16(uint16_t* p, const float (&v)[V
   }
 }
 
+// VW consecutive fp32 values (16-byte loads for VW = 4, 8; 8-byte for VW = 2;
+// p aligned to VW floats)
+template <int VW>
+__device__ __forceinline__ void layer_load_f32(const float* p, float (&v)[VW]) {
+  if (VW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < VW / 4; ++i) {
+      const float4 t = reinterpret_cast<const float4*>(p)[i];
+      v[4 * i] = t.x;
+      v[(4 * i + 1) % VW] = t.y;
+      v[(4 * i + 2) % VW] = t.z;
+      v[(4 * i + 3) % VW] = t.w;
+    }
+  } else {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x;
+    v[1 % VW] = t.y;
+  }
+}
+
 // LayerNorm of one token row held by one warp: lane t holds the VW
 // consecutive columns VW*t + 32*VW*j, j < NJ (hidden = 32 * VW * NJ).
 template <int VW, int NJ>
@@ -117,9 +137,11 @@ __device__ __forceinline__ void layer_norm_row(float (&v)[NJ][VW], float eps,
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int c = VW * lane + 32 * VW * j;
-    float y[VW];
+    float g[VW], bt[VW], y[VW];
+    layer_load_f32<VW>(gamma + c, g);
+    layer_load_f32<VW>(beta + c, bt);
 #pragma unroll
-    for (int e = 0; e < VW; ++e) y[e] = (v[j][e] - mean) * rstd * gamma[c + e] + beta[c + e];
+    for (int e = 0; e < VW; ++e) y[e] = (v[j][e] - mean) * rstd * g[e] + bt[e];
     layer_store_bf16<VW>(out_row + c, y);
   }
 }
@@ -164,15 +186,12 @@ __global__ void lf_layer_ln2_kernel(const uint16_t* __restrict__ x1, const float
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int c = VW * lane + 32 * VW * j;
-    float xa[VW];
+    float xa[VW], fa[VW], ba[VW];
     layer_load_bf16<VW>(x1 + (size_t)row * hidden + c, xa);
+    layer_load_f32<VW>(F + (size_t)row * hidden + c, fa);
+    layer_load_f32<VW>(bf + c, ba);
 #pragma unroll
-    for (int i = 0; i < VW; i += 2) {
-      const float2 f = *reinterpret_cast<const float2*>(F + (size_t)row * hidden + c + i);
-      const float2 bb = *reinterpret_cast<const float2*>(bf + c + i);
-      v[j][i] = xa[i] + f.x + bb.x;
-      v[j][(i + 1) % VW] = xa[(i + 1) % VW] + f.y + bb.y;
-    }
+    for (int i = 0; i < VW; ++i) v[j][i] = xa[i] + fa[i] + ba[i];
   }
   layer_norm_row<VW, NJ>(v, eps, ln2, ln2 + hidden, lane, y + (size_t)row * hidden);
 }
