@@ -1273,7 +1273,8 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   if (gs != LF_OK) return gs;
   if (M > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "B*L=%lld tokens is too many", M);
   traced("layer_split_qkv", stream, [&] {
-    lf::lf_layer_split_qkv_kernel<<<(unsigned)M, 3 * hidden / 8, 0, stream>>>(
+    lf::lf_layer_split_qkv_kernel<<<(unsigned)((M + lf::kSplitRows - 1) / lf::kSplitRows),
+                                    3 * hidden / 8, 0, stream>>>(
         reinterpret_cast<const uint4*>(y), reinterpret_cast<const float4*>(b_qkv),
         reinterpret_cast<uint4*>(qkv), B, H, L, D);
   });

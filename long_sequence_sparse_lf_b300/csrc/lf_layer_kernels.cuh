@@ -24,29 +24,41 @@ __device__ __forceinline__ uint32_t layer_pack_bf16x2(float lo, float hi) {
 
 // Y: bf16 [M = B*L, 3*hidden] (row = token, columns q | k | v features, head
 // h of each at h*D .. h*D + D-1); bias fp32 [3*hidden].  qkv: bf16, three
-// consecutive [B, H, L, D] tensors: qkv = bf16(Y + bias).  One CTA per token
-// row, one thread per 8 consecutive columns (16 bytes in, 16 bytes out).
+// consecutive [B, H, L, D] tensors: qkv = bf16(Y + bias).  One thread per 8
+// consecutive columns (16 bytes in, 16 bytes out) of ROWS consecutive token
+// rows per CTA: the ROWS loads are issued before the first store, so that
+// each thread keeps several 16-byte reads in flight.
+constexpr int kSplitRows = 4;
 __global__ void lf_layer_split_qkv_kernel(const uint4* __restrict__ Y,
                                           const float4* __restrict__ bias,
                                           uint4* __restrict__ qkv, int B, int H, int L, int D) {
   const int hidden = H * D;
   const int c8 = threadIdx.x;                    // column group: columns 8*c8 .. 8*c8+7
   if (c8 >= 3 * hidden / 8) return;
-  const long long row = blockIdx.x;              // token b*L + l
-  const int b = (int)(row / L), l = (int)(row % L);
+  const long long M = (long long)B * L;
+  const long long row0 = (long long)blockIdx.x * kSplitRows;
+  uint4 y[kSplitRows];
+#pragma unroll
+  for (int r = 0; r < kSplitRows; ++r)
+    if (row0 + r < M) y[r] = Y[(row0 + r) * (3 * hidden / 8) + c8];
   const int c = 8 * c8;
   const int s = c / hidden, hc = c - s * hidden;
   const int h = hc / D, e = hc - h * D;
-  const uint4 y = Y[row * (3 * hidden / 8) + c8];
   const float4 b0 = bias[2 * c8], b1 = bias[2 * c8 + 1];
   auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
   auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
-  const uint4 o = make_uint4(layer_pack_bf16x2(lo(y.x) + b0.x, hi(y.x) + b0.y),
-                             layer_pack_bf16x2(lo(y.y) + b0.z, hi(y.y) + b0.w),
-                             layer_pack_bf16x2(lo(y.z) + b1.x, hi(y.z) + b1.y),
-                             layer_pack_bf16x2(lo(y.w) + b1.z, hi(y.w) + b1.w));
-  const size_t dst = ((((size_t)s * B + b) * H + h) * L + l) * D + e;
-  qkv[dst / 8] = o;
+#pragma unroll
+  for (int r = 0; r < kSplitRows; ++r) {
+    const long long row = row0 + r;              // token b*L + l
+    if (row >= M) break;
+    const int b = (int)(row / L), l = (int)(row % L);
+    const uint4 o = make_uint4(layer_pack_bf16x2(lo(y[r].x) + b0.x, hi(y[r].x) + b0.y),
+                               layer_pack_bf16x2(lo(y[r].y) + b0.z, hi(y[r].y) + b0.w),
+                               layer_pack_bf16x2(lo(y[r].z) + b1.x, hi(y[r].z) + b1.y),
+                               layer_pack_bf16x2(lo(y[r].w) + b1.z, hi(y[r].w) + b1.w));
+    const size_t dst = ((((size_t)s * B + b) * H + h) * L + l) * D + e;
+    qkv[dst / 8] = o;
+  }
 }
 
 // bf16 <-> fp32 vectors of VW elements (VW = 2, 4 or 8: 4, 8 or 16 bytes)
