@@ -120,3 +120,57 @@ def test_binding_raises_without_cuda_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         lf_attn_fwd(q, q, q, q.clone(), 2, [1], [], 0.125)
+
+
+def _prototypes():
+    """name -> (return type, [parameter declarations]) of every LF_API call."""
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"LF_API\s+([\w\s\*]+?)\b(lf_\w+)\s*\(([^)]*)\)\s*;", text):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        protos[name] = (ret, plist)
+    return protos
+
+
+def _ctype_kind(decl: str) -> str:
+    """'ptr', 'i32', 'i64', 'u64', 'f32' or 'other' of a C parameter or return type."""
+    d = decl.replace("const", " ").strip()
+    if "*" in d or re.search(r"\blf_stream_t\b", d):
+        return "ptr"
+    if re.search(r"\b(int64_t|long long)\b", d):
+        return "i64"
+    if re.search(r"\buint64_t\b", d):
+        return "u64"
+    if re.search(r"\b(int|int32_t|lf_status)\b", d):
+        return "i32"
+    if re.search(r"\bfloat\b", d):
+        return "f32"
+    return "other"
+
+
+def _ctypes_kind(t) -> str:
+    if t is None:
+        return "void"
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "_type_") and isinstance(
+            getattr(t, "_type_", None), type):
+        return "ptr"
+    return {ctypes.c_int32: "i32", ctypes.c_int: "i32", ctypes.c_int64: "i64",
+            ctypes.c_longlong: "i64", ctypes.c_uint64: "u64", ctypes.c_float: "f32"}.get(t, "other")
+
+
+def test_binding_signatures_match_header(lib):
+    """Every call the header declares has ctypes argtypes of the same length
+    and kinds (pointer / int32 / int64 / uint64 / float) and the same return
+    kind, so the binding and the library cannot drift apart."""
+    protos = _prototypes()
+    assert set(protos) == set(declared_symbols())
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
+        got = [_ctypes_kind(t) for t in fn.argtypes]
+        want = [_ctype_kind(p) for p in params]
+        assert got == want, f"{name}: binding {got} vs header {want}"
+        want_ret = "void" if ret == "void" else _ctype_kind(ret)
+        assert _ctypes_kind(fn.restype) == want_ret, f"{name}: return {fn.restype} vs {ret}"
