@@ -33,6 +33,11 @@
  *     every later call on that stream.  A stream handle that is destroyed
  *     and reused by a new stream inherits the buffer: finish the old
  *     stream's work first.
+ *   - Threads: the caches are locked, and calls from several host threads
+ *     may overlap, with one exception.  A call that frees cached plans
+ *     (lf_plan_cache_clear, and a call with a new extra-block table once 32
+ *     are cached: see lf_attn_fwd_blocks) must not overlap calls of other
+ *     threads that use the plans it frees.
  *   - No C++ exception crosses this interface.  A non-OK status leaves a
  *     message for lf_last_error() in the calling thread.
  *   - Device-side waits are bounded; a wait that runs out records a timeout

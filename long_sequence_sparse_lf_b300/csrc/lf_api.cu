@@ -664,7 +664,9 @@ lf_status get_workspace(int dev, cudaStream_t stream, size_t bytes, uint8_t** ou
 // nothing.
 using ParamKey = std::tuple<const Plan*, const void*, const void*, const void*, void*, bool,
                             const uint8_t*, float, float*, const float*>;
-std::map<ParamKey, std::unique_ptr<MainParams>> g_params;
+// (shared ownership: a call keeps its parameters alive until it has
+// launched, even if another thread clears the cache meanwhile)
+std::map<ParamKey, std::shared_ptr<MainParams>> g_params;
 constexpr size_t kMaxCachedParams = 256;
 
 // Frees every cached pattern that has an extra-block table, with its plans
@@ -829,24 +831,24 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   }
 
   const ParamKey pkey{pl, qb, kb, vb, out, f32, ws, scale, lse, rel_bias};
-  MainParams* cached = nullptr;
+  std::shared_ptr<MainParams> cached;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_params.find(pkey);
-    if (it != g_params.end()) cached = it->second.get();
+    if (it != g_params.end()) cached = it->second;
   }
   uint16_t* qg = reinterpret_cast<uint16_t*>(ws + off_g);
   uint16_t* kg = qg + g_elems;
   uint16_t* vg = kg + g_elems;
   if (cached == nullptr) {
-    auto fresh = std::make_unique<MainParams>();
+    auto fresh = std::make_shared<MainParams>();
     if ((s = build_params(ds, *pl, *pat, qb, kb, vb, out, f32, ws, off_g, off_po, off_pm, scale,
                           lse, rel_bias, fresh.get())) != LF_OK)
       return s;
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_params.size() >= kMaxCachedParams) g_params.clear();
-    cached = fresh.get();
-    g_params[pkey] = std::move(fresh);
+    cached = fresh;
+    g_params[pkey] = fresh;
   }
   const MainParams& prm = *cached;
 
