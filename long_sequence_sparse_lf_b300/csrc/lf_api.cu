@@ -867,6 +867,10 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   }
   if (prm.n_items > 0) {
     const int grid = pl->grid;
+    // the kernel build: plain, with a relative position bias (BIAS: adds the
+    // padded table to the window's scores), or with extra key blocks per
+    // slot (XB: random / strided block patterns); the plain build is not
+    // affected by the others' code
     traced("attn_main", stream, [&] {
       if (D == 64 && xb)
         lf::lf_attn_main_kernel<64, false, true><<<grid, lf::KCfg<64>::THREADS, lf::KCfg<64>::SMEM_BYTES, stream>>>(prm);
