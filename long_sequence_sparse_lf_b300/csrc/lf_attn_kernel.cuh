@@ -43,9 +43,8 @@
 // common reference point gives the same O / l, and this keeps the rescale (a
 // TMEM round trip) off the common path.  Warps find, per 16-key chunk of a
 // block, whether all of their 32 rows see the chunk fully, not at all, or in
-// part: chunks no row sees are skipped (P = 0), and only partial chunks are
-// masked element by element.  A fixed share of the exponentials runs on the
-// FMA pipe (exp2_poly2) to relieve the special-function unit.
+// part: only chunks not every row sees are masked, and a block no row of the
+// warp sees is skipped (P = 0).
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // kStatusTimeout in the device status word, all roles leave their loops,
@@ -64,8 +63,8 @@
 #ifndef LF_SLOT_OFFSET
 #define LF_SLOT_OFFSET 1   // start slot 1 half a block after slot 0 (D = 64)
 #endif
-#ifndef LF_EMU16_D64
-#define LF_EMU16_D64 0     // exponentials per 16 columns done on the FMA pipe (D = 64)
+#ifndef LF_WAIT_SPIN
+#define LF_WAIT_SPIN 0
 #endif
 #ifndef LF_REGS_SM64
 #define LF_REGS_SM64 216   // register split, softmax / other warpgroups (D = 64)
@@ -74,9 +73,6 @@
 #ifndef LF_REGS_SM128
 #define LF_REGS_SM128 216  // (D = 128)
 #define LF_REGS_OT128 72
-#endif
-#ifndef LF_EMU16_D128
-#define LF_EMU16_D128 0    // (D = 128)
 #endif
 
 namespace lf {
@@ -90,7 +86,6 @@ struct KCfg {
   static constexpr int NQ = (D == 64) ? 2 : 1;      // Q buffers per slot
   static constexpr int NST = (D == 64) ? 4 : 2;     // K/V stages
   static constexpr bool P_ALIAS = (D != 64);        // P_X lives in S_X's columns
-  static constexpr int EMU16 = (D == 64) ? LF_EMU16_D64 : LF_EMU16_D128;
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
   static constexpr uint32_t TM_P0 = P_ALIAS ? 0 : 256, TM_P1 = P_ALIAS ? 128 : 320;
   static constexpr uint32_t TM_O0 = P_ALIAS ? 256 : 384, TM_O1 = P_ALIAS ? 384 : 448;
@@ -136,10 +131,26 @@ struct Waiter {
 // inlined at every wait site.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
                                           bool honour_abort) {
+#if LF_WAIT_SPIN
+  // poll without suspending; the bound is the same time, read from the
+  // global timer every 64 polls
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = static_cast<uint64_t>(w.iters) * kWaitSliceNs;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (honour_abort && *w.abort) return false;
+      if (globaltimer_ns() - t0 > limit) break;
+    }
+  }
+#else
+  if (mbar_try_wait(bar, parity)) return true;   // already complete: no suspend hint
   for (uint32_t it = 0; it < w.iters; ++it) {
     if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return true;
     if (honour_abort && (it & 255u) == 255u && *w.abort) return false;
   }
+#endif
   *w.abort = 1;
   atomicOr(w.status, kStatusTimeout);
   return false;
@@ -513,14 +524,20 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
         continue;
       }
       int d = 1, i = 0, wlo = 0, whi = p.L - 1, gi = 0;
+      // windows of the warp's first row and of its last valid row (every
+      // row of a global-row item sees all L keys)
+      int wf_lo = 0, wf_hi = p.L - 1, wl_lo = 0, wl_hi = p.L - 1;
       bool rowvalid;
       if (band) {
         d = p.dil[wi.slot];
         const int Lr = residue_len(p.L, d, wi.r);
-        const int t = wi.t0 + kBM * X + row;
+        const int tf = wi.t0 + kBM * X + q4 * 32;
+        const int t = tf + lane;
         i = wi.r + d * t;
         rowvalid = t < Lr;
         band_window(t, p.w, Lr, wlo, whi);
+        band_window(tf, p.w, Lr, wf_lo, wf_hi);
+        band_window(min(tf + 31, Lr - 1), p.w, Lr, wl_lo, wl_hi);
       } else {
         gi = wi.r * kBM + row;
         rowvalid = gi < p.n_g;
@@ -557,28 +574,28 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           mbar_arrive(BAR(C::B_PF + X));
           continue;
         }
-        bool all_full = false;
-        if (j < wi.nkb) {
-          // interior blocks (every row sees all 128 keys) need no masks
-          const int kpos0 = wi.kb0 + kBN * j;
-          all_full = __reduce_max_sync(FULL, wlo - kpos0) <= 0 &&
-                     __reduce_min_sync(FULL, whi - kpos0) >= kBN - 1;
-        }
-        // this row's visible columns as four 32-bit words, and the warp-wide
-        // classes of the 16-key chunks: seen by some row (vis) / by every row
-        // (full)
+        // Which 16-key chunks of the block the warp's rows see: by some row
+        // (vis) / by every row (full).  v0..v3 hold this row's visible
+        // columns; they are only read for chunks seen in part.
         uint32_t v0 = ~0u, v1 = ~0u, v2 = ~0u, v3 = ~0u;
         uint32_t vis = 0xFFu, full = 0xFFu;
-        if (!all_full) {
-          if (j < wi.nkb) {
-            // band block / key chunk: the columns [clo, chi]
-            const int kpos0 = wi.kb0 + kBN * j;
+        if (j < wi.nkb) {
+          // band block / key chunk: the rows' windows [wlo, whi] grow with
+          // the row, so the warp's union is [wlo(first), whi(last)] and its
+          // intersection [wlo(last), whi(first)]: the chunk classes follow
+          // from warp-uniform scalars
+          const int kpos0 = wi.kb0 + kBN * j;
+          vis = chunk_overlap_bits(wf_lo - kpos0, wl_hi - kpos0);
+          full = chunk_inside_bits(wl_lo - kpos0, wf_hi - kpos0);
+          if (vis != full) {
             const int clo = wlo - kpos0, chi1 = whi - kpos0 + 1;
             v0 = range_bits(clo, chi1, 0);
             v1 = range_bits(clo, chi1, 32);
             v2 = range_bits(clo, chi1, 64);
             v3 = range_bits(clo, chi1, 96);
-          } else if (XB && j >= wi.nkb + wi.ngb) {
+          }
+        } else {
+          if (XB && j >= wi.nkb + wi.ngb) {
             // extra block: its keys inside [0, Lr), minus the row's window
             // (the band blocks hold those) and the global positions (the
             // gathered blocks hold those)
@@ -634,7 +651,6 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             full |= (ah == 0xffffu ? 1u : 0u) << ch;
           }
         }
-        const bool live0 = (vis & 0x0Fu) != 0u, live1 = (vis & 0xF0u) != 0u;
         // P_X (and O_X) are free once the previous O += P V of this slot has
         // completed; that is awaited just before the first write (for
         // D = 128, S_X(k) was issued after PV_X(k-1), so it already has)
@@ -648,164 +664,138 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           return true;
         };
 
-        if (!C::P_ALIAS && !live0 && !live1) {
-          tc_fence_before();
-          mbar_arrive(BAR(C::B_SR + X));
-        }
-
-        // ---- two halves of 64 keys: load, mask, exponentials, row sum, P
-        const float2 sl2v = make_float2(sl2, sl2);
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint32_t tPh = tP + 32 * hf;
-          if (!(hf ? live1 : live0)) {
-            if (!await_pfree()) { ok = false; break; }
-            uint32_t z[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) z[e] = 0u;
-            tmem_st16(tPh, z);
-            tmem_st16(tPh + 16, z);
-            continue;
+        if (vis == 0u) {
+          // no row of the warp sees a key of this block: P = 0
+          if (!C::P_ALIAS) {
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_SR + X));
           }
-          float s[64];
-          {
-            uint32_t r[64];
-            tmem_ld64(tS + 64 * hf, r);
+          if (!await_pfree()) { ok = false; break; }
+          uint32_t z[32];
 #pragma unroll
-            for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 32; ++e) z[e] = 0u;
+          tmem_st32(tP, z);
+          tmem_st32(tP + 32, z);
+        } else {
+          // ---- the whole 128-score row in one TMEM load; S_X is then free
+          // for the next block's product (D = 64)
+          float s[128];
+          {
+            uint32_t r[128];
+            tmem_ld128(tS, r);
+#pragma unroll
+            for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
+          }
+          if (!C::P_ALIAS) {
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_SR + X));
           }
           if (BIAS && band && j < wi.nkb) {
             // rel_bias / scale added to the raw score, so that everything
             // after (max, rescale, exponentials) sees scale*q.k + rel_bias.
-            // The row's 64 values start at I = kBiasPad + w + kpos0 - t in
+            // The row's 128 values start at I = kBiasPad + w + kpos0 - t in
             // the zero-padded table (t the row's residue index; the columns
             // outside the window read padding or neighbours and are masked
             // below).  Copy I % 4 of the table is shifted so that this start
-            // is 16-byte aligned: sixteen 16-byte loads.
-            const int I = kBiasPad + p.w + wi.kb0 + kBN * j + 64 * hf - (wi.t0 + kBM * X + row);
-            const int sft = I & 3;
-            const float4* tp = reinterpret_cast<const float4*>(
-                p.rel_bias + static_cast<size_t>((wi.bh % p.H) * 4 + sft) * bias_row_len(p.w) +
-                (I - sft));
+            // is 16-byte aligned: 16-byte loads.
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float4 bv = __ldg(tp + e);
-              const float2 lo = add2(make_float2(s[4 * e], s[4 * e + 1]), make_float2(bv.x, bv.y));
-              const float2 hi = add2(make_float2(s[4 * e + 2], s[4 * e + 3]), make_float2(bv.z, bv.w));
-              s[4 * e] = lo.x;
-              s[4 * e + 1] = lo.y;
-              s[4 * e + 2] = hi.x;
-              s[4 * e + 3] = hi.y;
-            }
-          }
-          if (!C::P_ALIAS && (hf == 1 || !live1)) {
-            tc_fence_before();
-            mbar_arrive(BAR(C::B_SR + X));
-          }
-          // mask the chunks not every row sees (chunks no row sees entirely)
-          const uint32_t va = hf ? v2 : v0, vb = hf ? v3 : v1;
-          const uint32_t hvis = (vis >> (4 * hf)) & 0xFu, hfull = (full >> (4 * hf)) & 0xFu;
-          if (hfull != 0xFu) {
+            for (int hf = 0; hf < 2; ++hf) {
+              const int I = kBiasPad + p.w + wi.kb0 + kBN * j + 64 * hf - (wi.t0 + kBM * X + row);
+              const int sft = I & 3;
+              const float4* tp = reinterpret_cast<const float4*>(
+                  p.rel_bias + static_cast<size_t>((wi.bh % p.H) * 4 + sft) * bias_row_len(p.w) +
+                  (I - sft));
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              if (hfull & (1u << c4)) continue;
-              if (!(hvis & (1u << c4))) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) s[16 * c4 + e] = NEG_INF;
-              } else {
-                const uint32_t vw = c4 < 2 ? va : vb;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const int bit = 16 * (c4 & 1) + e;
-                  s[16 * c4 + e] = (vw & (1u << bit)) ? s[16 * c4 + e] : NEG_INF;
-                }
+              for (int e = 0; e < 16; ++e) {
+                const float4 bv = __ldg(tp + e);
+                float* sv = s + 64 * hf + 4 * e;
+                const float2 lo = add2(make_float2(sv[0], sv[1]), make_float2(bv.x, bv.y));
+                const float2 hi = add2(make_float2(sv[2], sv[3]), make_float2(bv.z, bv.w));
+                sv[0] = lo.x;
+                sv[1] = lo.y;
+                sv[2] = hi.x;
+                sv[3] = hi.y;
               }
             }
           }
-
-          // Exponentials relative to the row's reference m_ref.  The row max is
-          // only computed when a row has no reference yet (first visible
-          // keys) or when the speculative pass finds a score far above it
-          // (the half's sum exceeds 2^16): then the reference moves, O (and
-          // P's first half) are rescaled, and the half is redone.
-          bool do_max = __any_sync(FULL, m_ref == NEG_INF);
-          float2 acc[4];
-          uint32_t pk[32];
-#pragma unroll 1
-          for (int pass = 0; pass < 2; ++pass) {
-            if (do_max) {
-              float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+          // mask every chunk that not all rows see: unseen ones whole, the
+          // others by the row's own bits (one straight-line path: branching
+          // around unseen chunks measured slower)
+          if (full != 0xFFu) {
 #pragma unroll
-              for (int e = 0; e < 64; e += 2)
-                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
-              const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-              const bool need = mxs > m_ref + 8.0f;
-              const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
-              if (__any_sync(FULL, need && m_ref != NEG_INF)) {
-                if (!await_pfree()) { ok = false; break; }
-                if (!firstblk) {
-#pragma unroll 1
-                  for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + c0, r);
+            for (int c = 0; c < 8; ++c) {
+              if (!(full & (1u << c))) {
+                const uint32_t vw = (vis & (1u << c)) ? (c < 2 ? v0 : (c < 4 ? v1 : (c < 6 ? v2 : v3))) : 0u;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(tO + c0, r);
-                  }
-                }
-                if (hf == 1 && live0) {
-                  uint32_t r[32];
-                  tmem_st_wait();
-                  tmem_ld32(tP, r);
-#pragma unroll
-                  for (int e = 0; e < 32; ++e) {
-                    const float lo = __uint_as_float(r[e] << 16), hi = __uint_as_float(r[e] & 0xffff0000u);
-                    r[e] = pack_bf16x2(lo * alpha, hi * alpha);
-                  }
-                  tmem_st32(tP, r);
-                }
-                tmem_st_wait();
+                for (int e = 0; e < 16; ++e)
+                  s[16 * c + e] = ((vw >> (16 * (c & 1) + e)) & 1u) ? s[16 * c + e] : NEG_INF;
               }
-              l *= alpha;
-              if (need) m_ref = mxs;
             }
+          }
+          const float2 sl2v = make_float2(sl2, sl2);
+          // Moves the row's reference m_ref to this block's row max where
+          // that is more than 2^8 above it (any common reference gives the
+          // same O / l; O and l are rescaled by 2^(m_old - m_new))
+          auto move_reference = [&]() -> bool {
+            float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+            for (int e = 0; e < 128; e += 2)
+              m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
+            const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+            const bool need = mxs > m_ref + 8.0f;
+            const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
+            if (__any_sync(FULL, need && m_ref != NEG_INF) && !firstblk) {
+              if (!await_pfree()) return false;
+#pragma unroll 1
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + c0, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                tmem_st32(tO + c0, r);
+              }
+              tmem_st_wait();
+            }
+            l *= alpha;
+            if (need) m_ref = mxs;
+            return true;
+          };
+          // a row without a reference yet (its first visible keys) takes
+          // this block's max
+          if (__any_sync(FULL, m_ref == NEG_INF) && !move_reference()) { ok = false; break; }
+          // P = 2^(s*sl2 - m_ref), speculatively without this block's max:
+          // each half's bf16 pairs and row sum (masked keys give 0).  Half 0
+          // goes to TMEM while half 1 is computed.
+          uint32_t pk0[32], pk1[32];
+          float lb;
+          {
             const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
             const float2 nmu = make_float2(-mu, -mu);
-            // P = 2^(s*sl2 - m) over all 64 keys (masked ones give 0), its
-            // sum, and bf16 pairs
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-              const float2 x = fma2(make_float2(s[e], s[e + 1]), sl2v, nmu);
-              float2 pv;
-              if ((e & 15) < C::EMU16) {
-                pv = exp2_poly2(x);
-              } else {
-                pv.x = ex2_approx(x.x);
-                pv.y = ex2_approx(x.y);
-              }
-              acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
-              pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
-            }
-            if (do_max) break;
-            const float lh = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                             ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-            if (!__any_sync(FULL, !(lh <= 65536.0f))) break;
-            do_max = true;
+            float2 acc[4];
+            exp2_half<0>(s, sl2v, nmu, pk0, acc);
+            if (!await_pfree()) { ok = false; break; }
+            tmem_st32(tP, pk0);
+            exp2_half<64>(s, sl2v, nmu, pk1, acc);
+            lb = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                 ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
           }
-          if (!ok) break;
-          if (!await_pfree()) { ok = false; break; }
-          {
-            uint32_t a[16], b2[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) { a[e] = pk[e]; b2[e] = pk[16 + e]; }
-            tmem_st16(tPh, a);
-            tmem_st16(tPh + 16, b2);
+          // Rare: a score far above the reference (the block's sum exceeds
+          // 2^16).  The reference moves to the block's max and the block's
+          // P is recomputed.
+          if (__any_sync(FULL, !(lb <= 65536.0f))) {
+            if (!move_reference()) { ok = false; break; }
+            const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+            const float2 nmu = make_float2(-mu, -mu);
+            float2 acc[4];
+            exp2_half<0>(s, sl2v, nmu, pk0, acc);
+            tmem_st32(tP, pk0);
+            exp2_half<64>(s, sl2v, nmu, pk1, acc);
+            lb = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                 ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
           }
-          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+          tmem_st32(tP + 32, pk1);
+          l += lb;
         }
-        if (!ok) break;
         firstblk = false;
         tmem_st_wait();
         tc_fence_before();

@@ -218,6 +218,21 @@ __host__ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base
   return below_b & ~below_a;
 }
 
+// 16-key chunks c (bit c, c = 0..7) of a 128-key block that overlap the
+// columns [lo, hi] / that lie inside them.
+__host__ __device__ __forceinline__ uint32_t chunk_overlap_bits(int lo, int hi) {
+  if (hi < lo || hi < 0 || lo > 127) return 0u;
+  const int a = lo < 0 ? 0 : lo >> 4;
+  const int b = hi > 127 ? 7 : hi >> 4;
+  return ((1u << (b + 1)) - 1u) & ~((1u << a) - 1u);
+}
+__host__ __device__ __forceinline__ uint32_t chunk_inside_bits(int lo, int hi) {
+  const int a = lo <= 0 ? 0 : (lo + 15) >> 4;
+  const int b = hi >= 127 ? 7 : ((hi + 1) >> 4) - 1;
+  if (hi < lo || a > b || a > 7 || b < 0) return 0u;
+  return ((1u << (b + 1)) - 1u) & ~((1u << a) - 1u);
+}
+
 // Number of positions p in [0, L) with p mod d == r.
 __host__ __device__ __forceinline__ int residue_len(int L, int d, int r) {
   return r < L ? (L - 1 - r) / d + 1 : 0;

@@ -242,20 +242,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
-// 64 consecutive columns starting at taddr, without waiting: the registers
-// are valid only after tmem_wait_ld_pin on them.
-__device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
-      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
-      "%62, %63}, [%64];"
-      : LF_R8(0), LF_R8(8), LF_R8(16), LF_R8(24), LF_R8(32), LF_R8(40), LF_R8(48), LF_R8(56)
-      : "r"(taddr)
-      : "memory");
-}
-
 // 128 consecutive columns starting at taddr; waits for completion.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -277,29 +263,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 }
 
 #undef LF_R8
-
-#define LF_P8(b) "+r"(r[b + 0]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), \
-                 "+r"(r[b + 4]), "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
-
-// Waits for this thread's outstanding TMEM loads; the registers of `r` are
-// tied to the wait, so that no use of them is scheduled before it.
-__device__ __forceinline__ void tmem_wait_ld_pin(uint32_t (&r)[64]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : LF_P8(0), LF_P8(8), LF_P8(16), LF_P8(24), LF_P8(32), LF_P8(40), LF_P8(48), LF_P8(56)
-               :
-               : "memory");
-}
-
-// Ties the registers of `r` to this point of the program (after an earlier
-// tmem_wait_ld_pin), for loads that the same wait completed.
-__device__ __forceinline__ void regs_pin(uint32_t (&r)[64]) {
-  asm volatile(""
-               : LF_P8(0), LF_P8(8), LF_P8(16), LF_P8(24), LF_P8(32), LF_P8(40), LF_P8(48), LF_P8(56)
-               :
-               : "memory");
-}
-
-#undef LF_P8
 
 #define LF_W8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), \
                  "r"(r[b + 4]), "r"(r[b + 5]), "r"(r[b + 6]), "r"(r[b + 7])
@@ -389,37 +352,23 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
 #endif
 }
 
-// 2^x for a pair of arguments x <= 8 on the FMA pipe instead of the
-// special-function unit (the software-exp2 idea of FlashAttention-4):
-// split x = n + f with n = round(x) (the 1.5 * 2^23 rounding constant puts n
-// in the low mantissa bits), evaluate 2^f on [-1/2, 1/2] with a cubic and
-// add n to the exponent field.  The cubic is our own relative-error minimax
-// fit (Remez exchange; csrc/fit_exp2_poly.py reproduces it): max relative
-// error 7.5e-5, below the bf16 rounding the result then goes through.
-// Arguments are clamped at -125 so that the exponent never underflows; the
-// result there (2^-125) stands in for 0 and is negligible in every sum.
-namespace exp2poly {
-constexpr float C0 = 0.9999280571937561f;
-constexpr float C1 = 0.6932609677314758f;
-constexpr float C2 = 0.2426111251115799f;
-constexpr float C3 = 0.0551716685295105f;
-constexpr float RND = 12582912.0f;   // 1.5 * 2^23
-}  // namespace exp2poly
-
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  using namespace exp2poly;
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 t = add2(x, make_float2(RND, RND));             // n in the low bits
-  const float2 n = add2(t, make_float2(-RND, -RND));           // n as a float
-  const float2 f = add2(x, make_float2(-n.x, -n.y));           // x - n in [-1/2, 1/2]
-  float2 q = fma2(f, make_float2(C3, C3), make_float2(C2, C2));
-  q = fma2(q, f, make_float2(C1, C1));
-  q = fma2(q, f, make_float2(C0, C0));
-  float2 r;
-  r.x = __int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23));
-  r.y = __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23));
-  return r;
+// P = 2^(s*sl2 - m) for the 64 scores s[C0 .. C0+63] of a row: bf16 pairs
+// (round to nearest even) into pk, and their fp32 sum into four fresh
+// accumulators (C0 = 0) or on top of them (C0 = 64).
+template <int C0>
+__device__ __forceinline__ void exp2_half(const float (&s)[128], float2 sl2v, float2 nmu,
+                                          uint32_t (&pk)[32], float2 (&acc)[4]) {
+  if (C0 == 0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float2 x = fma2(make_float2(s[C0 + e], s[C0 + e + 1]), sl2v, nmu);
+    const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+    pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
+  }
 }
 
 }  // namespace lf
