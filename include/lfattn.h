@@ -260,8 +260,13 @@ LF_API lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, v
  * the output is the same.  It calls no cudaMalloc, cudaFree or other
  * allocating routine: its scratch (work list, global-position tables,
  * gathered global rows, global-row partials) lives in one fixed device array
- * of 32 MiB that the library declares and that every GPU loading the library
- * holds until the process exits.  A problem needing more scratch is rejected
+ * of 32 MiB that the library declares.  A device holds the array from the
+ * library's first use on it until the process exits: the library's device
+ * code is loaded lazily, on the first call of any of its entry points on
+ * that device, and the array is reserved then.  A caller whose allocator
+ * will hold the device's free memory should therefore make one call per
+ * device at start-up, before the allocator reserves its memory.  A problem
+ * needing more scratch is rejected
  * with LF_ERR_UNSUPPORTED and a message giving both sizes (for example B=1,
  * H=16, L=65536, D=128 with 16 global tokens needs about 55 MiB).  Problems
  * without global tokens need only the work list and the global flags.

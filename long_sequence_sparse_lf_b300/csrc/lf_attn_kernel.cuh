@@ -63,9 +63,6 @@
 #ifndef LF_SLOT_OFFSET
 #define LF_SLOT_OFFSET 1   // start slot 1 half a block after slot 0 (D = 64)
 #endif
-#ifndef LF_WAIT_SPIN
-#define LF_WAIT_SPIN 0
-#endif
 #ifndef LF_REGS_SM64
 #define LF_REGS_SM64 216   // register split, softmax / other warpgroups (D = 64)
 #define LF_REGS_OT64 72
@@ -131,26 +128,11 @@ struct Waiter {
 // inlined at every wait site.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
                                           bool honour_abort) {
-#if LF_WAIT_SPIN
-  // poll without suspending; the bound is the same time, read from the
-  // global timer every 64 polls
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  const uint64_t limit = static_cast<uint64_t>(w.iters) * kWaitSliceNs;
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (honour_abort && *w.abort) return false;
-      if (globaltimer_ns() - t0 > limit) break;
-    }
-  }
-#else
   if (mbar_try_wait(bar, parity)) return true;   // already complete: no suspend hint
   for (uint32_t it = 0; it < w.iters; ++it) {
     if (mbar_try_wait_hint(bar, parity, kWaitSliceNs)) return true;
     if (honour_abort && (it & 255u) == 255u && *w.abort) return false;
   }
-#endif
   *w.abort = 1;
   atomicOr(w.status, kStatusTimeout);
   return false;
@@ -579,6 +561,13 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
         // columns; they are only read for chunks seen in part.
         uint32_t v0 = ~0u, v1 = ~0u, v2 = ~0u, v3 = ~0u;
         uint32_t vis = 0xFFu, full = 0xFFu;
+        // Gathered blocks of many globals (or at D = 128, where P aliases
+        // S and the previous product has completed by now) take the chunked
+        // path below.  At D = 64 a narrow gathered block keeps the full-row
+        // path: its exponentials cover the wait for the previous product,
+        // which the short chunked path would expose.
+        const bool gathered = (XB ? (j >= wi.nkb && j < wi.nkb + wi.ngb) : j >= wi.nkb) &&
+                              (C::P_ALIAS || p.NGB >= 64);
         if (j < wi.nkb) {
           // band block / key chunk: the rows' windows [wlo, whi] grow with
           // the row, so the warp's union is [wlo(first), whi(last)] and its
@@ -636,19 +625,21 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
             v2 = range_bits(0, nvalid, 64) & ~(range_bits(c_lo, c_hi, 64) & ~off2);
             v3 = range_bits(0, nvalid, 96) & ~(range_bits(c_lo, c_hi, 96) & ~off3);
           }
-          const uint32_t o0 = __reduce_or_sync(FULL, v0), o1 = __reduce_or_sync(FULL, v1);
-          const uint32_t o2 = __reduce_or_sync(FULL, v2), o3 = __reduce_or_sync(FULL, v3);
-          const uint32_t a0 = __reduce_and_sync(FULL, v0), a1 = __reduce_and_sync(FULL, v1);
-          const uint32_t a2 = __reduce_and_sync(FULL, v2), a3 = __reduce_and_sync(FULL, v3);
-          const uint32_t ow[4] = {o0, o1, o2, o3}, aw[4] = {a0, a1, a2, a3};
-          vis = 0;
-          full = 0;
+          if (!gathered) {
+            const uint32_t o0 = __reduce_or_sync(FULL, v0), o1 = __reduce_or_sync(FULL, v1);
+            const uint32_t o2 = __reduce_or_sync(FULL, v2), o3 = __reduce_or_sync(FULL, v3);
+            const uint32_t a0 = __reduce_and_sync(FULL, v0), a1 = __reduce_and_sync(FULL, v1);
+            const uint32_t a2 = __reduce_and_sync(FULL, v2), a3 = __reduce_and_sync(FULL, v3);
+            const uint32_t ow[4] = {o0, o1, o2, o3}, aw[4] = {a0, a1, a2, a3};
+            vis = 0;
+            full = 0;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t oh = (ow[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
-            const uint32_t ah = (aw[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
-            vis |= (oh != 0u ? 1u : 0u) << ch;
-            full |= (ah == 0xffffu ? 1u : 0u) << ch;
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint32_t oh = (ow[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
+              const uint32_t ah = (aw[ch >> 1] >> (16 * (ch & 1))) & 0xffffu;
+              vis |= (oh != 0u ? 1u : 0u) << ch;
+              full |= (ah == 0xffffu ? 1u : 0u) << ch;
+            }
           }
         }
         // P_X (and O_X) are free once the previous O += P V of this slot has
@@ -664,7 +655,77 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
           return true;
         };
 
-        if (vis == 0u) {
+        // Moves the row's reference m_ref to the block's row max mxs (log2
+        // units) where that is more than 2^8 above it: any common reference
+        // gives the same O / l, and O and l are rescaled by 2^(m_old - m_new).
+        auto rebase = [&](float mxs) -> bool {
+          const bool need = mxs > m_ref + 8.0f;
+          const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
+          if (__any_sync(FULL, need && m_ref != NEG_INF) && !firstblk) {
+            if (!await_pfree()) return false;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c0, r);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(tO + c0, r);
+            }
+            tmem_st_wait();
+          }
+          l *= alpha;
+          if (need) m_ref = mxs;
+          return true;
+        };
+
+        if (gathered) {
+          // Gathered global keys: the product wrote only the block's first
+          // NGB columns, so the row is handled in 16-column chunks of them:
+          // the row max first, then P (columns past NGB are never read by
+          // O += P V, whose K extent is NGB).
+          const int nch = p.NGB >> 4;
+          float mx = NEG_INF;
+#pragma unroll 1
+          for (int c = 0; c < nch; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tS + 16 * c, r);
+            const uint32_t vw = (c < 2 ? v0 : (c < 4 ? v1 : (c < 6 ? v2 : v3))) >> (16 * (c & 1));
+#pragma unroll
+            for (int e = 0; e < 16; e += 2)
+              mx = fmax3(mx, ((vw >> e) & 1u) ? __uint_as_float(r[e]) : NEG_INF,
+                         ((vw >> (e + 1)) & 1u) ? __uint_as_float(r[e + 1]) : NEG_INF);
+          }
+          if (!rebase(mx * sl2)) { ok = false; break; }
+          const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+          const float2 nmu = make_float2(-mu, -mu), sl2v = make_float2(sl2, sl2);
+          float2 acc[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
+          if (!await_pfree()) { ok = false; break; }
+#pragma unroll 1
+          for (int c = 0; c < nch; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tS + 16 * c, r);
+            const uint32_t vw = (c < 2 ? v0 : (c < 4 ? v1 : (c < 6 ? v2 : v3))) >> (16 * (c & 1));
+            uint32_t pk8[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float2 sv = make_float2(((vw >> e) & 1u) ? __uint_as_float(r[e]) : NEG_INF,
+                                            ((vw >> (e + 1)) & 1u) ? __uint_as_float(r[e + 1]) : NEG_INF);
+              const float2 x = fma2(sv, sl2v, nmu);
+              const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+              pk8[e >> 1] = pack_bf16x2(pv.x, pv.y);
+            }
+            tmem_st8(tP + 8 * c, pk8);
+          }
+          if (!C::P_ALIAS) {
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_SR + X));
+          }
+          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+               ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+        } else if (vis == 0u) {
           // no row of the warp sees a key of this block: P = 0
           if (!C::P_ALIAS) {
             tc_fence_before();
@@ -741,24 +802,7 @@ __global__ void __launch_bounds__(384, 1) lf_attn_main_kernel(const __grid_const
 #pragma unroll
             for (int e = 0; e < 128; e += 2)
               m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s[e], s[e + 1]);
-            const float mxs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-            const bool need = mxs > m_ref + 8.0f;
-            const float alpha = need ? (m_ref == NEG_INF ? 0.f : ex2_approx(m_ref - mxs)) : 1.f;
-            if (__any_sync(FULL, need && m_ref != NEG_INF) && !firstblk) {
-              if (!await_pfree()) return false;
-#pragma unroll 1
-              for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tO + c0, r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                tmem_st32(tO + c0, r);
-              }
-              tmem_st_wait();
-            }
-            l *= alpha;
-            if (need) m_ref = mxs;
-            return true;
+            return rebase(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2);
           };
           // a row without a reference yet (its first visible keys) takes
           // this block's max

@@ -1,15 +1,23 @@
 """The Longformer layer forward (lf_layer_fwd) against the layer oracle.
 
-The GPU path stores q, k, v, the attention output, x1 and the result in bf16
-at the same points as oracle.longformer_layer(store_bf16=True); its products
-accumulate in fp32 (the GEMMs and the attention) where the oracle uses
-float64.  Tolerance, beyond half a bf16 step of the reference value:
-  - the attention step's own error (within 1e-2 max-abs against float64,
-    typically a few 1e-3);
-  - LayerNorm's division by the row's spread (about 1) and gamma (about 1);
-  - an occasional one-step bf16 difference where an fp32 and a float64
-    intermediate fall on either side of a rounding boundary.
-The result stays within max-abs 2e-2 and rel-L2 1e-2.
+Primary check: the plain float64 layer (oracle.longformer_layer with
+store_bf16=False), which is pinned to a dense torch layer by the CPU tests.
+The GPU path stores the q/k/v product, q, k, v, the attention output, x1 and
+the result in bf16 (the storage points its header documents) and accumulates
+its products in fp32.  Tolerance against float64, derived from those points
+(bf16 unit roundoff u = 2^-8):
+  - the final bf16 store: u * |y| per element, allowed on top of the bound;
+  - upstream, to first order: the q/k/v roundings (2u relative) move the
+    attention output by about 1e-3 rms, the stored attention output and x1
+    add u * |a| and u * |x1|, and the feed-forward map carries x1's error
+    through (rms about u * rms(x1)); after LayerNorm (dividing by a row
+    spread of about sqrt(2)) the result's upstream error is about 2.5e-3 rms,
+    about 1.3e-2 at five standard deviations over the 6.3M outputs of the
+    largest case;
+  - so: |gpu - ref| <= 3e-2 + u * |ref| per element, and rel-L2 <= 1e-2.
+Second check, tighter: the oracle with the same bf16 storage points
+(store_bf16=True), which isolates the accumulation-order and attention-kernel
+error: |gpu - ref| <= 2e-2 + u * |ref|, rel-L2 <= 1e-2.
 """
 import numpy as np
 import pytest
@@ -19,7 +27,8 @@ from long_sequence_sparse_lf_b300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS = 2e-2
+MAX_ABS_F64 = 3e-2      # against the float64 layer (see above)
+MAX_ABS_STORED = 2e-2   # against the layer with the same bf16 storage points
 REL_L2 = 1e-2
 BF16_HALF_ULP = 2.0 ** -8
 
@@ -44,18 +53,27 @@ def _run(lf, lw, inputs):
     return out.float().cpu().double().numpy()
 
 
-def _oracle(lw, inputs, rows=None):
+def _oracle(lw, inputs, rows=None, store_bf16=False):
     import oracle as O
     x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2 = (t.double().numpy() for t in inputs)
     return O.longformer_layer(x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, lw.H, lw.w, lw.dilation,
-                              lw.global_idx, lw.scale, lw.eps, store_bf16=True, rows=rows)
+                              lw.global_idx, lw.scale, lw.eps, store_bf16=store_bf16,
+                              rows=rows)
 
 
-def _close(got, ref, what):
+def _close(got, ref, what, max_abs):
     d = np.abs(got - ref) - BF16_HALF_ULP * np.abs(ref)
     rel = float(np.linalg.norm((got - ref).ravel()) / np.linalg.norm(ref.ravel()))
-    assert float(d.max()) <= MAX_ABS and rel <= REL_L2, \
+    print(f"{what}: max(|err| - u|ref|)={float(d.max()):.3e} "
+          f"max|err|={float(np.abs(got - ref).max()):.3e} rel_l2={rel:.3e}")
+    assert float(d.max()) <= max_abs and rel <= REL_L2, \
         f"{what}: max_abs={float(d.max()):.3e} rel_l2={rel:.3e}"
+
+
+def _check(got, lw, inputs, what, rows=None):
+    _close(got, _oracle(lw, inputs, rows=rows), what + " (float64 layer)", MAX_ABS_F64)
+    _close(got, _oracle(lw, inputs, rows=rows, store_bf16=True),
+           what + " (bf16 storage points)", MAX_ABS_STORED)
 
 
 SMALL = [
@@ -68,7 +86,7 @@ SMALL = [
 @pytest.mark.parametrize("lw", SMALL, ids=[c.name for c in SMALL])
 def test_layer_matches_oracle(lf, lw):
     inputs = W.make_layer_inputs(lw)
-    _close(_run(lf, lw, inputs), _oracle(lw, inputs), lw.name)
+    _check(_run(lf, lw, inputs), lw, inputs, lw.name)
 
 
 def test_layer_base_size_sampled_rows(lf):
@@ -77,7 +95,7 @@ def test_layer_base_size_sampled_rows(lf):
     got = _run(lf, lw, inputs)
     rows = sorted({0, 1, 127, 128, 255, 256, 2047, 2048, 4094, 4095} |
                   set(np.random.default_rng(7).integers(0, lw.L, 22).tolist()))
-    _close(got[:, rows], _oracle(lw, inputs, rows=rows), "layer-base rows")
+    _check(got[:, rows], lw, inputs, "layer-base rows", rows=rows)
 
 
 def test_layer_rejects_unsupported_width_and_misaligned_pointers(lf):

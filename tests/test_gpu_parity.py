@@ -1,13 +1,17 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
 
-Tolerance (for every output comparison), in float64 on the same
-bf16-rounded inputs:
-  * max |gpu - oracle| <= 1e-2 beyond the output format's own rounding:
-    a bf16 output cannot be closer to the exact value than half a bf16 ulp
-    (2^-8 relative), so each element may differ by 1e-2 + 2^-8 * |oracle|
-    (fp32 outputs get no allowance);
-  * ||gpu - oracle||_2 / ||oracle||_2 <= 5e-3.
-Key lists are compared bit-exactly.
+Tolerance, in float64 on the same bf16-rounded inputs:
+  * the five workloads (tiny, base, dilated, qa, long): the plain bound,
+    max |gpu - oracle| <= 1e-2 and ||gpu - oracle||_2 / ||oracle||_2 <= 5e-3,
+    on every output element of tiny, base, dilated and qa, and on a row
+    sample of long (edges, around globals, random rows); the measured values
+    are printed;
+  * the other shapes (randomised, with outputs up to |out| of a few units):
+    each element may also differ by the bf16 output's own rounding,
+    2^-8 * |oracle| (a bf16 value cannot be nearer the exact result than
+    half its step), on top of 1e-2; fp32 outputs get no allowance.
+Key lists are compared bit-exactly: in full for tiny, base, dilated and qa,
+and for long the totals and a row sample.
 """
 import math
 
@@ -51,6 +55,14 @@ def _assert_close(got, ref, what="", out_bf16=True):
     return mx, rel
 
 
+def _assert_plain(got, ref, what):
+    """The workloads' bound with no allowance for the output's rounding."""
+    mx, rel = _errors(got, ref, out_bf16=False)
+    print(f"{what}: max_abs={mx:.3e} rel_l2={rel:.3e} elements={got.size}")
+    assert mx <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs={mx:.3e} rel_l2={rel:.3e}"
+    return mx, rel
+
+
 def _run(lf, q, k, v, w, dil, G, scale):
     """q, k, v: CPU tensors (bf16 or fp32).  Returns the output as float64."""
     qd, kd, vd = (t.cuda() for t in (q, k, v))
@@ -75,7 +87,7 @@ def test_tiny_config_full_parity(lf):
     q, k, v = W.make_qkv(wl)
     got = _run(lf, q, k, v, wl.w, wl.dilation, wl.global_idx, wl.scale)
     ref = O.attention(_f64(q), _f64(k), _f64(v), wl.w, wl.dilation, wl.global_idx, wl.scale)
-    _assert_close(got, ref, "tiny", out_bf16=False)
+    _assert_plain(got, ref, "tiny")
 
 
 # ------------------------------------------------ closed-form special cases
@@ -157,7 +169,19 @@ def test_repeat_calls_are_deterministic(lf):
     np.testing.assert_array_equal(a, b)
 
 
-# -------------------------------------------- full-size configs (sampled)
+# -------------------------------------------------------- full-size configs
+
+@pytest.mark.parametrize("name", ["base", "dilated", "qa"])
+def test_config_full_size_every_element(lf, name):
+    """The full-size workload in the bench's launch configuration, every
+    output element against the oracle (about 1e11 to 3e11 fp64 FLOP each on
+    the host)."""
+    wl = W.CONFIGS[name]
+    q, k, v = W.make_qkv(wl)
+    got = _run(lf, q, k, v, wl.w, wl.dilation, wl.global_idx, wl.scale)
+    ref = O.attention(_f64(q), _f64(k), _f64(v), wl.w, wl.dilation, wl.global_idx, wl.scale)
+    _assert_plain(got, ref, name)
+
 
 def _sample_rows(wl, n_extra, seed):
     L = wl.L
@@ -169,18 +193,17 @@ def _sample_rows(wl, n_extra, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["base", "dilated", "qa", "long"])
-def test_config_full_size_sampled_rows(lf, name):
-    """The full-size workload in the bench's launch configuration; the oracle
-    computes a sample of rows (edges, around globals, random)."""
-    wl = W.CONFIGS[name]
+def test_config_long_sampled_rows(lf):
+    """B=1, H=16, L=65536, D=128: the oracle's full cost (3.5e13 fp64 FLOP)
+    is out of reach, so a row sample (edges, around globals, random) is
+    compared, and every row is checked to be finite."""
+    wl = W.CONFIGS["long"]
     q, k, v = W.make_qkv(wl)
     got = _run(lf, q, k, v, wl.w, wl.dilation, wl.global_idx, wl.scale)
-    rows = _sample_rows(wl, 64 if name == "long" else 128, wl.seed)
+    rows = _sample_rows(wl, 64, wl.seed)
     qf, kf, vf = _f64(q), _f64(k), _f64(v)
     ref = O.attention(qf, kf, vf, wl.w, wl.dilation, wl.global_idx, wl.scale, rows=rows)
-    _assert_close(got[:, :, rows], ref, name)
-    # every row is finite and every row was written
+    _assert_plain(got[:, :, rows], ref, "long (sampled rows)")
     assert np.isfinite(got).all()
 
 
@@ -206,29 +229,36 @@ def test_pairs_bit_exact_small(lf, pat):
     np.testing.assert_array_equal(col.cpu().numpy(), col_ref)
 
 
-@pytest.mark.parametrize("name", ["tiny", "base", "dilated", "qa", "long"])
-def test_pairs_configs(lf, name):
-    """Totals equal the closed form; sampled rows equal the oracle's lists."""
+@pytest.mark.parametrize("name", ["tiny", "base", "dilated", "qa"])
+def test_pairs_configs_full(lf, name):
+    """Every key list of the workload's pattern, bit-exact against the
+    oracle's enumeration, and the total against the closed form."""
     wl = W.CONFIGS[name]
+    row_ptr, col, total = lf.lf_attn_pairs(wl.H, wl.L, wl.w, wl.dilation, wl.global_idx)
+    rp_ref, col_ref = O.key_lists(wl.L, wl.w, wl.dilation, wl.global_idx)
+    assert total == int(rp_ref[-1]) == O.total_pairs(wl.L, wl.w, wl.dilation, wl.global_idx)
+    np.testing.assert_array_equal(row_ptr.cpu().numpy(), rp_ref)
+    np.testing.assert_array_equal(col.cpu().numpy(), col_ref)
+
+
+def test_pairs_long_total_and_sampled_rows(lf):
+    """long: the whole CSR is built on the device (1.1e9 entries, 4.4 GB);
+    the total is checked against the closed form and a sample of rows
+    (edges, globals, random) bit-exactly against the oracle's lists."""
+    wl = W.CONFIGS["long"]
     H = wl.H
-    row_ptr, col, total = lf.lf_attn_pairs(H, wl.L, wl.w, wl.dilation, wl.global_idx,
-                                           count_only=(name == "long"))
+    row_ptr, col, total = lf.lf_attn_pairs(H, wl.L, wl.w, wl.dilation, wl.global_idx)
     assert total == O.total_pairs(wl.L, wl.w, wl.dilation, wl.global_idx)
     rp = row_ptr.cpu().numpy()
     rng = np.random.default_rng(5)
     rows = [(h, i) for h in range(H) for i in
-            sorted(set(rng.integers(0, wl.L, 40).tolist()) | {0, wl.L - 1}
+            sorted(set(rng.integers(0, wl.L, 40).tolist()) | {0, 1, wl.L - 2, wl.L - 1}
                    | set(wl.global_idx[:3]))]
     _, col_ref = O.key_lists(wl.L, wl.w, wl.dilation, wl.global_idx, rows=rows)
-    rp_ref = np.concatenate([[0], np.cumsum([len(O.key_set(i, wl.L, wl.w, wl.dilation[h],
-                                                            wl.global_idx)) for h, i in rows])])
-    for n, (h, i) in enumerate(rows):
-        r = h * wl.L + i
-        assert rp[r + 1] - rp[r] == rp_ref[n + 1] - rp_ref[n]
-    if col is not None:
-        c = col.cpu().numpy()
-        got = np.concatenate([c[rp[h * wl.L + i]:rp[h * wl.L + i + 1]] for h, i in rows])
-        np.testing.assert_array_equal(got, col_ref)
+    got = torch.cat([col[int(rp[h * wl.L + i]):int(rp[h * wl.L + i + 1])] for h, i in rows])
+    np.testing.assert_array_equal(got.cpu().numpy(), col_ref)
+    del col
+    torch.cuda.empty_cache()
 
 
 def test_pairs_capacity_error(lf):
