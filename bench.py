@@ -277,6 +277,44 @@ def run_reference(args, wl):
     return 0
 
 
+# Timed steps are queued in batches behind a GPU-side pause (torch.cuda._sleep
+# of about 10 ms at 2 GHz), long enough for the host to queue a batch.
+QUEUE_BATCH = 100
+QUEUE_SLEEP_CYCLES = 20_000_000
+
+
+def percentiles_us(ms_list):
+    """median, p10 and p90 of per-step times, in microseconds."""
+    a = sorted(1e3 * x for x in ms_list)
+    pick = lambda f: a[min(len(a) - 1, max(0, int(round(f * (len(a) - 1)))))]   # noqa: E731
+    return {"median_us": pick(0.5), "p10_us": pick(0.1), "p90_us": pick(0.9), "n": len(a)}
+
+
+def host_link(qh, kh, vh, oh, dev, reps: int = 3):
+    """Time plain pinned copies: q, k, v host->device on one stream while
+    the output's bytes go device->host on another (the copy engines work in
+    both directions at once).  Returns the best of ``reps``."""
+    nb = qh.numel() * qh.element_size()
+    dq = torch.empty(3 * qh.numel(), dtype=qh.dtype, device=dev)
+    do = torch.empty_like(oh, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = None
+    for _ in range(reps):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s_in):
+            for x, t in enumerate((qh, kh, vh)):
+                dq[x * qh.numel():(x + 1) * qh.numel()].view_as(t).copy_(t, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            oh.copy_(do, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    return {"ms": best * 1e3, "h2d_bytes": 3 * nb, "d2h_bytes": nb,
+            "h2d_gbs": 3 * nb / best / 1e9,
+            "what": "pinned cudaMemcpyAsync of the same bytes, in and out concurrently"}
+
+
 def run_ours(args, wl):
     import long_sequence_sparse_lf_b300 as lf
     ws, rank, local = dist_env()
@@ -330,11 +368,16 @@ def run_ours(args, wl):
         pg.barrier()
     torch.cuda.synchronize(dev)
     launches0 = lf.lf_launch_count()
-    for s in range(args.steps):
-        flush.zero_()
-        evs[s][0].record(stream)
-        step()
-        evs[s][1].record(stream)
+    for lo in range(0, args.steps, QUEUE_BATCH):
+        # a GPU-side pause ahead of each batch lets the host queue the
+        # batch's launches before the GPU reaches them, so that the events
+        # time the GPU's work and not the host's launch rate
+        torch.cuda._sleep(QUEUE_SLEEP_CYCLES)
+        for s in range(lo, min(args.steps, lo + QUEUE_BATCH)):
+            flush.zero_()
+            evs[s][0].record(stream)
+            step()
+            evs[s][1].record(stream)
     torch.cuda.synchronize(dev)
     launches = lf.lf_launch_count() - launches0
     if pg:
@@ -349,6 +392,29 @@ def run_ours(args, wl):
     if lf.lf_attn_get_status(stream) != 0:
         raise SystemExit("device status error in timed region: " + lf.lf_last_error())
     total_ms = max_over_ranks(total_ms, pg, dev)
+
+    # ---- a second, L2-warm series (no flush between steps), reported
+    # beside the cold headline: the same steps back to back
+    wsteps = max(3, min(args.steps, 200))
+    wevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(wsteps)]
+    for _ in range(3):
+        step()
+    lf.lf_profile_enable(True)
+    lf.lf_profile_only("attn_main")
+    torch.cuda.synchronize(dev)
+    for lo in range(0, wsteps, QUEUE_BATCH):
+        torch.cuda._sleep(QUEUE_SLEEP_CYCLES)
+        for s_ in range(lo, min(wsteps, lo + QUEUE_BATCH)):
+            wevs[s_][0].record(stream)
+            step()
+            wevs[s_][1].record(stream)
+    torch.cuda.synchronize(dev)
+    lf.lf_profile_enable(False)
+    lf.lf_profile_only(None)
+    warm_ms = [a.elapsed_time(b) for a, b in wevs]
+    warm_main_ms, warm_main_n = lf.lf_profile_query("attn_main")
+    lf.lf_profile_reset()
     value = replica_value(flops, args.steps, ws, total_ms)
     ms_per_step = total_ms / args.steps
 
@@ -366,6 +432,9 @@ def run_ours(args, wl):
     e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
     e2e_value = replica_value(flops, e2e_steps, ws, e2e_s * 1e3)
     io_bytes = qh.numel() * qh.element_size()
+    # the host link alone: plain pinned copies of the same bytes, in (q, k,
+    # v) and out at the same time on two streams, the bound of the e2e call
+    link = host_link(qh, kh, vh, oh, dev)
 
     if rank != 0:
         if pg:
@@ -401,13 +470,25 @@ def run_ours(args, wl):
         "data": "synthetic (seeded N(0,1), bf16-rounded)",
         "config": dict(wl.describe(), parallelism=f"replica x{ws}",
                        l2="flushed between timed steps (256 MiB memset)",
+                       queue=f"launches queued ahead of the GPU in batches of {QUEUE_BATCH}",
                        pairs=pairs * wl.B),
         "peak_frac_bf16": value / peaks["bf16_tflops"],
         "roofline": roof,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 3 * io_bytes,
                 "d2h_bytes_per_step": io_bytes, "steps": e2e_steps,
-                "api": "lf_attn_fwd_host (pinned host buffers)"},
+                "api": "lf_attn_fwd_host (pinned host buffers)",
+                "ms_per_step": e2e_s * 1e3 / e2e_steps,
+                "host_link": link,
+                "link_bound_frac": link["ms"] / (e2e_s * 1e3 / e2e_steps)},
+        "series": {
+            "cold": dict(percentiles_us(step_ms), attn_main_avg_us=1e3 * main_ms / max(main_n, 1),
+                         l2="256 MiB memset before every step"),
+            "warm": dict(percentiles_us(warm_ms),
+                         attn_main_avg_us=1e3 * warm_main_ms / max(warm_main_n, 1),
+                         attn_main_tflops=flops / (warm_main_ms / max(warm_main_n, 1) * 1e-3) / 1e12,
+                         steps=wsteps, l2="no flush (back-to-back steps)"),
+        },
         "clocks": clocks,
     }
     if ws == 1 and not args.no_cpu_baseline:

@@ -237,10 +237,16 @@ LF_API lf_status lf_layer_fwd(const void* x, const void* w_qkv, const float* b_q
 
 /*
  * lf_attn_fwd_host — lf_attn_fwd (is_f32 == 0) or lf_attn_fwd_f32
- * (is_f32 != 0) on HOST buffers: copies q, k, v to device memory it
- * allocates on `stream`, runs the forward, copies the result into the host
- * buffer `out` and synchronises the stream before returning.  Pinned host
- * memory gives asynchronous copies; pageable memory works too.
+ * (is_f32 != 0) on HOST buffers, same layout: copies q, k, v to device
+ * memory it allocates on `stream`, runs the forward, copies the result into
+ * the host buffer `out` and synchronises `stream` before returning.  The
+ * work is split into chunks of whole heads of one batch element (about
+ * eight chunks), pipelined over two streams of the library, so that the
+ * copies in, the computation and the copies out of different chunks
+ * overlap; those streams start after the work already queued on `stream`,
+ * and `stream` continues after them.  Pinned host memory gives
+ * asynchronous copies (pageable memory works, without the overlap).  One
+ * host-buffer call runs at a time per process.
  */
 LF_API lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, void* out, int is_f32,
                            int B, int H, int L, int D, int w, const int32_t* dilation,

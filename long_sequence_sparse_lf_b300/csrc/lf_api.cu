@@ -392,14 +392,12 @@ void build_items(Plan& pl, int num_sms) {
     pl.NGQ = 0;
   }
   // key-chunk length of the global-row items: about half a band pair's
-  // blocks, so that they also fill the tail of the schedule
-  int pair_blocks = 0;
-  for (int h = 0; h < H; ++h) {
-    const int d = pt.dil[h];
-    const int Lr = lf::residue_len(L, d, 0);
-    const int span = std::min(2 * lf::kBM + 2 * w, Lr);
-    pair_blocks = std::max(pair_blocks, ceil_div(span, lf::kBN) + pl.n_gblk);
-  }
+  // blocks (of an undilated head), so that they also fill the tail of the
+  // schedule.  It depends on (L, w, n_g) only, not on which heads a call
+  // holds, so that a head's global rows are summed in the same key chunks
+  // whatever heads it is computed with.
+  const int pair_blocks =
+      ceil_div(std::min(2 * lf::kBM + 2 * w, L), lf::kBN) + pl.n_gblk;
   const int nblocks = ceil_div(L, lf::kBN);
   int n_items1 = 0, CB = 0;
   if (n_g > 0) {
@@ -1551,6 +1549,102 @@ lf_status blocks_fwd_impl(const void* q, const void* k, const void* v, void* out
 
 }  // namespace
 
+// ------------------------------------------------------- host-buffer forward
+//
+// lf_attn_fwd_host splits the problem into chunks of whole heads of one
+// batch element (each head's attention is independent of the others) and
+// pipelines them over two streams of the library: while one chunk is
+// computed, the next one's inputs are copied in and the previous one's
+// output is copied out, so that the host link, which bounds this call,
+// carries data in both directions while the GPU computes.  The streams are
+// ordered after the caller's stream at entry, and the caller's stream after
+// them at exit.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t s[2] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
+};
+std::vector<HostPipe> g_host_pipe;
+std::mutex g_host_mu;   // one host-buffer call at a time per process (it blocks anyway)
+
+constexpr int kHostChunks = 8;   // target number of chunks per call
+
+lf_status fwd_host_impl(const void* q, const void* k, const void* v, void* out, bool f32, int B,
+                        int H, int L, int D, int w, const int32_t* dilation,
+                        const int32_t* gidx, int n_g, float scale, cudaStream_t st) {
+  t_last_error.clear();
+  if (!q || !k || !v || !out) return fail(LF_ERR_INVALID_ARG, "a host pointer is NULL");
+  if (B < 1 || H < 1 || L < 1 || (D != 64 && D != 128))
+    return fail(LF_ERR_INVALID_ARG, "bad shape B=%d H=%d L=%d D=%d", B, H, L, D);
+  if (dilation == nullptr) return fail(LF_ERR_INVALID_ARG, "dilation is NULL");
+  // the whole pattern is checked once here, so that a bad argument fails
+  // before any copy
+  lf_status s = check_pattern(H, L, w, dilation, gidx, n_g);
+  if (s != LF_OK) return s;
+  std::lock_guard<std::mutex> hk(g_host_mu);
+  int dev = 0;
+  LF_CUDA(cudaGetDevice(&dev));
+  if ((int)g_host_pipe.size() <= dev) g_host_pipe.resize(dev + 1);
+  HostPipe& hp = g_host_pipe[dev];
+  if (!hp.ready) {
+    for (int x = 0; x < 2; ++x) {
+      LF_CUDA(cudaStreamCreateWithFlags(&hp.s[x], cudaStreamNonBlocking));
+      LF_CUDA(cudaEventCreateWithFlags(&hp.join[x], cudaEventDisableTiming));
+    }
+    LF_CUDA(cudaEventCreateWithFlags(&hp.fork, cudaEventDisableTiming));
+    hp.ready = true;
+  }
+  const size_t esz = f32 ? 4 : 2;
+  const size_t head = (size_t)L * D * esz;   // bytes of one (b, h) slice
+  const size_t bytes = (size_t)B * H * head;
+  // heads per chunk: whole heads of one batch element, about kHostChunks
+  // chunks in all
+  const int per_b = std::max(1, kHostChunks / B);
+  const int hc = (H + per_b - 1) / per_b;
+
+  uint8_t* buf = nullptr;
+  LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&buf), 4 * align_up(bytes, 256), st));
+  uint8_t* dq = buf;
+  uint8_t* dk = dq + align_up(bytes, 256);
+  uint8_t* dv = dk + align_up(bytes, 256);
+  uint8_t* dout = dv + align_up(bytes, 256);
+  cudaError_t e = cudaEventRecord(hp.fork, st);
+  for (int x = 0; x < 2 && e == cudaSuccess; ++x) e = cudaStreamWaitEvent(hp.s[x], hp.fork, 0);
+  int chunk = 0;
+  for (int b = 0; b < B && e == cudaSuccess && s == LF_OK; ++b) {
+    for (int h0 = 0; h0 < H && e == cudaSuccess && s == LF_OK; h0 += hc, ++chunk) {
+      const int nh = std::min(hc, H - h0);
+      const size_t off = ((size_t)b * H + h0) * head, n = (size_t)nh * head;
+      cudaStream_t cs = hp.s[chunk & 1];
+      const uint8_t* hq = static_cast<const uint8_t*>(q) + off;
+      const uint8_t* hk = static_cast<const uint8_t*>(k) + off;
+      const uint8_t* hv = static_cast<const uint8_t*>(v) + off;
+      if ((e = cudaMemcpyAsync(dq + off, hq, n, cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(dk + off, hk, n, cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(dv + off, hv, n, cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+        break;
+      s = fwd_impl(dq + off, dk + off, dv + off, dout + off, f32, 1, nh, L, D, w, dilation + h0,
+                   gidx, n_g, scale, cs);
+      if (s != LF_OK) break;
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + off, dout + off, n,
+                          cudaMemcpyDeviceToHost, cs);
+    }
+  }
+  // join: the caller's stream waits for both pipeline streams, then frees
+  cudaError_t ej = cudaSuccess;
+  for (int x = 0; x < 2; ++x) {
+    if (ej == cudaSuccess) ej = cudaEventRecord(hp.join[x], hp.s[x]);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, hp.join[x], 0);
+  }
+  cudaFreeAsync(buf, st);
+  const cudaError_t e2 = cudaStreamSynchronize(st);
+  if (s != LF_OK) return s;
+  if (e != cudaSuccess) return fail(LF_ERR_CUDA, "copy failed: %s", cudaGetErrorString(e));
+  if (ej != cudaSuccess) return fail(LF_ERR_CUDA, "stream join: %s", cudaGetErrorString(ej));
+  if (e2 != cudaSuccess) return fail(LF_ERR_CUDA, "stream: %s", cudaGetErrorString(e2));
+  return LF_OK;
+}
+
 // =================================================================== C ABI
 
 extern "C" {
@@ -1660,33 +1754,8 @@ lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, void* ou
                            const int32_t* global_idx, int n_global, float scale,
                            lf_stream_t stream) {
   try {
-    t_last_error.clear();
-    if (!q || !k || !v || !out) return fail(LF_ERR_INVALID_ARG, "a host pointer is NULL");
-    if (B < 1 || H < 1 || L < 1 || (D != 64 && D != 128))
-      return fail(LF_ERR_INVALID_ARG, "bad shape B=%d H=%d L=%d D=%d", B, H, L, D);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t bytes = (size_t)B * H * L * D * (is_f32 ? 4 : 2);
-    uint8_t* buf = nullptr;
-    LF_CUDA(cudaMallocAsync(reinterpret_cast<void**>(&buf), 4 * align_up(bytes, 256), st));
-    uint8_t* dq = buf;
-    uint8_t* dk = dq + align_up(bytes, 256);
-    uint8_t* dv = dk + align_up(bytes, 256);
-    uint8_t* dout = dv + align_up(bytes, 256);
-    cudaError_t e = cudaSuccess;
-    lf_status s = LF_OK;
-    if ((e = cudaMemcpyAsync(dq, q, bytes, cudaMemcpyHostToDevice, st)) == cudaSuccess &&
-        (e = cudaMemcpyAsync(dk, k, bytes, cudaMemcpyHostToDevice, st)) == cudaSuccess &&
-        (e = cudaMemcpyAsync(dv, v, bytes, cudaMemcpyHostToDevice, st)) == cudaSuccess) {
-      s = fwd_impl(dq, dk, dv, dout, is_f32 != 0, B, H, L, D, w, dilation, global_idx, n_global,
-                   scale, st);
-      if (s == LF_OK) e = cudaMemcpyAsync(out, dout, bytes, cudaMemcpyDeviceToHost, st);
-    }
-    cudaFreeAsync(buf, st);
-    cudaError_t e2 = cudaStreamSynchronize(st);
-    if (s != LF_OK) return s;
-    if (e != cudaSuccess) return fail(LF_ERR_CUDA, "copy failed: %s", cudaGetErrorString(e));
-    if (e2 != cudaSuccess) return fail(LF_ERR_CUDA, "stream: %s", cudaGetErrorString(e2));
-    return LF_OK;
+    return fwd_host_impl(q, k, v, out, is_f32 != 0, B, H, L, D, w, dilation, global_idx,
+                         n_global, scale, static_cast<cudaStream_t>(stream));
   } catch (...) {
     return fail(LF_ERR_NOMEM, "host exception");
   }
