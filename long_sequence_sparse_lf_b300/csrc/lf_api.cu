@@ -29,6 +29,7 @@
 #include "lf_aux_kernels.cuh"
 #include "lf_common.cuh"
 #include "lf_bwd_kernels.cuh"
+#include "lf_bwd_tc_kernel.cuh"
 #include "lf_layer_kernels.cuh"
 
 namespace {
@@ -1333,8 +1334,11 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
 // Band tiles of the backward (bh, residue r, first key t0, dilation d), per
 // batch size and pattern; plus the backward's own scratch (delta).
 struct BwdPlan {
-  int4* d_tiles = nullptr;
-  int n_tiles = 0;
+  int4* d_tc_tiles = nullptr;   // 128-key band tiles of the tcgen05 kernel: (bh, r, t0, slot)
+  int n_tc_tiles = 0;
+  int n_slots = 0;
+  int slot_dil[lf::kMaxDilSlots] = {0};
+  int dmax = 1;
 };
 std::map<PlanKey, BwdPlan> g_bwd_plans;
 std::map<std::pair<int, cudaStream_t>, LayerWorkspace> g_bwd_ws;
@@ -1371,29 +1375,47 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_bwd_plans.find(key);
     if (it == g_bwd_plans.end()) {
-      std::vector<int4> tiles;
+      BwdPlan np;
+      std::vector<int> head_slot(H);
+      for (int h = 0; h < H; ++h) {
+        int sl = 0;
+        while (sl < np.n_slots && np.slot_dil[sl] != dilation[h]) ++sl;
+        if (sl == np.n_slots) {
+          if (np.n_slots == lf::kMaxDilSlots)
+            return fail(LF_ERR_UNSUPPORTED, "more than %d distinct dilation values",
+                        lf::kMaxDilSlots);
+          np.slot_dil[np.n_slots++] = dilation[h];
+        }
+        head_slot[h] = sl;
+        np.dmax = std::max(np.dmax, dilation[h]);
+      }
+      std::vector<int4> tc_tiles;
       for (int b = 0; b < B; ++b)
         for (int h = 0; h < H; ++h) {
           const int d = dilation[h];
           for (int r = 0; r < d; ++r) {
             const int Lr = lf::residue_len(L, d, r);
-            for (int t0 = 0; t0 < Lr; t0 += lf::kBwdB) tiles.push_back(make_int4(b * H + h, r, t0, d));
+            for (int t0 = 0; t0 < Lr; t0 += lf::kBtcKeys)
+              tc_tiles.push_back(make_int4(b * H + h, r, t0, head_slot[h]));
           }
         }
-      BwdPlan np;
-      np.n_tiles = (int)tiles.size();
-      LF_CUDA(cudaMalloc(&np.d_tiles, sizeof(int4) * std::max<size_t>(tiles.size(), 1)));
-      LF_CUDA(cudaMemcpy(np.d_tiles, tiles.data(), sizeof(int4) * tiles.size(), cudaMemcpyHostToDevice));
+      np.n_tc_tiles = (int)tc_tiles.size();
+      LF_CUDA(cudaMalloc(&np.d_tc_tiles, sizeof(int4) * std::max<size_t>(tc_tiles.size(), 1)));
+      LF_CUDA(cudaMemcpy(np.d_tc_tiles, tc_tiles.data(), sizeof(int4) * tc_tiles.size(),
+                         cudaMemcpyHostToDevice));
       it = g_bwd_plans.emplace(key, np).first;
     }
     bp = &it->second;
   }
   const long long rows = (long long)B * H * L;
+  // workspace: delta [rows] | band statistics [B*H][stats_bh] float4
+  const long long stats_bh = (long long)L + (long long)lf::kBtcQ * bp->dmax;
+  const size_t off_stats = align_up((size_t)rows * 4, 256);
   uint8_t* ws = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     LayerWorkspace& wsp = g_bwd_ws[{dev, stream}];
-    const size_t need = align_up((size_t)rows * 4, 256);
+    const size_t need = off_stats + align_up((size_t)B * H * stats_bh * 16, 256);
     if (wsp.bytes < need) {
       if (wsp.ptr) LF_CUDA(cudaFreeAsync(wsp.ptr, stream));
       wsp.ptr = nullptr;
@@ -1404,10 +1426,35 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     ws = wsp.ptr;
   }
   float* delta = reinterpret_cast<float*>(ws);
+  float4* stats = reinterpret_cast<float4*>(ws + off_stats);
   const size_t grad_bytes = (size_t)rows * D * 4;
+  // dq is accumulated by every class; dk and dv are stored by the band
+  // kernel (every key row has one band tile) before the global classes add
   LF_CUDA(cudaMemsetAsync(dq, 0, grad_bytes, stream));
-  LF_CUDA(cudaMemsetAsync(dk, 0, grad_bytes, stream));
-  LF_CUDA(cudaMemsetAsync(dv, 0, grad_bytes, stream));
+
+  // parameters of the tcgen05 band kernel: residue views of k, v, q, dout
+  lf::BwdTcParams T;
+  std::memset(&T, 0, sizeof(T));
+  for (int sl = 0; sl < bp->n_slots; ++sl) {
+    const int d = bp->slot_dil[sl];
+    T.dil[sl] = d;
+    if ((s = map_residue(ds, &T.tmK[sl], k, D, L, d, B * H)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmV[sl], v, D, L, d, B * H)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmQ[sl], q, D, L, d, B * H)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmO[sl], dout, D, L, d, B * H)) != LF_OK) return s;
+  }
+  T.tiles = bp->d_tc_tiles;
+  T.stats = stats;
+  T.stats_bh = stats_bh;
+  T.dq = dq;
+  T.dk = dk;
+  T.dv = dv;
+  T.L = L;
+  T.w = w;
+  T.scale = scale;
+  T.sl2 = scale * 1.4426950408889634f;
+  T.status = ds->status;
+  T.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
   lf::BwdParams P;
   P.q = static_cast<const __nv_bfloat16*>(q);
@@ -1421,8 +1468,6 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   P.dv = dv;
   P.gidx = pat->d_G;
   P.is_glob = pat->d_isg;
-  P.tiles = bp->d_tiles;
-  P.n_tiles = bp->n_tiles;
   P.head_dil = pat->d_dil;
   P.H = H;
   P.L = L;
@@ -1442,9 +1487,11 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
       std::lock_guard<std::mutex> lk(g_mu);
       const int slot = dev * 2 + (DD == 128 ? 1 : 0);
       if (slot < 64 && !g_bwd_smem_set[slot]) {
-        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_band_tc_kernel<DD>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)lf::BtcCfg<DD>::SMEM_BYTES));
         g_bwd_smem_set[slot] = true;
       }
     }
@@ -1452,9 +1499,20 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
       lf::lf_bwd_delta_kernel<DD><<<dblocks, dthreads, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(out), P.dout, delta, rows);
     });
-    if (P.n_tiles > 0)
+    {
+      const long long total = (long long)B * H * stats_bh;
+      const int sthreads = 256;
+      const unsigned sblocks = (unsigned)std::min<long long>((total + sthreads - 1) / sthreads,
+                                                             (long long)ds->num_sms * 16);
+      traced("bwd_stats", stream, [&] {
+        lf::lf_bwd_tc_stats_kernel<<<sblocks, sthreads, 0, stream>>>(
+            lse, delta, pat->d_isg, pat->d_dil, H, L, stats_bh, total, stats);
+      });
+    }
+    if (bp->n_tc_tiles > 0)
       traced("bwd_band", stream, [&] {
-        lf::lf_bwd_kernel<DD, 0><<<(unsigned)P.n_tiles, lf::kBwdThreads, smem, stream>>>(P);
+        lf::lf_bwd_band_tc_kernel<DD><<<(unsigned)bp->n_tc_tiles, lf::BtcCfg<DD>::THREADS,
+                                        lf::BtcCfg<DD>::SMEM_BYTES, stream>>>(T);
       });
     if (gunits > 0) {
       if (gunits > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "too many global tiles");
@@ -1841,7 +1899,7 @@ void lf_plan_cache_clear(void) {
   for (auto& kv : g_bias_ws)
     if (kv.second.ptr) cudaFree(kv.second.ptr);
   g_bias_ws.clear();
-  for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tiles);
+  for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tc_tiles);
   g_bwd_plans.clear();
   for (auto& kv : g_gemms) {
     cublasLtMatmulDescDestroy(kv.second.op);

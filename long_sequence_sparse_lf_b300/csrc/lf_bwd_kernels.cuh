@@ -9,15 +9,13 @@
 // (The pages give only the forward; this is the derivative of its plain
 // definition: "Longformer explained" §2, §4.)
 //
-// The attended pairs split into three classes, each a kernel over 64 x 64
-// blocks of (query rows, key rows):
-//   band        i not global, j in band(i): per 64-key tile of one residue
-//               class (the band is symmetric, so the queries are those of
-//               the key's own window), over the query blocks it reaches;
+// The attended pairs split into three classes:
+//   band        i not global, j in band(i): the tcgen05 kernel of
+//               lf_bwd_tc_kernel.cuh;
 //   global keys j global, i not global, j not in band(i): per 64 gathered
-//               global keys, over every query block;
+//               global keys, over every query block (this file);
 //   global rows i global, every j: per 64 gathered global rows, over every
-//               key block.
+//               key block (this file).
 // The two global classes split their streamed side into chunks of kBwdChunk
 // blocks, one CTA each, so that a few global tokens still fill the GPU.
 // Each block pair computes S = Q K^T and dP = dO V^T with WMMA (bf16 in, fp32
@@ -52,8 +50,6 @@ struct BwdParams {
   float* dv;
   const int32_t* gidx;           // [n_g] sorted global positions
   const uint8_t* is_glob;        // [L]
-  const int4* tiles;             // band tiles: (bh, residue r, first key t0, dilation d)
-  int n_tiles;
   const int32_t* head_dil;       // [H]
   int H, L, w, n_g;
   float scale;
@@ -212,51 +208,31 @@ __device__ __forceinline__ void bwd_add_rows(float* X, const float* acc, float s
   }
 }
 
-// kind 0: band tile; 1: global keys; 2: global rows.  One CTA per unit (two
-// per SM for D = 64, whose shared memory allows it).
+// KIND 1: global keys; 2: global rows.  One CTA per unit (two per SM for
+// D = 64, whose shared memory allows it).
 template <int D, int KIND>
 __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1) lf_bwd_kernel(const BwdParams p) {
   extern __shared__ __align__(128) uint8_t bwd_smem_raw[];
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(bwd_smem_raw);
   using LD = BwdLd<D>;
   const float log2e = 1.4426950408889634f;
-  size_t bh;
-  int d = 1, r = 0, Lr = p.L;
-  int n_blocks;                  // blocks of the streamed side
-  int blk0 = 0;                  // first of them (global classes: this CTA's chunk)
-  int fixed0 = 0;                // first fixed row (residue space / gathered index)
-  if (KIND == 0) {
-    const int4 t = p.tiles[blockIdx.x];
-    bh = (size_t)t.x;
-    r = t.y;
-    fixed0 = t.z;
-    d = t.w;
-    Lr = (p.L - 1 - r) / d + 1;
-    const int s_lo = max(fixed0 - p.w, 0), s_hi = min(fixed0 + kBwdB - 1 + p.w, Lr - 1);
-    n_blocks = (s_hi - s_lo) / kBwdB + 1;
-  } else {
-    const int n_gt = (p.n_g + kBwdB - 1) / kBwdB;
-    const int all_blocks = (p.L + kBwdB - 1) / kBwdB;
-    const int n_sc = (all_blocks + kBwdChunk - 1) / kBwdChunk;
-    const int sc = (int)(blockIdx.x % n_sc);
-    const size_t unit = blockIdx.x / n_sc;
-    bh = unit / n_gt;
-    fixed0 = (int)(unit % n_gt) * kBwdB;
-    d = p.head_dil[bh % p.H];
-    blk0 = sc * kBwdChunk;
-    n_blocks = min(all_blocks, blk0 + kBwdChunk);
-  }
-  // the fixed side: keys (band, global keys) or queries (global rows)
+  static_assert(KIND == 1 || KIND == 2, "global classes only");
+  // the unit: gathered global rows fixed0 .. +63 of head bh against the
+  // streamed blocks blk0 .. n_blocks-1 (this CTA's chunk)
+  const int n_gt = (p.n_g + kBwdB - 1) / kBwdB;
+  const int all_blocks = (p.L + kBwdB - 1) / kBwdB;
+  const int n_sc = (all_blocks + kBwdChunk - 1) / kBwdChunk;
+  const int sc = (int)(blockIdx.x % n_sc);
+  const size_t unit = blockIdx.x / n_sc;
+  const size_t bh = unit / n_gt;
+  const int fixed0 = (int)(unit % n_gt) * kBwdB;
+  const int d = p.head_dil[bh % p.H];
+  const int blk0 = sc * kBwdChunk;
+  const int n_blocks = min(all_blocks, blk0 + kBwdChunk);
+  // the fixed side: keys (global keys) or queries (global rows)
   int* fixed_pos = (KIND == 2) ? sm.qpos : sm.kpos;
-  for (int c = threadIdx.x; c < kBwdB; c += blockDim.x) {
-    int pos = -1;
-    if (KIND == 0) {
-      if (fixed0 + c < Lr) pos = r + d * (fixed0 + c);
-    } else if (fixed0 + c < p.n_g) {
-      pos = p.gidx[fixed0 + c];
-    }
-    fixed_pos[c] = pos;
-  }
+  for (int c = threadIdx.x; c < kBwdB; c += blockDim.x)
+    fixed_pos[c] = fixed0 + c < p.n_g ? p.gidx[fixed0 + c] : -1;
   // the fixed rows' sums over the streamed blocks: dV, dK of the keys, or
   // dQ of the global rows (fix0 only)
   BwdFragAcc<D> fix0, fix1;
@@ -275,7 +251,6 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1) lf_bwd_kernel(co
     bwd_load_rows<D>(sm.k, p.k, bh, p.L, sm.kpos);
     bwd_load_rows<D>(sm.v, p.v, bh, p.L, sm.kpos);
   }
-  const int s_lo = (KIND == 0) ? max(fixed0 - p.w, 0) : 0;
   const float sl2 = p.scale * log2e;
 
   for (int blk = blk0; blk < n_blocks; ++blk) {
@@ -283,15 +258,8 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1) lf_bwd_kernel(co
     // the streamed side's rows
     int* str_pos = (KIND == 2) ? sm.kpos : sm.qpos;
     for (int c = threadIdx.x; c < kBwdB; c += blockDim.x) {
-      int pos = -1;
-      if (KIND == 0) {
-        const int s = s_lo + blk * kBwdB + c;
-        if (s < Lr) pos = r + d * s;
-      } else {
-        const int i = blk * kBwdB + c;
-        if (i < p.L) pos = i;
-      }
-      str_pos[c] = pos;
+      const int i = blk * kBwdB + c;
+      str_pos[c] = i < p.L ? i : -1;
     }
     __syncthreads();
     if (KIND == 2) {
@@ -317,11 +285,7 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1) lf_bwd_kernel(co
       const int i = sm.qpos[a], j = sm.kpos[b];
       bool ok = i >= 0 && j >= 0;
       if (ok) {
-        if (KIND == 0) {
-          // same residue class by construction; the window in residue space
-          const int ts = (i - r) / d, tk = (j - r) / d;
-          ok = abs(ts - tk) <= p.w && sm.qglob[a] == 0;
-        } else if (KIND == 1) {
+        if (KIND == 1) {
           const int diff = i - j;
           const bool in_band = abs(diff) <= d * p.w && diff % d == 0;
           ok = sm.qglob[a] == 0 && !in_band;

@@ -200,6 +200,31 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16, bf16 x bf16 -> fp32, with the major-ness
+// of both operands given (bit 15: A MN-major, i.e. its M dimension is the
+// contiguous one in shared memory).
+__host__ __device__ constexpr uint32_t idesc_bf16_ab(int M, int N, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
+// One-dimensional bulk copy global -> shared memory, completing on an
+// mbarrier's transaction count (both addresses 16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (the tensor core reading an operand this thread wrote).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- TMEM <-> registers (32 lanes x 32-bit, one lane per thread of the warp)
 
 #define LF_R8(b) "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), \
