@@ -614,10 +614,10 @@ lf_status encode(DevState* ds, CUtensorMap* m, const void* base, int rank, const
 
 // 4-D residue view {D, d, L/d, BH} of a [BH, L, D] bf16 tensor
 lf_status map_residue(DevState* ds, CUtensorMap* m, const void* base, int D, int L, int d,
-                      int BH) {
+                      int BH, uint32_t box_rows = 128) {
   const uint64_t dims[4] = {(uint64_t)D, (uint64_t)d, (uint64_t)(L / d), (uint64_t)BH};
   const uint64_t st[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * d, (uint64_t)D * 2 * L};
-  const uint32_t box[4] = {64, 1, 128, 1};
+  const uint32_t box[4] = {64, 1, box_rows, 1};
   return encode(ds, m, base, 4, dims, st, box);
 }
 
@@ -1409,7 +1409,7 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   }
   const long long rows = (long long)B * H * L;
   // workspace: delta [rows] | band statistics [B*H][stats_bh] float4
-  const long long stats_bh = (long long)L + (long long)lf::kBtcQ * bp->dmax;
+  const long long stats_bh = (long long)L + (long long)lf::kBtcQPad * bp->dmax;
   const size_t off_stats = align_up((size_t)rows * 4, 256);
   uint8_t* ws = nullptr;
   {
@@ -1440,8 +1440,9 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     T.dil[sl] = d;
     if ((s = map_residue(ds, &T.tmK[sl], k, D, L, d, B * H)) != LF_OK) return s;
     if ((s = map_residue(ds, &T.tmV[sl], v, D, L, d, B * H)) != LF_OK) return s;
-    if ((s = map_residue(ds, &T.tmQ[sl], q, D, L, d, B * H)) != LF_OK) return s;
-    if ((s = map_residue(ds, &T.tmO[sl], dout, D, L, d, B * H)) != LF_OK) return s;
+    const uint32_t qb = D == 64 ? lf::BtcCfg<64>::QB : lf::BtcCfg<128>::QB;
+    if ((s = map_residue(ds, &T.tmQ[sl], q, D, L, d, B * H, qb)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmO[sl], dout, D, L, d, B * H, qb)) != LF_OK) return s;
   }
   T.tiles = bp->d_tc_tiles;
   T.stats = stats;

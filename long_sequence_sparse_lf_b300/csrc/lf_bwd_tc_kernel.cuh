@@ -6,9 +6,10 @@
 // backward.  band(i) is symmetric in residue space (t_j - t_i in [-w, w]
 // within one residue class), so one CTA owns a tile of 128 keys of one
 // residue class of one head, keeps K and V in shared memory, and walks the
-// 128-query blocks its keys' windows reach.  Per query block, with keys on
-// the TMEM lanes:
-//   S^T  = K Q^T            (M = 128 keys, N = 128 queries, K = D)
+// query blocks its keys' windows reach (64 queries at D = 64, where two
+// CTAs share an SM; 128 at D = 128).  Per query block, with keys on the
+// TMEM lanes:
+//   S^T  = K Q^T            (M = 128 keys, N = block queries, K = D)
 //   dP^T = V dO^T
 //   P^T  = 2^(S^T scale log2e - lse log2e), masked    (softmax warps, fp32)
 //   dS^T = P^T (dP^T - delta)
@@ -22,10 +23,12 @@
 // and added to dq with atomics (several key tiles reach each query).
 //
 // P^T (bf16) is written over the first half of S^T's columns after the
-// whole block of S^T has been read, dS^T over the first half of dP^T's;
-// the two 64-query halves of dQ^T land in the second halves of S^T and dP^T
-// (read by then).  At D = 64 the M = 128 product K^T dS^T reads a zero tile
-// as the missing 64 rows of K^T.
+// whole block of S^T has been read, dS^T over the first half of dP^T's
+// (adjacent to S^T).  dQ^T lands in the columns from S^T's second half on:
+// S^T's second half has been read, and the tensor pipe runs this thread's
+// products in order, so the dV and dK products have read P^T and dS^T
+// before dQ^T overwrites dS^T.  At D = 64 the M = 128 product K^T dS^T
+// reads a zero tile as the missing 64 rows of K^T.
 //
 // Query rows that are global tokens (their gradients come from the
 // global-row class) and padding rows past the residue class's end carry
@@ -45,7 +48,7 @@
 namespace lf {
 
 constexpr int kBtcKeys = 128;   // keys per tile (TMEM lanes)
-constexpr int kBtcQ = 128;      // queries per block
+constexpr int kBtcQPad = 128;   // padding of each residue class of the statistics
 
 struct BwdTcParams {
   CUtensorMap tmK[kMaxDilSlots];   // 4-D residue views {D, d, L/d, B*H}, box {64, 1, 128, 1}
@@ -67,32 +70,38 @@ struct BwdTcParams {
 
 // Entries of one residue class of the statistics (Lr + a block of padding,
 // so that a block starting anywhere in the class stays inside it).
-__host__ __device__ __forceinline__ int btc_class_len(int L, int d) { return L / d + kBtcQ; }
+__host__ __device__ __forceinline__ int btc_class_len(int L, int d) { return L / d + kBtcQPad; }
 
 template <int D>
 struct BtcCfg {
+  static constexpr int QB = (D == 64) ? 64 : 128;         // queries per block
+  static constexpr int CTAS = (D == 64) ? 2 : 1;          // CTAs per SM
   static constexpr int NH = D / 64;
   static constexpr uint32_t HALF = 128u * 128u;           // [128 rows][64] bf16, SW128
+  static constexpr uint32_t QHALF = QB * 128u;            // [QB rows][64] bf16
   static constexpr uint32_t TILE = NH * HALF;             // a [128 x D] bf16 tile
+  static constexpr uint32_t QTILE = NH * QHALF;           // a [QB x D] bf16 tile
   static constexpr int NQB = (D == 64) ? 2 : 1;           // Q / dO / stats buffers
   static constexpr uint32_t OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;
-  static constexpr uint32_t OFF_O = OFF_Q + NQB * TILE;
-  static constexpr uint32_t OFF_DS = OFF_O + NQB * TILE;  // dS^T [128 keys][128 queries] bf16
-  static constexpr uint32_t OFF_Z = OFF_DS + 2 * HALF;    // zero tile (D = 64)
-  static constexpr uint32_t OFF_ST = OFF_Z + (D == 64 ? HALF : 0);   // stats [NQB][128] float4
-  static constexpr uint32_t OFF_BAR = OFF_ST + NQB * kBtcQ * 16;
+  static constexpr uint32_t OFF_O = OFF_Q + NQB * QTILE;
+  static constexpr uint32_t OFF_DS = OFF_O + NQB * QTILE; // dS^T [128 keys][QB queries] bf16
+  static constexpr uint32_t OFF_Z = OFF_DS + (QB / 64) * HALF;   // zero tile (D = 64)
+  static constexpr uint32_t OFF_ST = OFF_Z + (D == 64 ? HALF : 0);   // stats [NQB][QB] float4
+  static constexpr uint32_t OFF_BAR = OFF_ST + NQB * QB * 16;
   // barriers
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQB, B_SP = B_QE + NQB, B_PD = B_SP + 1,
                        B_DQ = B_PD + 1, B_DF = B_DQ + 1, B_DR = B_DF + 1, NBAR = B_DR + 1;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
   // TMEM columns
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
-  static constexpr uint32_t TM_COLS = 512;
+  static constexpr uint32_t TM_S = 0, TM_DP = QB, TM_DV = 2 * QB, TM_DK = 2 * QB + D;
+  static constexpr uint32_t TM_DQ = QB / 2;               // dQ^T: QB columns from here
+  static constexpr uint32_t TM_COLS = (D == 64) ? 256 : 512;
   static constexpr int THREADS = 192;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_constant__ BwdTcParams p) {
+__global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
+    lf_bwd_band_tc_kernel(const __grid_constant__ BwdTcParams p) {
   using C = BtcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -112,7 +121,7 @@ __global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_con
   // the query blocks: the keys' windows [t0 - w, t0 + 127 + w], clipped
   const int qs0 = max(t0 - p.w, 0);
   const int qend = min(t0 + kBtcKeys - 1 + p.w, Lr - 1);
-  const int nqb = (qend - qs0) / kBtcQ + 1;
+  const int nqb = (qend - qs0) / C::QB + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_KV), 1);
@@ -161,16 +170,16 @@ __global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_con
         const int b = j % C::NQB;
         const uint32_t u = j / C::NQB;
         if (u > 0 && !bwait(BAR(C::B_QE + b), (u - 1) & 1, W)) { ok = false; break; }
-        const int qs = qs0 + kBtcQ * j;
-        mbar_arrive_expect_tx(BAR(C::B_QF + b), 2u * C::TILE + kBtcQ * 16u);
+        const int qs = qs0 + C::QB * j;
+        mbar_arrive_expect_tx(BAR(C::B_QF + b), 2u * C::QTILE + C::QB * 16u);
 #pragma unroll
         for (int hh = 0; hh < C::NH; ++hh) {
-          tma_load_4d(sb + C::OFF_Q + b * C::TILE + hh * C::HALF, &p.tmQ[slot], BAR(C::B_QF + b),
-                      64 * hh, r, qs, bh);
-          tma_load_4d(sb + C::OFF_O + b * C::TILE + hh * C::HALF, &p.tmO[slot], BAR(C::B_QF + b),
-                      64 * hh, r, qs, bh);
+          tma_load_4d(sb + C::OFF_Q + b * C::QTILE + hh * C::QHALF, &p.tmQ[slot],
+                      BAR(C::B_QF + b), 64 * hh, r, qs, bh);
+          tma_load_4d(sb + C::OFF_O + b * C::QTILE + hh * C::QHALF, &p.tmO[slot],
+                      BAR(C::B_QF + b), 64 * hh, r, qs, bh);
         }
-        bulk_load(sb + C::OFF_ST + b * kBtcQ * 16, st_src + qs, kBtcQ * 16u, BAR(C::B_QF + b));
+        bulk_load(sb + C::OFF_ST + b * C::QB * 16, st_src + qs, C::QB * 16u, BAR(C::B_QF + b));
         ++armed;
       }
       // drain: every armed load completes before the CTA exits
@@ -181,9 +190,9 @@ __global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_con
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_ab(128, 128, false, false);
+      const uint32_t id_s = idesc_bf16_ab(128, C::QB, false, false);
       const uint32_t id_g = idesc_bf16_ab(128, D, false, true);     // dV, dK
-      const uint32_t id_q = idesc_bf16_ab(128, 64, true, true);     // dQ^T halves
+      const uint32_t id_q = idesc_bf16_ab(128, C::QB, true, true);  // dQ^T
       const uint32_t tS = tmem + C::TM_S, tP = tmem + C::TM_DP;
       const uint32_t tV = tmem + C::TM_DV, tK = tmem + C::TM_DK;
       // K^T as an M-major A operand: 64-row groups of M (= D) lie C::HALF
@@ -198,42 +207,37 @@ __global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_con
         // the previous block's dQ^T has been read out
         if (j > 0 && !bwait(BAR(C::B_DF), (j - 1) & 1, W)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t qa = sb + C::OFF_Q + b * C::TILE, oa = sb + C::OFF_O + b * C::TILE;
+        const uint32_t qa = sb + C::OFF_Q + b * C::QTILE, oa = sb + C::OFF_O + b * C::QTILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32u;
-          mma_ss(tS, sdesc_sw128(sb + C::OFF_K + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                 id_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk & 3) * 32u;
+          mma_ss(tS, sdesc_sw128(sb + C::OFF_K + (kk >> 2) * C::HALF + off, 16, 1024),
+                 sdesc_sw128(qa + (kk >> 2) * C::QHALF + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32u;
-          mma_ss(tP, sdesc_sw128(sb + C::OFF_V + off, 16, 1024), sdesc_sw128(oa + off, 16, 1024),
-                 id_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk & 3) * 32u;
+          mma_ss(tP, sdesc_sw128(sb + C::OFF_V + (kk >> 2) * C::HALF + off, 16, 1024),
+                 sdesc_sw128(oa + (kk >> 2) * C::QHALF + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(BAR(C::B_SP));
         if (!bwait(BAR(C::B_PD), j & 1, W)) { ok = false; break; }
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q  (K = 128 queries in 8 steps)
+        // dV += P^T dO, dK += dS^T Q  (K = QB queries in steps of 16)
 #pragma unroll
-        for (int kk = 0; kk < kBtcQ / 16; ++kk)
-          mma_ts(tV, tS + kk * 8, sdesc_sw128(oa + kk * 2048u, C::HALF, 1024), id_g,
+        for (int kk = 0; kk < C::QB / 16; ++kk)
+          mma_ts(tV, tS + kk * 8, sdesc_sw128(oa + kk * 2048u, C::QHALF, 1024), id_g,
                  (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBtcQ / 16; ++kk)
-          mma_ts(tK, tP + kk * 8, sdesc_sw128(qa + kk * 2048u, C::HALF, 1024), id_g,
+        for (int kk = 0; kk < C::QB / 16; ++kk)
+          mma_ts(tK, tP + kk * 8, sdesc_sw128(qa + kk * 2048u, C::QHALF, 1024), id_g,
                  (j > 0 || kk > 0) ? 1u : 0u);
-        // dQ^T = K^T dS^T, queries 0..63 into S^T's second half, 64..127
-        // into dP^T's (K = 128 keys in 8 steps)
+        // dQ^T = K^T dS^T into the QB columns from S^T's second half on
+        // (K = 128 keys in 8 steps)
 #pragma unroll
         for (int kk = 0; kk < kBtcKeys / 16; ++kk)
-          mma_ss(tS + 64, sdesc_sw128(sb + C::OFF_K + kk * 2048u, lbo_kt, 1024),
+          mma_ss(tmem + C::TM_DQ, sdesc_sw128(sb + C::OFF_K + kk * 2048u, lbo_kt, 1024),
                  sdesc_sw128(sb + C::OFF_DS + kk * 2048u, C::HALF, 1024), id_q, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kBtcKeys / 16; ++kk)
-          mma_ss(tP + 64, sdesc_sw128(sb + C::OFF_K + kk * 2048u, lbo_kt, 1024),
-                 sdesc_sw128(sb + C::OFF_DS + C::HALF + kk * 2048u, C::HALF, 1024), id_q,
-                 kk > 0 ? 1u : 0u);
         mma_commit(BAR(C::B_DQ));
         mma_commit(BAR(C::B_QE + b));
       }
@@ -255,24 +259,24 @@ __global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_con
     for (int j = 0; j < nqb && ok; ++j) {
       const int b = j % C::NQB;
       const uint32_t u = j / C::NQB;
-      const int qs = qs0 + kBtcQ * j;
+      const int qs = qs0 + C::QB * j;
       ok = bwait(BAR(C::B_QF + b), u & 1, W) && bwait(BAR(C::B_SP), j & 1, W);
       if (!__all_sync(FULL, ok)) { ok = false; break; }
       tc_fence_after();
-      const float4* st = stats_s + b * kBtcQ;
+      const float4* st = stats_s + b * C::QB;
       // the block's query rows that have band gradients (not a global token,
       // inside the class): bit c of qv[c >> 5].  Kept in registers: the
       // statistics buffer is refilled once this block's products are done,
       // before its dQ has been read out.
-      uint32_t qv[4];
+      uint32_t qv[C::QB / 32];
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < C::QB / 32; ++x)
         qv[x] = __ballot_sync(FULL, st[32 * x + lane].x != __int_as_float(0x7f800000) &&
                                         qs + 32 * x + lane < Lr);
       // this key's queries: t_q in [tk - w, tk + w], as block columns
       const int clo = kvalid ? tk - p.w - qs : 1, chi = kvalid ? tk + p.w - qs : 0;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 0; c4 < C::QB / 32; ++c4) {
         uint32_t sr[32], pr[32];
         tmem_ld32(tl + C::TM_S + 32 * c4, sr);
         tmem_ld32(tl + C::TM_DP + 32 * c4, pr);
@@ -318,21 +322,18 @@ __global__ void __launch_bounds__(192, 1) lf_bwd_band_tc_kernel(const __grid_con
       if (warp * 32 < D) {
         const int dcol = row;   // lane = row of dQ^T = element of D
 #pragma unroll 1
-        for (int hq = 0; hq < 2; ++hq) {
-#pragma unroll 1
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t qr[32];
-            tmem_ld32(tl + (hq ? C::TM_DP : C::TM_S) + 64 + 32 * c2, qr);
+        for (int c2 = 0; c2 < C::QB / 32; ++c2) {
+          uint32_t qr[32];
+          tmem_ld32(tl + C::TM_DQ + 32 * c2, qr);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int col = 64 * hq + 32 * c2 + e;
-              // global query rows and padding rows: no contribution (and
-              // no valid position)
-              if ((qv[col >> 5] >> (col & 31)) & 1u) {
-                const size_t i = static_cast<size_t>(r) + static_cast<size_t>(d) * (qs + col);
-                atomicAdd(p.dq + (static_cast<size_t>(bh) * p.L + i) * D + dcol,
-                          p.scale * __uint_as_float(qr[e]));
-              }
+          for (int e = 0; e < 32; ++e) {
+            const int col = 32 * c2 + e;
+            // global query rows and padding rows: no contribution (and no
+            // valid position)
+            if ((qv[col >> 5] >> (col & 31)) & 1u) {
+              const size_t i = static_cast<size_t>(r) + static_cast<size_t>(d) * (qs + col);
+              atomicAdd(p.dq + (static_cast<size_t>(bh) * p.L + i) * D + dcol,
+                        p.scale * __uint_as_float(qr[e]));
             }
           }
         }
