@@ -28,7 +28,6 @@
 #include "lf_attn_kernel.cuh"
 #include "lf_aux_kernels.cuh"
 #include "lf_common.cuh"
-#include "lf_bwd_kernels.cuh"
 #include "lf_bwd_tc_kernel.cuh"
 #include "lf_layer_kernels.cuh"
 
@@ -1333,9 +1332,12 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
 
 // Band tiles of the backward (bh, residue r, first key t0, dilation d), per
 // batch size and pattern; plus the backward's own scratch (delta).
+// Tiles of the backward kernel (per batch size, pattern and D): band tiles
+// of 128 keys per residue class, then the global-key tiles (launched second,
+// after the band tiles have stored dK and dV).
 struct BwdPlan {
-  int4* d_tc_tiles = nullptr;   // 128-key band tiles of the tcgen05 kernel: (bh, r, t0, slot)
-  int n_tc_tiles = 0;
+  lf::BtcTile* d_tiles = nullptr;
+  int n_band = 0, n_gkey = 0;
   int n_slots = 0;
   int slot_dil[lf::kMaxDilSlots] = {0};
   int dmax = 1;
@@ -1343,6 +1345,11 @@ struct BwdPlan {
 std::map<PlanKey, BwdPlan> g_bwd_plans;
 std::map<std::pair<int, cudaStream_t>, LayerWorkspace> g_bwd_ws;
 bool g_bwd_smem_set[64] = {false};
+
+// query blocks per global-key tile: the head's rows are split into chunks of
+// kBwdGkeyMinBlocks .. kBwdGkeyBlocks blocks, so that a few global keys still
+// spread over the GPU
+constexpr int kBwdGkeyBlocks = 8, kBwdGkeyMinBlocks = 2;
 
 lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
                    const void* dout, float* dq, float* dk, float* dv, int B, int H, int L, int D,
@@ -1368,6 +1375,8 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
   std::shared_ptr<Pattern> pat;
   if ((s = get_pattern(dev, H, L, w, dilation, gidx, n_g, &pat)) != LF_OK) return s;
+  const int QB = D == 64 ? lf::BtcCfg<64>::QB : lf::BtcCfg<128>::QB;
+  const int NGQ = n_g > 0 ? ceil_div(n_g, lf::kBtcKeys) * lf::kBtcKeys : 0;
   BwdPlan* bp = nullptr;
   {
     PatKey pk{dev, H, L, w, pat->dil, pat->G, pat->xkey};
@@ -1389,33 +1398,54 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
         head_slot[h] = sl;
         np.dmax = std::max(np.dmax, dilation[h]);
       }
-      std::vector<int4> tc_tiles;
+      std::vector<lf::BtcTile> tiles;
       for (int b = 0; b < B; ++b)
         for (int h = 0; h < H; ++h) {
           const int d = dilation[h];
           for (int r = 0; r < d; ++r) {
             const int Lr = lf::residue_len(L, d, r);
             for (int t0 = 0; t0 < Lr; t0 += lf::kBtcKeys)
-              tc_tiles.push_back(make_int4(b * H + h, r, t0, head_slot[h]));
+              tiles.push_back(lf::BtcTile{b * H + h, 0, r, t0, head_slot[h], 0, 0, 0});
           }
         }
-      np.n_tc_tiles = (int)tc_tiles.size();
-      LF_CUDA(cudaMalloc(&np.d_tc_tiles, sizeof(int4) * std::max<size_t>(tc_tiles.size(), 1)));
-      LF_CUDA(cudaMemcpy(np.d_tc_tiles, tc_tiles.data(), sizeof(int4) * tc_tiles.size(),
+      np.n_band = (int)tiles.size();
+      // global-key tiles: query chunks short enough for a few waves of
+      // resident CTAs (2 per SM at D = 64, 1 at D = 128)
+      const int all_blocks = ceil_div(L, QB);
+      const long long units = (long long)B * H * ceil_div(std::max(n_g, 1), lf::kBtcKeys) * all_blocks;
+      const long long slots = (long long)ds->num_sms * (D == 64 ? 2 : 1);
+      const int chunk = (int)std::max<long long>(
+          kBwdGkeyMinBlocks, std::min<long long>(kBwdGkeyBlocks, units / (4 * slots)));
+      for (int b = 0; b < B && n_g > 0; ++b)
+        for (int h = 0; h < H; ++h)
+          for (int g0 = 0; g0 < n_g; g0 += lf::kBtcKeys)
+            for (int c = 0; c < all_blocks; c += chunk)
+              tiles.push_back(lf::BtcTile{b * H + h, 1, 0, g0, head_slot[h], c * QB,
+                                          std::min(chunk, all_blocks - c), 0});
+      np.n_gkey = (int)tiles.size() - np.n_band;
+      LF_CUDA(cudaMalloc(&np.d_tiles, sizeof(lf::BtcTile) * std::max<size_t>(tiles.size(), 1)));
+      LF_CUDA(cudaMemcpy(np.d_tiles, tiles.data(), sizeof(lf::BtcTile) * tiles.size(),
                          cudaMemcpyHostToDevice));
       it = g_bwd_plans.emplace(key, np).first;
     }
     bp = &it->second;
   }
-  const long long rows = (long long)B * H * L;
-  // workspace: delta [rows] | band statistics [B*H][stats_bh] float4
+  const int BH = B * H;
+  const long long rows = (long long)BH * L;
+  // workspace: statistics (residue order [BH][stats_bh], gathered global
+  // rows [BH][NGQ], natural order [BH][L + pad]) | gathered q, dout, k, v
+  // [BH][NGQ][D]
   const long long stats_bh = (long long)L + (long long)lf::kBtcQPad * bp->dmax;
-  const size_t off_stats = align_up((size_t)rows * 4, 256);
+  const size_t off_stats = 0;
+  const size_t off_sg = off_stats + align_up((size_t)BH * stats_bh * 16, 256);
+  const size_t off_sn = off_sg + align_up((size_t)BH * NGQ * 16 + 16, 256);
+  const size_t off_g = off_sn + align_up((size_t)BH * (L + lf::kBtcQPad) * 16, 256);
+  const size_t g_elems = (size_t)BH * NGQ * D;
+  const size_t need = off_g + align_up(4 * g_elems * 2 + 16, 256);
   uint8_t* ws = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     LayerWorkspace& wsp = g_bwd_ws[{dev, stream}];
-    const size_t need = off_stats + align_up((size_t)B * H * stats_bh * 16, 256);
     if (wsp.bytes < need) {
       if (wsp.ptr) LF_CUDA(cudaFreeAsync(wsp.ptr, stream));
       wsp.ptr = nullptr;
@@ -1425,28 +1455,46 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     }
     ws = wsp.ptr;
   }
-  float* delta = reinterpret_cast<float*>(ws);
   float4* stats = reinterpret_cast<float4*>(ws + off_stats);
+  float4* stats_g = reinterpret_cast<float4*>(ws + off_sg);
+  float4* stats_n = reinterpret_cast<float4*>(ws + off_sn);
+  uint16_t* qg = reinterpret_cast<uint16_t*>(ws + off_g);
+  uint16_t* og = qg + g_elems;
+  uint16_t* kg = og + g_elems;
+  uint16_t* vg = kg + g_elems;
   const size_t grad_bytes = (size_t)rows * D * 4;
-  // dq is accumulated by every class; dk and dv are stored by the band
-  // kernel (every key row has one band tile) before the global classes add
+  // dq is accumulated by every tile; dk and dv are stored by the band tiles
+  // (every key row has one) before the global-key tiles add to them
   LF_CUDA(cudaMemsetAsync(dq, 0, grad_bytes, stream));
 
-  // parameters of the tcgen05 band kernel: residue views of k, v, q, dout
+  // kernel parameters: residue views of k, v, q, dout per dilation value,
+  // undilated views of q and dout, and the gathered global rows
   lf::BwdTcParams T;
   std::memset(&T, 0, sizeof(T));
   for (int sl = 0; sl < bp->n_slots; ++sl) {
     const int d = bp->slot_dil[sl];
     T.dil[sl] = d;
-    if ((s = map_residue(ds, &T.tmK[sl], k, D, L, d, B * H)) != LF_OK) return s;
-    if ((s = map_residue(ds, &T.tmV[sl], v, D, L, d, B * H)) != LF_OK) return s;
-    const uint32_t qb = D == 64 ? lf::BtcCfg<64>::QB : lf::BtcCfg<128>::QB;
-    if ((s = map_residue(ds, &T.tmQ[sl], q, D, L, d, B * H, qb)) != LF_OK) return s;
-    if ((s = map_residue(ds, &T.tmO[sl], dout, D, L, d, B * H, qb)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmK[sl], k, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmV[sl], v, D, L, d, BH)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmQ[sl], q, D, L, d, BH, QB)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmO[sl], dout, D, L, d, BH, QB)) != LF_OK) return s;
   }
-  T.tiles = bp->d_tc_tiles;
+  if (n_g > 0) {
+    if ((s = map_residue(ds, &T.tmQn, q, D, L, 1, BH, QB)) != LF_OK) return s;
+    if ((s = map_residue(ds, &T.tmOn, dout, D, L, 1, BH, QB)) != LF_OK) return s;
+    if ((s = map_rows(ds, &T.tmQg, qg, D, NGQ, BH, QB)) != LF_OK) return s;
+    if ((s = map_rows(ds, &T.tmOg, og, D, NGQ, BH, QB)) != LF_OK) return s;
+    if ((s = map_rows(ds, &T.tmKg, kg, D, NGQ, BH, lf::kBtcKeys)) != LF_OK) return s;
+    if ((s = map_rows(ds, &T.tmVg, vg, D, NGQ, BH, lf::kBtcKeys)) != LF_OK) return s;
+  }
+  T.tiles = bp->d_tiles;
   T.stats = stats;
   T.stats_bh = stats_bh;
+  T.stats_g = stats_g;
+  T.stats_n = stats_n;
+  T.gidx = pat->d_G;
+  T.n_g = n_g;
+  T.NGQ = NGQ;
   T.dq = dq;
   T.dk = dk;
   T.dv = dv;
@@ -1457,71 +1505,49 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   T.status = ds->status;
   T.wait_iters = lf::wait_iters_for(wait_timeout_ns());
 
-  lf::BwdParams P;
-  P.q = static_cast<const __nv_bfloat16*>(q);
-  P.k = static_cast<const __nv_bfloat16*>(k);
-  P.v = static_cast<const __nv_bfloat16*>(v);
-  P.dout = static_cast<const __nv_bfloat16*>(dout);
-  P.lse = lse;
-  P.delta = delta;
-  P.dq = dq;
-  P.dk = dk;
-  P.dv = dv;
-  P.gidx = pat->d_G;
-  P.is_glob = pat->d_isg;
-  P.head_dil = pat->d_dil;
-  P.H = H;
-  P.L = L;
-  P.w = w;
-  P.n_g = n_g;
-  P.scale = scale;
-
-  const int dthreads = 256;
-  const unsigned dblocks = (unsigned)((rows + dthreads / 32 - 1) / (dthreads / 32));
-  const int gt = (n_g + lf::kBwdB - 1) / lf::kBwdB;
-  const int n_sc = ((L + lf::kBwdB - 1) / lf::kBwdB + lf::kBwdChunk - 1) / lf::kBwdChunk;
-  const long long gunits = (long long)B * H * gt * n_sc;
   auto launch_all = [&](auto dc) -> lf_status {
     constexpr int DD = decltype(dc)::value;
-    const int smem = (int)sizeof(lf::BwdSmem<DD>);
+    using CF = lf::BtcCfg<DD>;
     {
       std::lock_guard<std::mutex> lk(g_mu);
       const int slot = dev * 2 + (DD == 128 ? 1 : 0);
       if (slot < 64 && !g_bwd_smem_set[slot]) {
-        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-        LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_kernel<DD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         LF_CUDA(cudaFuncSetAttribute(lf::lf_bwd_band_tc_kernel<DD>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)lf::BtcCfg<DD>::SMEM_BYTES));
+                                     (int)CF::SMEM_BYTES));
         g_bwd_smem_set[slot] = true;
       }
     }
-    traced("bwd_delta", stream, [&] {
-      lf::lf_bwd_delta_kernel<DD><<<dblocks, dthreads, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(out), P.dout, delta, rows);
-    });
     {
-      const long long total = (long long)B * H * stats_bh;
-      const int sthreads = 256;
-      const unsigned sblocks = (unsigned)std::min<long long>((total + sthreads - 1) / sthreads,
-                                                             (long long)ds->num_sms * 16);
-      traced("bwd_stats", stream, [&] {
-        lf::lf_bwd_tc_stats_kernel<<<sblocks, sthreads, 0, stream>>>(
-            lse, delta, pat->d_isg, pat->d_dil, H, L, stats_bh, total, stats);
+      // blocks per part: the rows, the gathered global rows, the padding
+      const int pthreads = 256;
+      auto nblk = [&](long long units) {
+        return (int)std::max<long long>(
+            1, std::min<long long>((units + pthreads - 1) / pthreads, (long long)ds->num_sms * 16));
+      };
+      const int nb0 = nblk(rows * (DD / 8)), nb1 = nblk((long long)BH * NGQ * (DD / 8));
+      const int nb2 = nblk((long long)BH * 2 * lf::kBtcQPad);
+      traced("bwd_prep", stream, [&] {
+        lf::lf_bwd_tc_prep_kernel<DD><<<nb0 + nb1 + nb2, pthreads, 0, stream>>>(
+            reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
+            reinterpret_cast<const uint4*>(v), reinterpret_cast<const uint4*>(out),
+            reinterpret_cast<const uint4*>(dout), lse, pat->d_isg, pat->d_dil, pat->d_G, n_g,
+            NGQ, H, L, stats_bh, BH, stats, stats_n, stats_g, reinterpret_cast<uint4*>(qg),
+            reinterpret_cast<uint4*>(og), reinterpret_cast<uint4*>(kg),
+            reinterpret_cast<uint4*>(vg), nb0, nb1);
       });
     }
-    if (bp->n_tc_tiles > 0)
-      traced("bwd_band", stream, [&] {
-        lf::lf_bwd_band_tc_kernel<DD><<<(unsigned)bp->n_tc_tiles, lf::BtcCfg<DD>::THREADS,
-                                        lf::BtcCfg<DD>::SMEM_BYTES, stream>>>(T);
+    if (bp->n_band > 0)
+      traced("bwd_tc_band", stream, [&] {
+        lf::lf_bwd_band_tc_kernel<DD><<<(unsigned)bp->n_band, CF::THREADS, CF::SMEM_BYTES,
+                                        stream>>>(T);
       });
-    if (gunits > 0) {
-      if (gunits > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "too many global tiles");
-      traced("bwd_global_keys", stream, [&] {
-        lf::lf_bwd_kernel<DD, 1><<<(unsigned)gunits, lf::kBwdThreads, smem, stream>>>(P);
-      });
-      traced("bwd_global_rows", stream, [&] {
-        lf::lf_bwd_kernel<DD, 2><<<(unsigned)gunits, lf::kBwdThreads, smem, stream>>>(P);
+    if (bp->n_gkey > 0) {
+      lf::BwdTcParams T2 = T;
+      T2.tiles = bp->d_tiles + bp->n_band;
+      traced("bwd_tc_global_keys", stream, [&] {
+        lf::lf_bwd_band_tc_kernel<DD><<<(unsigned)bp->n_gkey, CF::THREADS, CF::SMEM_BYTES,
+                                        stream>>>(T2);
       });
     }
     return LF_OK;
@@ -1900,7 +1926,7 @@ void lf_plan_cache_clear(void) {
   for (auto& kv : g_bias_ws)
     if (kv.second.ptr) cudaFree(kv.second.ptr);
   g_bias_ws.clear();
-  for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tc_tiles);
+  for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tiles);
   g_bwd_plans.clear();
   for (auto& kv : g_gemms) {
     cublasLtMatmulDescDestroy(kv.second.op);

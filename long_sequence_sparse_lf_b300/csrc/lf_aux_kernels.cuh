@@ -27,13 +27,15 @@ __global__ void lf_cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __
 }
 
 // ---------------------------------------------------------------- gather
-// dst_X[bh][g][:] = X[bh][G[g]][:] for g < n_g, 0 for n_g <= g < NGQ.
+// dst_X[bh][g][:] = X[bh][G[g]][:] for g < n_g, 0 for n_g <= g < NGQ, for
+// X = q, k, v and, when `x4` is not null, a fourth tensor x4.
 // One thread per 16-byte piece (D/8 pieces per row).
 __global__ void lf_gather_globals_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
                                          const uint4* __restrict__ v, uint4* __restrict__ qg,
                                          uint4* __restrict__ kg, uint4* __restrict__ vg,
                                          const int32_t* __restrict__ gidx, int n_g, int NGQ, int L,
-                                         int D, int BH) {
+                                         int D, int BH, const uint4* __restrict__ x4 = nullptr,
+                                         uint4* __restrict__ x4g = nullptr) {
   const int pieces = D / 8;
   const size_t total = (size_t)BH * NGQ * pieces;
   for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < total;
@@ -42,16 +44,18 @@ __global__ void lf_gather_globals_kernel(const uint4* __restrict__ q, const uint
     const size_t rowi = x / pieces;
     const int g = (int)(rowi % NGQ);
     const size_t bh = rowi / NGQ;
-    uint4 a = make_uint4(0, 0, 0, 0), b = a, c = a;
+    uint4 a = make_uint4(0, 0, 0, 0), b = a, c = a, e = a;
     if (g < n_g) {
       const size_t src = (bh * L + gidx[g]) * pieces + pc;
       a = q[src];
       b = k[src];
       c = v[src];
+      if (x4 != nullptr) e = x4[src];
     }
     qg[x] = a;
     kg[x] = b;
     vg[x] = c;
+    if (x4g != nullptr) x4g[x] = e;
   }
 }
 

@@ -1,11 +1,29 @@
-// Backward of the sparse attention, band pairs, on the 5th-generation tensor
-// core (tcgen05 / TMEM / TMA) for sm_103a.
+// Backward of the sparse attention on the 5th-generation tensor core
+// (tcgen05 / TMEM / TMA) for sm_103a: dq, dk, dv of sum(out * dout).
 //
-// The pairs (i, j) with i not a global token and j in band(i) ("Longformer
-// explained" §2: the sliding and dilated windows) are the bulk of the
-// backward.  band(i) is symmetric in residue space (t_j - t_i in [-w, w]
-// within one residue class), so one CTA owns a tile of 128 keys of one
-// residue class of one head, keeps K and V in shared memory, and walks the
+// With s_ij = scale q_i.k_j over the key set K(i) (band(i) ∪ G, or every key
+// for a global row i), p_ij = exp(s_ij - lse_i) (lse from the forward) and
+// out_i = sum_j p_ij v_j, the chain rule gives per attended pair (i, j):
+//   dv_j += p_ij dout_i,   dp_ij = dout_i . v_j,
+//   ds_ij = p_ij (dp_ij - delta_i),   delta_i = dout_i . out_i,
+//   dq_i += scale ds_ij k_j,   dk_j += scale ds_ij q_i.
+// (The pages give only the forward; this is the derivative of its plain
+// definition: "Longformer explained" §2, §4.)
+//
+// The attended pairs (i, j) split into three classes ("Longformer explained"
+// §2: sliding and dilated windows, global attention):
+//   band        i not global, j in band(i);
+//   global rows i global, every j;
+//   global keys j global, i not global, j not in band(i).
+// A band tile (kind 0) owns 128 keys of one residue class of one head and
+// walks the query blocks of its keys' windows, then the gathered global
+// query rows (which see every key): the band and global-row classes.  A
+// global-key tile (kind 1) owns up to 128 gathered global keys of a head and
+// walks a chunk of the head's query rows in natural order, keeping the
+// pairs outside the key's window.
+//
+// band(i) is symmetric in residue space (t_j - t_i in [-w, w] within one
+// residue class), so a band tile keeps K and V in shared memory and walks the
 // query blocks its keys' windows reach (64 queries at D = 64, where two
 // CTAs share an SM; 128 at D = 128).  Per query block, with keys on the
 // TMEM lanes:
@@ -17,10 +35,11 @@
 //   dK  += dS^T Q           (A = dS^T from TMEM)
 //   dQ^T = K^T dS^T         (A = K^T: the K tile read M-major; B = dS^T,
 //                            written to shared memory by the softmax warps)
-// dV and dK accumulate in TMEM over the tile's query blocks and are stored
-// once (every key has exactly one band tile, so plain stores; the global
-// classes add to them afterwards).  dQ^T of each block is read out of TMEM
-// and added to dq with atomics (several key tiles reach each query).
+// dV and dK accumulate in TMEM over the tile's query blocks; a band tile
+// stores them (every key has exactly one band tile), a global-key tile,
+// launched afterwards, adds its keys' with atomics.  dQ^T of each block is
+// read out of TMEM and added to dq with atomics (several key tiles reach
+// each query).
 //
 // P^T (bf16) is written over the first half of S^T's columns after the
 // whole block of S^T has been read, dS^T over the first half of dP^T's
@@ -30,9 +49,9 @@
 // before dQ^T overwrites dS^T.  At D = 64 the M = 128 product K^T dS^T
 // reads a zero tile as the missing 64 rows of K^T.
 //
-// Query rows that are global tokens (their gradients come from the
-// global-row class) and padding rows past the residue class's end carry
-// lse = +inf in the per-block statistics, so their P is 0.
+// Query rows without pairs of a block's class (global tokens in the band
+// and global-key blocks, padding rows) carry lse = +inf in the block's
+// statistics, so their P is 0.
 //
 // Roles (192 threads): warps 0-3, thread = key = TMEM lane: P, dS, the dQ
 // read-out and the final dK, dV; warp 4: TMA producer; warp 5: TMEM owner
@@ -50,15 +69,32 @@ namespace lf {
 constexpr int kBtcKeys = 128;   // keys per tile (TMEM lanes)
 constexpr int kBtcQPad = 128;   // padding of each residue class of the statistics
 
+// A unit of the backward kernel.
+//   kind 0 (band tile): keys t0 .. t0+127 of residue class r of head bh
+//     (dilation slot `slot`); its query blocks are those of the keys'
+//     windows, then the blocks of gathered global query rows.
+//   kind 1 (global-key tile): gathered global keys t0 .. t0+127 of head bh
+//     (dilation slot `slot`) against the nqb query blocks from row q0 on.
+struct BtcTile {
+  int bh, kind, r, t0, slot, q0, nqb, pad_;
+};
+
 struct BwdTcParams {
   CUtensorMap tmK[kMaxDilSlots];   // 4-D residue views {D, d, L/d, B*H}, box {64, 1, 128, 1}
   CUtensorMap tmV[kMaxDilSlots];
-  CUtensorMap tmQ[kMaxDilSlots];
+  CUtensorMap tmQ[kMaxDilSlots];   // box {64, 1, QB, 1}
   CUtensorMap tmO[kMaxDilSlots];   // dout
+  CUtensorMap tmQn, tmOn;          // undilated views of q and dout (box {64, 1, QB, 1})
+  CUtensorMap tmQg, tmOg;          // gathered global rows {D, NGQ, B*H}, box {64, QB, 1}
+  CUtensorMap tmKg, tmVg;          // gathered global rows, box {64, 128, 1}
   int dil[kMaxDilSlots];
-  const int4* tiles;               // (bh, residue r, first key t0, dilation slot)
+  const BtcTile* tiles;
   const float4* stats;             // per (bh, r, t): (lse log2e or +inf, delta, 0, 0)
   long long stats_bh;              // entries per bh
+  const float4* stats_g;           // [B*H][NGQ]: the gathered global rows' (lse log2e, delta)
+  const float4* stats_n;           // [B*H][L + 128]: natural order, +inf for global rows
+  const int32_t* gidx;             // [n_g] sorted global positions
+  int n_g, NGQ;
   float* dq;                       // [B*H, L, D] fp32, accumulated (zeroed first)
   float* dk;                       // [B*H, L, D] fp32, stored
   float* dv;
@@ -71,6 +107,14 @@ struct BwdTcParams {
 // Entries of one residue class of the statistics (Lr + a block of padding,
 // so that a block starting anywhere in the class stays inside it).
 __host__ __device__ __forceinline__ int btc_class_len(int L, int d) { return L / d + kBtcQPad; }
+
+// Bits lo .. hi (clipped to 0 .. 31) set, or none when the range misses them.
+__device__ __forceinline__ uint32_t range_bits32(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 31);
+  if (lo > hi) return 0u;
+  return (0xffffffffu >> (31 - hi)) & (0xffffffffu << lo);
+}
 
 template <int D>
 struct BtcCfg {
@@ -114,14 +158,18 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
   const float4* stats_s = reinterpret_cast<const float4*>(smem + C::OFF_ST);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int4 tile = p.tiles[blockIdx.x];
-  const int bh = tile.x, r = tile.y, t0 = tile.z, slot = tile.w;
+  const BtcTile tile = p.tiles[blockIdx.x];
+  const int bh = tile.bh, r = tile.r, t0 = tile.t0, slot = tile.slot;
+  const bool gkeys = tile.kind == 1;
   const int d = p.dil[slot];
   const int Lr = residue_len(p.L, d, r);
-  // the query blocks: the keys' windows [t0 - w, t0 + 127 + w], clipped
-  const int qs0 = max(t0 - p.w, 0);
-  const int qend = min(t0 + kBtcKeys - 1 + p.w, Lr - 1);
-  const int nqb = (qend - qs0) / C::QB + 1;
+  // band tile: the query blocks of the keys' windows [t0 - w, t0 + 127 + w]
+  // (clipped), then the gathered global rows; global-key tile: nqb blocks
+  // from q0 on
+  const int qs0 = gkeys ? tile.q0 : max(t0 - p.w, 0);
+  const int nqb_band =
+      gkeys ? tile.nqb : (min(t0 + kBtcKeys - 1 + p.w, Lr - 1) - qs0) / C::QB + 1;
+  const int nqb = nqb_band + (gkeys ? 0 : (p.n_g + C::QB - 1) / C::QB);
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_KV), 1);
@@ -161,25 +209,41 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       mbar_arrive_expect_tx(BAR(C::B_KV), 2u * C::TILE);
 #pragma unroll
       for (int hh = 0; hh < C::NH; ++hh) {
-        tma_load_4d(sb + C::OFF_K + hh * C::HALF, &p.tmK[slot], BAR(C::B_KV), 64 * hh, r, t0, bh);
-        tma_load_4d(sb + C::OFF_V + hh * C::HALF, &p.tmV[slot], BAR(C::B_KV), 64 * hh, r, t0, bh);
+        if (gkeys) {
+          tma_load_3d(sb + C::OFF_K + hh * C::HALF, &p.tmKg, BAR(C::B_KV), 64 * hh, t0, bh);
+          tma_load_3d(sb + C::OFF_V + hh * C::HALF, &p.tmVg, BAR(C::B_KV), 64 * hh, t0, bh);
+        } else {
+          tma_load_4d(sb + C::OFF_K + hh * C::HALF, &p.tmK[slot], BAR(C::B_KV), 64 * hh, r, t0, bh);
+          tma_load_4d(sb + C::OFF_V + hh * C::HALF, &p.tmV[slot], BAR(C::B_KV), 64 * hh, r, t0, bh);
+        }
       }
       const float4* st_src = p.stats + static_cast<long long>(bh) * p.stats_bh +
                              static_cast<long long>(r) * btc_class_len(p.L, d);
+      const float4* stg_src = p.stats_g + static_cast<long long>(bh) * p.NGQ;
+      const float4* stn_src = p.stats_n + static_cast<long long>(bh) * (p.L + kBtcQPad);
       for (int j = 0; j < nqb && ok; ++j) {
         const int b = j % C::NQB;
         const uint32_t u = j / C::NQB;
         if (u > 0 && !bwait(BAR(C::B_QE + b), (u - 1) & 1, W)) { ok = false; break; }
         const int qs = qs0 + C::QB * j;
+        const int gq = (j - nqb_band) * C::QB;   // first gathered row of a global-row block
         mbar_arrive_expect_tx(BAR(C::B_QF + b), 2u * C::QTILE + C::QB * 16u);
+        const uint32_t qd = sb + C::OFF_Q + b * C::QTILE, od = sb + C::OFF_O + b * C::QTILE;
 #pragma unroll
         for (int hh = 0; hh < C::NH; ++hh) {
-          tma_load_4d(sb + C::OFF_Q + b * C::QTILE + hh * C::QHALF, &p.tmQ[slot],
-                      BAR(C::B_QF + b), 64 * hh, r, qs, bh);
-          tma_load_4d(sb + C::OFF_O + b * C::QTILE + hh * C::QHALF, &p.tmO[slot],
-                      BAR(C::B_QF + b), 64 * hh, r, qs, bh);
+          if (gkeys) {
+            tma_load_4d(qd + hh * C::QHALF, &p.tmQn, BAR(C::B_QF + b), 64 * hh, 0, qs, bh);
+            tma_load_4d(od + hh * C::QHALF, &p.tmOn, BAR(C::B_QF + b), 64 * hh, 0, qs, bh);
+          } else if (j < nqb_band) {
+            tma_load_4d(qd + hh * C::QHALF, &p.tmQ[slot], BAR(C::B_QF + b), 64 * hh, r, qs, bh);
+            tma_load_4d(od + hh * C::QHALF, &p.tmO[slot], BAR(C::B_QF + b), 64 * hh, r, qs, bh);
+          } else {
+            tma_load_3d(qd + hh * C::QHALF, &p.tmQg, BAR(C::B_QF + b), 64 * hh, gq, bh);
+            tma_load_3d(od + hh * C::QHALF, &p.tmOg, BAR(C::B_QF + b), 64 * hh, gq, bh);
+          }
         }
-        bulk_load(sb + C::OFF_ST + b * C::QB * 16, st_src + qs, C::QB * 16u, BAR(C::B_QF + b));
+        const float4* src = gkeys ? stn_src + qs : (j < nqb_band ? st_src + qs : stg_src + gq);
+        bulk_load(sb + C::OFF_ST + b * C::QB * 16, src, C::QB * 16u, BAR(C::B_QF + b));
         ++armed;
       }
       // drain: every armed load completes before the CTA exits
@@ -252,7 +316,9 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
     const int row = warp * 32 + lane;   // key row = TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int tk = t0 + row;
-    const bool kvalid = tk < Lr;
+    // the key row's position, and whether it exists
+    const bool kvalid = gkeys ? tk < p.n_g : tk < Lr;
+    const int kpos = gkeys ? (kvalid ? __ldg(p.gidx + tk) : 0) : r + d * tk;
     const float NEG_INF = -__int_as_float(0x7f800000);
     uint8_t* ds_s = smem + C::OFF_DS;
     bool ok = true;
@@ -260,6 +326,8 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       const int b = j % C::NQB;
       const uint32_t u = j / C::NQB;
       const int qs = qs0 + C::QB * j;
+      const bool gblock = !gkeys && j >= nqb_band;   // gathered global query rows
+      const int gq = (j - nqb_band) * C::QB;
       ok = bwait(BAR(C::B_QF + b), u & 1, W) && bwait(BAR(C::B_SP), j & 1, W);
       if (!__all_sync(FULL, ok)) { ok = false; break; }
       tc_fence_after();
@@ -272,14 +340,37 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
 #pragma unroll
       for (int x = 0; x < C::QB / 32; ++x)
         qv[x] = __ballot_sync(FULL, st[32 * x + lane].x != __int_as_float(0x7f800000) &&
-                                        qs + 32 * x + lane < Lr);
-      // this key's queries: t_q in [tk - w, tk + w], as block columns
-      const int clo = kvalid ? tk - p.w - qs : 1, chi = kvalid ? tk + p.w - qs : 0;
+                                        (gblock || gkeys || qs + 32 * x + lane < Lr));
+      // the columns [clo, chi] of this key's pairs in a band block (the
+      // window t_q in [tk - w, tk + w]) or a global-row block (every row);
+      // in a global-key block, the columns of the key's window [elo, ehi]
+      // (positions on its residue class) are the ones left out
+      int clo = 1, chi = 0;
+      if (kvalid && !gkeys) {
+        clo = gblock ? 0 : tk - p.w - qs;
+        chi = gblock ? C::QB - 1 : tk + p.w - qs;
+      }
+      const int elo = kpos - d * p.w - qs, ehi = kpos + d * p.w - qs;
 #pragma unroll 1
       for (int c4 = 0; c4 < C::QB / 32; ++c4) {
         uint32_t sr[32], pr[32];
         tmem_ld32(tl + C::TM_S + 32 * c4, sr);
         tmem_ld32(tl + C::TM_DP + 32 * c4, pr);
+        // bit e: column 32 c4 + e holds one of this key's pairs
+        uint32_t inm;
+        if (!gkeys) {
+          inm = range_bits32(clo - 32 * c4, chi - 32 * c4);
+        } else if (!kvalid) {
+          inm = 0u;
+        } else if (d == 1) {
+          inm = ~range_bits32(elo - 32 * c4, ehi - 32 * c4);
+        } else {
+          // the window's columns on the key's residue class: elo, elo + d, ..
+          uint32_t ex = 0u;
+          const int lo = max(elo, 32 * c4), hi = min(ehi, 32 * c4 + 31);
+          for (int c = lo + ((elo - lo) % d + d) % d; c <= hi; c += d) ex |= 1u << (c - 32 * c4);
+          inm = ~ex;
+        }
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -288,7 +379,7 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
           for (int h = 0; h < 2; ++h) {
             const int col = 32 * c4 + e + h;
             const float4 sv = st[col];
-            const bool in = col >= clo && col <= chi;
+            const bool in = (inm >> (e + h)) & 1u;
             const float x = in ? fmaf(__uint_as_float(sr[e + h]), p.sl2, -sv.x) : NEG_INF;
             pv[h] = ex2_approx(x);
             dv2[h] = pv[h] * (__uint_as_float(pr[e + h]) - sv.y);
@@ -320,37 +411,46 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       if (!__all_sync(FULL, ok)) { ok = false; break; }
       tc_fence_after();
       if (warp * 32 < D) {
-        const int dcol = row;   // lane = row of dQ^T = element of D
+        // lane = row of dQ^T = element of D; column col is query row
+        // i0 + istep * col (band and global-key blocks) or gidx[gq + col]
+        float* dqb = p.dq + static_cast<size_t>(bh) * p.L * D + row;
+        const int i0 = gkeys ? qs : r + d * qs, istep = gkeys ? 1 : d;
 #pragma unroll 1
         for (int c2 = 0; c2 < C::QB / 32; ++c2) {
           uint32_t qr[32];
           tmem_ld32(tl + C::TM_DQ + 32 * c2, qr);
+          // rows without pairs of the block's class (global tokens, padding)
+          // have no bit, and no valid position
+          const uint32_t m = qv[c2];
+          if (!gblock) {
+            float* dqc = dqb + static_cast<size_t>(i0 + istep * 32 * c2) * D;
+            const size_t step = static_cast<size_t>(istep) * D;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = 32 * c2 + e;
-            // global query rows and padding rows: no contribution (and no
-            // valid position)
-            if ((qv[col >> 5] >> (col & 31)) & 1u) {
-              const size_t i = static_cast<size_t>(r) + static_cast<size_t>(d) * (qs + col);
-              atomicAdd(p.dq + (static_cast<size_t>(bh) * p.L + i) * D + dcol,
-                        p.scale * __uint_as_float(qr[e]));
-            }
+            for (int e = 0; e < 32; ++e)
+              if ((m >> e) & 1u) atomicAdd(dqc + e * step, p.scale * __uint_as_float(qr[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if ((m >> e) & 1u)
+                atomicAdd(dqb + static_cast<size_t>(__ldg(p.gidx + gq + 32 * c2 + e)) * D,
+                          p.scale * __uint_as_float(qr[e]));
           }
         }
       }
       tc_fence_before();
       mbar_arrive(BAR(C::B_DF));
     }
-    // ---- the tile's dV and dK rows (every key has one band tile: stored);
-    // the warp's TMEM loads stay converged, the stores are per row
+    // ---- the tile's dV and dK rows: a band tile stores them (every key has
+    // one band tile), a global-key tile adds to them; the warp's TMEM loads
+    // stay converged, the stores are per row
     if (ok) {
-      const size_t base = (static_cast<size_t>(bh) * p.L + r + static_cast<size_t>(d) * tk) * D;
+      const size_t base = (static_cast<size_t>(bh) * p.L + kpos) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t vr[32], kr[32];
         tmem_ld32(tl + C::TM_DV + c0, vr);
         tmem_ld32(tl + C::TM_DK + c0, kr);
-        if (kvalid) {
+        if (kvalid && !gkeys) {
           float4* dvp = reinterpret_cast<float4*>(p.dv + base + c0);
           float4* dkp = reinterpret_cast<float4*>(p.dk + base + c0);
 #pragma unroll
@@ -361,6 +461,12 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
                                       p.scale * __uint_as_float(kr[e + 1]),
                                       p.scale * __uint_as_float(kr[e + 2]),
                                       p.scale * __uint_as_float(kr[e + 3]));
+          }
+        } else if (kvalid) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            atomicAdd(p.dv + base + c0 + e, __uint_as_float(vr[e]));
+            atomicAdd(p.dk + base + c0 + e, p.scale * __uint_as_float(kr[e]));
           }
         }
       }
@@ -375,30 +481,111 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
   }
 }
 
-// Per (bh, residue class, t) statistics of the band kernel's query rows:
-// (lse log2e, delta) of row i = r + d t, or lse = +inf for a global token
-// or a padding entry past the class's end (their band gradients are 0).
-__global__ void lf_bwd_tc_stats_kernel(const float* __restrict__ lse,
-                                       const float* __restrict__ delta,
-                                       const uint8_t* __restrict__ is_glob,
-                                       const int32_t* __restrict__ head_dil, int H, int L,
-                                       long long stats_bh, long long total, float4* __restrict__ stats) {
+// Inputs of the backward kernel, in one pass over the rows:
+//   stats   [bh][r][t]: residue order, each class padded by kBtcQPad
+//           entries; row r + d t's (lse log2e, delta), lse = +inf for a global
+//           token and for the padding (band blocks);
+//   stats_n [bh][i]: natural order, +inf for global tokens and for the
+//           kBtcQPad entries past L (global-key blocks);
+//   stats_g [bh][g]: gathered global row g < n_g, +inf past n_g
+//           (global-row blocks);
+//   qg, og, kg, vg [bh][g][:]: rows gidx[g] of q, dout, k, v, zero past n_g;
+// with delta_i = dout_i . out_i (bf16 rows, fp32 sum).  A row is read by
+// D / 8 threads, 16 bytes each.  The first nb0 blocks take the rows, the next
+// nb1 the gathered global rows, the rest the padding entries.
+template <int D>
+__global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
+                                      const uint4* __restrict__ v, const uint4* __restrict__ out,
+                                      const uint4* __restrict__ dout,
+                                      const float* __restrict__ lse,
+                                      const uint8_t* __restrict__ is_glob,
+                                      const int32_t* __restrict__ head_dil,
+                                      const int32_t* __restrict__ gidx, int n_g, int NGQ, int H,
+                                      int L, long long stats_bh, long long BH,
+                                      float4* __restrict__ stats, float4* __restrict__ stats_n,
+                                      float4* __restrict__ stats_g, uint4* __restrict__ qg,
+                                      uint4* __restrict__ og, uint4* __restrict__ kg,
+                                      uint4* __restrict__ vg, int nb0, int nb1) {
+  constexpr int G = D / 8;   // threads per row (a divisor of 32)
   const float INF = __int_as_float(0x7f800000);
-  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
-       x += (long long)gridDim.x * blockDim.x) {
-    const long long bh = x / stats_bh;
-    const int e = (int)(x - bh * stats_bh);
-    const int d = head_dil[bh % H];
-    const int cl = btc_class_len(L, d);
-    float4 o = make_float4(INF, 0.f, 0.f, 0.f);
-    if (e < d * cl) {
-      const int r = e / cl, t = e - r * cl;
-      if (t < residue_len(L, d, r)) {
-        const int i = r + d * t;
-        if (!is_glob[i]) o = make_float4(lse[bh * L + i] * 1.4426950408889634f, delta[bh * L + i], 0.f, 0.f);
+  const float LOG2E = 1.4426950408889634f;
+  const int lane = threadIdx.x & 31, sub = lane % G;
+  const int part = blockIdx.x < nb0 ? 0 : blockIdx.x < nb0 + nb1 ? 1 : 2;
+  const int pb = blockIdx.x - (part == 0 ? 0 : part == 1 ? nb0 : nb0 + nb1);
+  const int pnb = part == 0 ? nb0 : part == 1 ? nb1 : (int)gridDim.x - nb0 - nb1;
+  const long long warp0 = (pb * (long long)blockDim.x + threadIdx.x) / 32;
+  const long long wstride = (long long)pnb * blockDim.x / 32;
+  // delta of row `row` (all lanes of the warp take part; invalid rows give 0)
+  auto delta_of = [&](bool ok, long long row) -> float {
+    float s = 0.f;
+    if (ok) {
+      const uint4 a = out[row * G + sub], b = dout[row * G + sub];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
       }
     }
-    stats[x] = o;
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+  };
+  if (part == 0) {
+    const long long rows = BH * L;
+    for (long long w0 = warp0; w0 * (32 / G) < rows; w0 += wstride) {
+      const long long row = w0 * (32 / G) + lane / G;
+      const bool ok = row < rows;
+      const float dl = delta_of(ok, row);
+      if (ok && sub == 0) {
+        const long long bh = row / L;
+        const int i = (int)(row - bh * L);
+        const int d = head_dil[bh % H];
+        const int r = i % d, t = i / d;
+        const float4 o = make_float4(is_glob[i] ? INF : lse[row] * LOG2E, dl, 0.f, 0.f);
+        stats[bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
+        stats_n[bh * (L + kBtcQPad) + i] = o;
+      }
+    }
+  } else if (part == 1) {
+    const long long grows = BH * NGQ;
+    for (long long w0 = warp0; w0 * (32 / G) < grows; w0 += wstride) {
+      const long long gr = w0 * (32 / G) + lane / G;
+      const bool in = gr < grows;
+      const long long bh = in ? gr / NGQ : 0;
+      const int g = in ? (int)(gr - bh * NGQ) : 0;
+      const bool ok = in && g < n_g;
+      const long long row = ok ? bh * L + gidx[g] : 0;
+      const float dl = delta_of(ok, row);
+      if (in) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const long long dst = gr * G + sub;
+        qg[dst] = ok ? q[row * G + sub] : z;
+        og[dst] = ok ? dout[row * G + sub] : z;
+        kg[dst] = ok ? k[row * G + sub] : z;
+        vg[dst] = ok ? v[row * G + sub] : z;
+        if (sub == 0) stats_g[gr] = ok ? make_float4(lse[row] * LOG2E, dl, 0.f, 0.f)
+                                       : make_float4(INF, 0.f, 0.f, 0.f);
+      }
+    }
+  } else {
+    // per bh: d classes of kBtcQPad entries past each class's end, and
+    // kBtcQPad entries past L in natural order
+    const float4 pad = make_float4(INF, 0.f, 0.f, 0.f);
+    for (long long x = pb * (long long)blockDim.x + threadIdx.x; x < BH * 2 * kBtcQPad;
+         x += (long long)pnb * blockDim.x) {
+      const long long bh = x / (2 * kBtcQPad);
+      const int e = (int)(x - bh * 2 * kBtcQPad);
+      if (e >= kBtcQPad) {
+        stats_n[bh * (L + kBtcQPad) + L + (e - kBtcQPad)] = pad;
+      } else {
+        const int d = head_dil[bh % H];
+        const int cl = btc_class_len(L, d);
+        for (int r = 0; r < d; ++r) stats[bh * stats_bh + (long long)r * cl + (cl - kBtcQPad) + e] = pad;
+      }
+    }
   }
 }
 

@@ -1,9 +1,6 @@
-"""The pair counts bench.py turns into useful FLOPs, against the oracle's key
-sets (dense masks) on small workloads:
-  - band_class_pairs: sum over non-global rows of |band(i)| (the backward's
-    band kernel);
-  - extra_block_pairs: the pairs a table of extra key blocks adds to
-    band ∪ G.
+"""The pair count bench.py turns into useful FLOPs for the extra-block
+workloads, against the oracle's key sets (dense masks) on small workloads:
+extra_block_pairs, the pairs a table of extra key blocks adds to band ∪ G.
 """
 import numpy as np
 import pytest
@@ -24,18 +21,6 @@ SHAPES = [
 def _mask_total(wl, h, xb_h=None, rows=None):
     rows = np.arange(wl.L) if rows is None else rows
     return int(O.mask_rows(rows, wl.L, wl.w, wl.dilation[h], wl.global_idx, xb_h).sum())
-
-
-@pytest.mark.parametrize("shape", SHAPES)
-def test_band_class_pairs_matches_masks(shape):
-    B, L, w, dil, G = shape
-    wl = W.custom("t", B, len(dil), L, 64, w, dil, G, 0)
-    want = 0
-    ng_rows = np.array([i for i in range(L) if i not in set(G)])
-    for h, d in enumerate(dil):
-        diff = np.arange(L)[None, :] - ng_rows[:, None]
-        want += int(((np.abs(diff) <= d * w) & (diff % d == 0)).sum())
-    assert bench.band_class_pairs(wl) == want * B
 
 
 @pytest.mark.parametrize("shape", SHAPES)

@@ -43,6 +43,11 @@ CASES = [
     (2, 2, 1000, 64, 70, (1, 1), (3, 500)),
     (1, 2, 768, 128, 40, (1, 2), (0, 100, 767)),
     (1, 1, 256, 64, 16, (1,), ()),
+    # more than 128 global tokens (two global-key tiles per head), dilated heads
+    (1, 2, 1024, 64, 24, (1, 2), tuple(range(0, 1024, 7))),
+    (1, 2, 640, 128, 20, (2, 1), tuple(range(5, 640, 4))),
+    # L not a multiple of the query block, globals at both ends
+    (1, 3, 333, 64, 50, (1, 1, 1), (0, 332)),
 ]
 
 
