@@ -594,7 +594,9 @@ lf_status get_plan(int dev, int num_sms, int B, int D, const std::shared_ptr<Pat
 // ------------------------------------------------------------ tensor maps
 
 lf_status encode(DevState* ds, CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box) {
+                 const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t gd[5];
   cuuint64_t gs[4];
   cuuint32_t bx[5], es[5];
@@ -604,8 +606,8 @@ lf_status encode(DevState* ds, CUtensorMap* m, const void* base, int rank, const
     es[i] = 1;
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-  CUresult r = ds->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd,
-                          gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = ds->encode(m, dtype, rank, const_cast<void*>(base), gd,
+                          gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return LF_OK;
@@ -618,6 +620,17 @@ lf_status map_residue(DevState* ds, CUtensorMap* m, const void* base, int D, int
   const uint64_t st[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * d, (uint64_t)D * 2 * L};
   const uint32_t box[4] = {64, 1, box_rows, 1};
   return encode(ds, m, base, 4, dims, st, box);
+}
+
+// 4-D residue view {D, d, L/d, BH} of a [BH, L, D] fp32 tensor, box
+// {64, 1, box_rows, 1}, unswizzled (the target of tiled reduce-adds)
+lf_status map_residue_f32(DevState* ds, CUtensorMap* m, const void* base, int D, int L, int d,
+                          int BH, uint32_t box_rows) {
+  const uint64_t dims[4] = {(uint64_t)D, (uint64_t)d, (uint64_t)(L / d), (uint64_t)BH};
+  const uint64_t st[3] = {(uint64_t)D * 4, (uint64_t)D * 4 * d, (uint64_t)D * 4 * L};
+  const uint32_t box[4] = {64, 1, box_rows, 1};
+  return encode(ds, m, base, 4, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // 3-D view {D, rows, BH} with a box of `box_rows` rows
@@ -1478,10 +1491,12 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     if ((s = map_residue(ds, &T.tmV[sl], v, D, L, d, BH)) != LF_OK) return s;
     if ((s = map_residue(ds, &T.tmQ[sl], q, D, L, d, BH, QB)) != LF_OK) return s;
     if ((s = map_residue(ds, &T.tmO[sl], dout, D, L, d, BH, QB)) != LF_OK) return s;
+    if ((s = map_residue_f32(ds, &T.tmDQ[sl], dq, D, L, d, BH, QB)) != LF_OK) return s;
   }
   if (n_g > 0) {
     if ((s = map_residue(ds, &T.tmQn, q, D, L, 1, BH, QB)) != LF_OK) return s;
     if ((s = map_residue(ds, &T.tmOn, dout, D, L, 1, BH, QB)) != LF_OK) return s;
+    if ((s = map_residue_f32(ds, &T.tmDQn, dq, D, L, 1, BH, QB)) != LF_OK) return s;
     if ((s = map_rows(ds, &T.tmQg, qg, D, NGQ, BH, QB)) != LF_OK) return s;
     if ((s = map_rows(ds, &T.tmOg, og, D, NGQ, BH, QB)) != LF_OK) return s;
     if ((s = map_rows(ds, &T.tmKg, kg, D, NGQ, BH, lf::kBtcKeys)) != LF_OK) return s;

@@ -47,11 +47,17 @@
 // S^T's second half has been read, and the tensor pipe runs this thread's
 // products in order, so the dV and dK products have read P^T and dS^T
 // before dQ^T overwrites dS^T.  At D = 64 the M = 128 product K^T dS^T
-// reads a zero tile as the missing 64 rows of K^T.
+// reads the V tile as the missing 64 rows of K^T: those rows land in TMEM
+// lanes 64..127, which nothing reads (the columns' earlier contents, P^T and
+// dS^T of keys 64..127, have been consumed by then).
+//
+// dQ^T is read out of TMEM into staging rows [query][D] fp32 in shared
+// memory and added to dq by one tiled bulk reduce-add per 64 columns (through
+// the fp32 residue view of dq), or per row for gathered global rows.
 //
 // Query rows without pairs of a block's class (global tokens in the band
-// and global-key blocks, padding rows) carry lse = +inf in the block's
-// statistics, so their P is 0.
+// and global-key blocks, padding rows) carry -lse log2e = -inf in the
+// block's statistics, so their P is 0.
 //
 // Roles (192 threads): warps 0-3, thread = key = TMEM lane: P, dS, the dQ
 // read-out and the final dK, dV; warp 4: TMA producer; warp 5: TMEM owner
@@ -87,12 +93,17 @@ struct BwdTcParams {
   CUtensorMap tmQn, tmOn;          // undilated views of q and dout (box {64, 1, QB, 1})
   CUtensorMap tmQg, tmOg;          // gathered global rows {D, NGQ, B*H}, box {64, QB, 1}
   CUtensorMap tmKg, tmVg;          // gathered global rows, box {64, 128, 1}
+  CUtensorMap tmDQ[kMaxDilSlots];  // fp32 residue views of dq, box {64, 1, QB, 1}, no swizzle
+  CUtensorMap tmDQn;               // the undilated fp32 view of dq
   int dil[kMaxDilSlots];
   const BtcTile* tiles;
-  const float4* stats;             // per (bh, r, t): (lse log2e or +inf, delta, 0, 0)
+  // per query row (-lse log2e, -delta, 0, 0), or (-inf, 0, 0, 0) where the
+  // row has no pairs of the block's class; 16 bytes an entry, so that a
+  // bulk copy from any entry starts 16-byte aligned
+  const float4* stats;             // per (bh, r, t), residue order
   long long stats_bh;              // entries per bh
-  const float4* stats_g;           // [B*H][NGQ]: the gathered global rows' (lse log2e, delta)
-  const float4* stats_n;           // [B*H][L + 128]: natural order, +inf for global rows
+  const float4* stats_g;           // [B*H][NGQ]: the gathered global rows
+  const float4* stats_n;           // [B*H][L + 128]: natural order
   const int32_t* gidx;             // [n_g] sorted global positions
   int n_g, NGQ;
   float* dq;                       // [B*H, L, D] fp32, accumulated (zeroed first)
@@ -128,9 +139,17 @@ struct BtcCfg {
   static constexpr int NQB = (D == 64) ? 2 : 1;           // Q / dO / stats buffers
   static constexpr uint32_t OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;
   static constexpr uint32_t OFF_O = OFF_Q + NQB * QTILE;
-  static constexpr uint32_t OFF_DS = OFF_O + NQB * QTILE; // dS^T [128 keys][QB queries] bf16
-  static constexpr uint32_t OFF_Z = OFF_DS + (QB / 64) * HALF;   // zero tile (D = 64)
-  static constexpr uint32_t OFF_ST = OFF_Z + (D == 64 ? HALF : 0);   // stats [NQB][QB] float4
+  // dS^T [128 keys][QB queries] bf16
+  static constexpr uint32_t OFF_DS = OFF_O + NQB * QTILE;
+  static constexpr uint32_t DS_TILE = (QB / 64) * HALF;
+  // the dQ staging rows [QB queries][D] fp32: a buffer of their own at
+  // D = 64 (the reduce-add's reads of it then overlap the next block), over
+  // the dS^T buffer (grown to fit) at D = 128, where shared memory is short
+  static constexpr bool STG_OWN = (D == 64);
+  static constexpr uint32_t STG_BYTES = QB * D * 4u;
+  static constexpr uint32_t OFF_STG = STG_OWN ? OFF_DS + DS_TILE : OFF_DS;
+  static constexpr uint32_t OFF_ST =   // stats [NQB][QB] float4
+      STG_OWN ? OFF_STG + STG_BYTES : OFF_DS + (DS_TILE > STG_BYTES ? DS_TILE : STG_BYTES);
   static constexpr uint32_t OFF_BAR = OFF_ST + NQB * QB * 16;
   // barriers
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQB, B_SP = B_QE + NQB, B_PD = B_SP + 1,
@@ -141,6 +160,11 @@ struct BtcCfg {
   static constexpr uint32_t TM_DQ = QB / 2;               // dQ^T: QB columns from here
   static constexpr uint32_t TM_COLS = (D == 64) ? 256 : 512;
   static constexpr int THREADS = 192;
+  // the dQ read-out: D threads, one staging row (query) each
+  static_assert(QB <= D, "one read-out thread per staging row");
+  static_assert(QB % 64 == 0, "the read-out loads 64 query columns at a time");
+  static_assert(SMEM_BYTES * CTAS <= 228u * 1024u && SMEM_BYTES <= 227u * 1024u,
+                "shared memory of the CTAs of one SM");
 };
 
 template <int D>
@@ -188,12 +212,6 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
   if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
     tmem_relinquish();
-  }
-  if (D == 64 && warp < 4) {
-    // the zero rows standing in for K^T's rows 64..127 in the M = 128 dQ product
-    uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_Z);
-    for (int x = threadIdx.x; x < (int)(C::HALF / 16); x += 128) z[x] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -260,8 +278,8 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       const uint32_t tS = tmem + C::TM_S, tP = tmem + C::TM_DP;
       const uint32_t tV = tmem + C::TM_DV, tK = tmem + C::TM_DK;
       // K^T as an M-major A operand: 64-row groups of M (= D) lie C::HALF
-      // apart; at D = 64 the second group is the zero tile
-      const uint32_t lbo_kt = (D == 128) ? C::HALF : (C::OFF_Z - C::OFF_K);
+      // apart; at D = 64 the second group is the V tile (rows never read)
+      const uint32_t lbo_kt = (D == 128) ? C::HALF : (C::OFF_V - C::OFF_K);
       bool ok = bwait(BAR(C::B_KV), 0, W);
       for (int j = 0; j < nqb && ok; ++j) {
         const int b = j % C::NQB;
@@ -320,6 +338,7 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
     const bool kvalid = gkeys ? tk < p.n_g : tk < Lr;
     const int kpos = gkeys ? (kvalid ? __ldg(p.gidx + tk) : 0) : r + d * tk;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    const float2 sl2v = make_float2(p.sl2, p.sl2);
     uint8_t* ds_s = smem + C::OFF_DS;
     bool ok = true;
     for (int j = 0; j < nqb && ok; ++j) {
@@ -339,7 +358,7 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       uint32_t qv[C::QB / 32];
 #pragma unroll
       for (int x = 0; x < C::QB / 32; ++x)
-        qv[x] = __ballot_sync(FULL, st[32 * x + lane].x != __int_as_float(0x7f800000) &&
+        qv[x] = __ballot_sync(FULL, st[32 * x + lane].x != NEG_INF &&
                                         (gblock || gkeys || qs + 32 * x + lane < Lr));
       // the columns [clo, chi] of this key's pairs in a band block (the
       // window t_q in [tk - w, tk + w]) or a global-row block (every row);
@@ -354,8 +373,9 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
 #pragma unroll 1
       for (int c4 = 0; c4 < C::QB / 32; ++c4) {
         uint32_t sr[32], pr[32];
-        tmem_ld32(tl + C::TM_S + 32 * c4, sr);
-        tmem_ld32(tl + C::TM_DP + 32 * c4, pr);
+        tmem_ld32_issue(tl + C::TM_S + 32 * c4, sr);
+        tmem_ld32_issue(tl + C::TM_DP + 32 * c4, pr);
+        tmem_ld_wait();
         // bit e: column 32 c4 + e holds one of this key's pairs
         uint32_t inm;
         if (!gkeys) {
@@ -374,18 +394,19 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv2[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = 32 * c4 + e + h;
-            const float4 sv = st[col];
-            const bool in = (inm >> (e + h)) & 1u;
-            const float x = in ? fmaf(__uint_as_float(sr[e + h]), p.sl2, -sv.x) : NEG_INF;
-            pv[h] = ex2_approx(x);
-            dv2[h] = pv[h] * (__uint_as_float(pr[e + h]) - sv.y);
-          }
-          pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          dd[e >> 1] = pack_bf16x2(dv2[0], dv2[1]);
+          // columns e, e + 1: (-lse log2e, -delta) of each
+          const float2 s0 = *reinterpret_cast<const float2*>(st + 32 * c4 + e);
+          const float2 s1 = *reinterpret_cast<const float2*>(st + 32 * c4 + e + 1);
+          float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2v,
+                          make_float2(s0.x, s1.x));
+          x.x = ((inm >> e) & 1u) ? x.x : NEG_INF;
+          x.y = ((inm >> (e + 1)) & 1u) ? x.y : NEG_INF;
+          const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          const float2 dv2 = mul2(
+              pv, add2(make_float2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+                       make_float2(s0.y, s1.y)));
+          pp[e >> 1] = pack_bf16x2(pv.x, pv.y);
+          dd[e >> 1] = pack_bf16x2(dv2.x, dv2.y);
         }
         // P^T over S^T's first half, dS^T over dP^T's (both already read)
         tmem_st16(tl + C::TM_S + 16 * c4, pp);
@@ -404,6 +425,10 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       }
       tmem_st_wait();
       fence_proxy_async_smem();
+      // the previous block's reduce-add has read its staging rows before
+      // this block's dQ^T overwrites them (the read-out follows this arrival
+      // through the products)
+      if (C::STG_OWN && threadIdx.x == 0) bulk_wait_read_all();
       tc_fence_before();
       mbar_arrive(BAR(C::B_PD));
       // ---- dQ of the block: dQ^T lanes are D's rows (warps with 32 * warp < D)
@@ -411,35 +436,57 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
       if (!__all_sync(FULL, ok)) { ok = false; break; }
       tc_fence_after();
       if (warp * 32 < D) {
-        // lane = row of dQ^T = element of D; column col is query row
-        // i0 + istep * col (band and global-key blocks) or gidx[gq + col]
-        float* dqb = p.dq + static_cast<size_t>(bh) * p.L * D + row;
-        const int i0 = gkeys ? qs : r + d * qs, istep = gkeys ? 1 : d;
+        // dQ^T (lane = element `row` of D, column = query) into the staging
+        // rows (at D = 128 over the dS^T buffer, whose last reader, the dQ^T
+        // product, has completed): NH halves [QB queries][64] fp32, half hh
+        // holding elements 64 hh .. 64 hh + 63
+        float* stg = reinterpret_cast<float*>(smem + C::OFF_STG);
+        float* my = stg + (row >> 6) * (C::QB * 64) + (row & 63);
 #pragma unroll 1
-        for (int c2 = 0; c2 < C::QB / 32; ++c2) {
-          uint32_t qr[32];
-          tmem_ld32(tl + C::TM_DQ + 32 * c2, qr);
-          // rows without pairs of the block's class (global tokens, padding)
-          // have no bit, and no valid position
-          const uint32_t m = qv[c2];
-          if (!gblock) {
-            float* dqc = dqb + static_cast<size_t>(i0 + istep * 32 * c2) * D;
-            const size_t step = static_cast<size_t>(istep) * D;
+        for (int c2 = 0; c2 < C::QB / 32; c2 += 2) {
+          uint32_t qa[32], qb[32];
+          tmem_ld32_issue(tl + C::TM_DQ + 32 * c2, qa);
+          tmem_ld32_issue(tl + C::TM_DQ + 32 * c2 + 32, qb);
+          tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if ((m >> e) & 1u) atomicAdd(dqc + e * step, p.scale * __uint_as_float(qr[e]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if ((m >> e) & 1u)
-                atomicAdd(dqb + static_cast<size_t>(__ldg(p.gidx + gq + 32 * c2 + e)) * D,
-                          p.scale * __uint_as_float(qr[e]));
+          for (int e = 0; e < 32; ++e) {
+            my[(32 * c2 + e) * 64] = p.scale * __uint_as_float(qa[e]);
+            my[(32 * c2 + 32 + e) * 64] = p.scale * __uint_as_float(qb[e]);
           }
         }
+        fence_proxy_async_smem();
+        named_bar_sync(1, D);
+        const uint32_t stg_a = smem_u32(stg);
+        if (!gblock) {
+          // the block's query rows are one box of the residue (or natural)
+          // view of dq; rows without pairs of the block's class hold zeros,
+          // rows past the end are skipped
+          if (row == 0) {
+#pragma unroll
+            for (int hh = 0; hh < C::NH; ++hh)
+              tma_reduce_add_4d(stg_a + hh * (C::QB * 64 * 4), gkeys ? &p.tmDQn : &p.tmDQ[slot],
+                                64 * hh, gkeys ? 0 : r, qs, bh);
+            bulk_commit_group();
+          }
+        } else if ((qv[row >> 5] >> (row & 31)) & 1u) {
+          // gathered global rows: one reduce-add per 64 elements of the row
+          const int i = __ldg(p.gidx + gq + row);
+#pragma unroll
+          for (int hh = 0; hh < C::NH; ++hh)
+            bulk_reduce_add_f32(p.dq + (static_cast<size_t>(bh) * p.L + i) * D + 64 * hh,
+                                stg_a + (hh * (C::QB * 64) + row * 64) * 4, 256u);
+          bulk_commit_group();
+        }
+        // before the staging rows are written again: at D = 128 the next
+        // block's dS^T (so here); at D = 64 the next read-out (thread 0
+        // waits before the next block's products); the gathered rows' adds
+        // wait here
+        if (!C::STG_OWN || gblock) bulk_wait_read_all();
       }
       tc_fence_before();
       mbar_arrive(BAR(C::B_DF));
     }
+    bulk_wait_all();
     // ---- the tile's dV and dK rows: a band tile stores them (every key has
     // one band tile), a global-key tile adds to them; the warp's TMEM loads
     // stay converged, the stores are per row
@@ -483,11 +530,11 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
 
 // Inputs of the backward kernel, in one pass over the rows:
 //   stats   [bh][r][t]: residue order, each class padded by kBtcQPad
-//           entries; row r + d t's (lse log2e, delta), lse = +inf for a global
-//           token and for the padding (band blocks);
-//   stats_n [bh][i]: natural order, +inf for global tokens and for the
+//           entries; row r + d t's (-lse log2e, -delta), (-inf, 0) for a
+//           global token and for the padding (band blocks);
+//   stats_n [bh][i]: natural order, (-inf, 0) for global tokens and for the
 //           kBtcQPad entries past L (global-key blocks);
-//   stats_g [bh][g]: gathered global row g < n_g, +inf past n_g
+//   stats_g [bh][g]: gathered global row g < n_g, (-inf, 0) past n_g
 //           (global-row blocks);
 //   qg, og, kg, vg [bh][g][:]: rows gidx[g] of q, dout, k, v, zero past n_g;
 // with delta_i = dout_i . out_i (bf16 rows, fp32 sum).  A row is read by
@@ -544,7 +591,8 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
         const int i = (int)(row - bh * L);
         const int d = head_dil[bh % H];
         const int r = i % d, t = i / d;
-        const float4 o = make_float4(is_glob[i] ? INF : lse[row] * LOG2E, dl, 0.f, 0.f);
+        const float4 o = is_glob[i] ? make_float4(-INF, 0.f, 0.f, 0.f)
+                                    : make_float4(-lse[row] * LOG2E, -dl, 0.f, 0.f);
         stats[bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
         stats_n[bh * (L + kBtcQPad) + i] = o;
       }
@@ -566,14 +614,15 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
         og[dst] = ok ? dout[row * G + sub] : z;
         kg[dst] = ok ? k[row * G + sub] : z;
         vg[dst] = ok ? v[row * G + sub] : z;
-        if (sub == 0) stats_g[gr] = ok ? make_float4(lse[row] * LOG2E, dl, 0.f, 0.f)
-                                       : make_float4(INF, 0.f, 0.f, 0.f);
+        if (sub == 0)
+          stats_g[gr] = ok ? make_float4(-lse[row] * LOG2E, -dl, 0.f, 0.f)
+                           : make_float4(-INF, 0.f, 0.f, 0.f);
       }
     }
   } else {
     // per bh: d classes of kBtcQPad entries past each class's end, and
     // kBtcQPad entries past L in natural order
-    const float4 pad = make_float4(INF, 0.f, 0.f, 0.f);
+    const float4 pad = make_float4(-INF, 0.f, 0.f, 0.f);
     for (long long x = pb * (long long)blockDim.x + threadIdx.x; x < BH * 2 * kBtcQPad;
          x += (long long)pnb * blockDim.x) {
       const long long bh = x / (2 * kBtcQPad);

@@ -219,6 +219,42 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// One-dimensional bulk reduce-add shared -> global of `bytes` bytes of fp32
+// (dst[x] += src[x]; both addresses 16-byte aligned, size a multiple of 16),
+// tracked by this thread's bulk async-group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::
+                   "l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes)
+               : "memory");
+}
+// Tiled bulk reduce-add shared -> global through a 4-D tensor map (the
+// element type and the box are the map's; coordinates non-negative, the
+// innermost one a multiple of 16 bytes; rows outside the tensor are skipped).
+__device__ __forceinline__ void tma_reduce_add_4d(uint32_t src, const CUtensorMap* m, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until this thread's committed bulk groups have read their shared
+// memory source (it may be overwritten afterwards).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until this thread's committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Named barrier `id` (1..15) over `n` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (the tensor core reading an operand this thread wrote).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -287,6 +323,20 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
       : "memory");
 }
 
+// The same load without the wait: the registers are valid after
+// tmem_ld_wait() (which waits for all of this thread's outstanding loads).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : LF_R8(0), LF_R8(8), LF_R8(16), LF_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 #undef LF_R8
 
 #define LF_W8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), \
@@ -363,6 +413,19 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 #endif
 }
 
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+#if LF_PACKED_F32X2
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+#else
+  return make_float2(a.x * b.x, a.y * b.y);
+#endif
+}
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
 #if LF_PACKED_F32X2
   float2 r;
