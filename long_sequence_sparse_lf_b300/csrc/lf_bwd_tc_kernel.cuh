@@ -581,20 +581,21 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
     return s;
   };
   if (part == 0) {
-    const long long rows = BH * L;
+    // B*H*L < 2^31 (the entry point checks it): 32-bit row arithmetic
+    const int rows = (int)(BH * L);
     for (long long w0 = warp0; w0 * (32 / G) < rows; w0 += wstride) {
-      const long long row = w0 * (32 / G) + lane / G;
+      const int row = (int)(w0 * (32 / G)) + lane / G;
       const bool ok = row < rows;
       const float dl = delta_of(ok, row);
       if (ok && sub == 0) {
-        const long long bh = row / L;
-        const int i = (int)(row - bh * L);
+        const int bh = row / L;
+        const int i = row - bh * L;
         const int d = head_dil[bh % H];
         const int r = i % d, t = i / d;
         const float4 o = is_glob[i] ? make_float4(-INF, 0.f, 0.f, 0.f)
                                     : make_float4(-lse[row] * LOG2E, -dl, 0.f, 0.f);
-        stats[bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
-        stats_n[bh * (L + kBtcQPad) + i] = o;
+        stats[(long long)bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
+        stats_n[(long long)bh * (L + kBtcQPad) + i] = o;
       }
     }
   } else if (part == 1) {
