@@ -223,10 +223,12 @@ LF_API lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, vo
  *   w, dilation, global_idx, n_global, scale: as for lf_attn_fwd.
  *   eps    finite, > 0.
  *
- * The two linear maps are cuBLASLt GEMMs (bf16 inputs, fp32 accumulation and
- * results); the head split, the attention, and the residual + LayerNorm
- * steps run in this library's kernels.  Scratch: a second grow-only buffer
- * per (device, stream), about (B*L*hidden*24 bytes + 32 MiB), apart from the
+ * The two linear maps are this library's tcgen05 GEMMs (bf16 inputs, fp32
+ * accumulation in tensor memory): the q/k/v map writes bf16(x W^T + b)
+ * straight into per-head q, k, v; the feed-forward map applies its bias, the
+ * residual and the second LayerNorm in its epilogue.  q, k, v, the attention
+ * output, x1 and out are stored in bf16.  Scratch: a second grow-only buffer
+ * per (device, stream), about B*L*hidden*10 bytes, apart from the
  * attention's.  Pointers must be 16-byte aligned (LF_ERR_INVALID_ARG).
  */
 LF_API lf_status lf_layer_fwd(const void* x, const void* w_qkv, const float* b_qkv,

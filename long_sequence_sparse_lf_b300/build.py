@@ -47,7 +47,7 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
     cmd = [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
            "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"),
-           "-o", LIB + ".tmp", *sources(), "-lcudart", "-lcublasLt"]
+           "-o", LIB + ".tmp", *sources(), "-lcudart"]
     if verbose:
         cmd.insert(1, "-Xptxas")
         cmd.insert(2, "-v")

@@ -22,13 +22,13 @@
 #include <tuple>
 #include <vector>
 
-#include <cublasLt.h>
 
 #include "../../include/lfattn.h"
 #include "lf_attn_kernel.cuh"
 #include "lf_aux_kernels.cuh"
 #include "lf_common.cuh"
 #include "lf_bwd_tc_kernel.cuh"
+#include "lf_gemm_kernel.cuh"
 #include "lf_layer_kernels.cuh"
 
 namespace {
@@ -1133,14 +1133,14 @@ lf_status fwd_noalloc_impl(const void* q, const void* k, const void* v, void* ou
 // The Longformer layer of "基于Block-Sparse Attention的Longformer" §6, with
 // the attention read as one softmax over band ∪ G per head (the attention
 // above):
-//   [q | k | v] = x W_qkv^T + b_qkv           (one GEMM, fp32 result)
-//   q, k, v     = bf16, split into H heads     (split_qkv)
-//   a           = attention(q, k, v)           (fwd_impl)
-//   x1          = bf16(LN1(x + merge(a)))      (merge_ln1)
-//   F           = x1 W_ff^T                    (one GEMM, fp32 result)
-//   y           = bf16(LN2(x1 + F + b_ff))     (ln2)
-// The GEMMs are plain library GEMMs (cuBLASLt, bf16 inputs, fp32
-// accumulation and output); everything else runs in this library's kernels.
+//   q, k, v = bf16(x W_qkv^T + b_qkv), split into H heads
+//                                              (tcgen05 GEMM, head-split epilogue)
+//   a       = attention(q, k, v)               (fwd_impl)
+//   x1      = bf16(LN1(x + merge(a)))          (merge_ln1)
+//   y       = bf16(LN2(x1 + x1 W_ff^T + b_ff)) (tcgen05 GEMM, LayerNorm epilogue
+//                                               over a cluster of CTAs per row block)
+// The products accumulate in fp32 in TMEM; only q, k, v, a, x1 and y are
+// stored (bf16).
 
 struct LayerWorkspace {
   uint8_t* ptr = nullptr;
@@ -1165,71 +1165,76 @@ lf_status get_layer_workspace(int dev, cudaStream_t stream, size_t bytes, uint8_
   return LF_OK;
 }
 
-constexpr size_t kGemmWorkspace = size_t(32) << 20;
-
-struct GemmPlan {
-  cublasLtMatmulDesc_t op = nullptr;
-  cublasLtMatrixLayout_t a = nullptr, b = nullptr, c = nullptr;
-  cublasLtMatmulAlgo_t algo{};
+// Tile width and cluster size of the feed-forward GEMM: a row's hidden
+// columns are split over `cluster` CTAs of NT columns (NT fp32 TMEM columns
+// each), at most kGemmMaxCluster.
+struct FfShape {
+  int nt = 0, cluster = 0;
 };
-using GemmKey = std::tuple<int, long long, int, int, bool>;   // device, M, N, K, bf16 Y
-std::map<GemmKey, GemmPlan> g_gemms;
-std::map<int, cublasLtHandle_t> g_lt;
+FfShape ff_shape(int hidden) {
+  if (hidden == 64) return {64, 1};
+  if (hidden % 128 == 0 && hidden / 128 <= lf::kGemmMaxCluster) return {128, hidden / 128};
+  if (hidden % 256 == 0 && hidden / 256 <= lf::kGemmMaxCluster) return {256, hidden / 256};
+  return {};
+}
 
-#define LF_LT(call)                                                                  \
-  do {                                                                               \
-    cublasStatus_t st_ = (call);                                                     \
-    if (st_ != CUBLAS_STATUS_SUCCESS) return fail(LF_ERR_CUDA, "%s: cuBLASLt status %d", #call, (int)st_); \
-  } while (0)
+bool g_gemm_smem_set[64][6] = {};
 
-// Y[M, N] = X[M, K] W[N, K]^T: X, W bf16 row-major, Y fp32 (or bf16, rounded
-// to nearest even) row-major, fp32 accumulation.  In cuBLASLt's column-major
-// terms Y^T = W X^T, i.e. op(A) = W (A stored K x N, transposed) and B = X^T
-// (stored K x M).
-lf_status gemm_xwt(int dev, const void* X, const void* W, void* Y, bool y_bf16, long long M,
-                   int N, int K, void* ws, cudaStream_t stream) {
-  cublasLtHandle_t h = nullptr;
-  GemmPlan* gp = nullptr;
+// C = A B^T through lf_gemm_tc_kernel<NT, EPI>: A [M, K], B [N, K] bf16
+// row-major (the caller sets P's output maps); grid (N / NT, row tiles):
+// B * ceil(L / 128) tiles of one batch element each for EPI 0, ceil(M / 128)
+// for EPI 1, with clusters of `cluster` CTAs along the columns.
+template <int NT, int EPI>
+lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const void* Bw,
+                  long long M, int N, int K, int cluster, cudaStream_t stream, const char* name) {
+  using CF = lf::GemmCfg<NT>;
+  lf_status s;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {(uint32_t)lf::kGemmBK, (uint32_t)lf::kGemmBM};
+    if ((s = encode(ds, &P.tmA, A, 2, dims, st, box)) != LF_OK) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t st[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {(uint32_t)lf::kGemmBK, (uint32_t)NT};
+    if ((s = encode(ds, &P.tmB, Bw, 2, dims, st, box)) != LF_OK) return s;
+  }
+  P.M = (int)M;
+  P.K = K;
+  P.status = ds->status;
+  P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto hi = g_lt.find(dev);
-    if (hi == g_lt.end()) {
-      LF_LT(cublasLtCreate(&h));
-      g_lt[dev] = h;
-    } else {
-      h = hi->second;
+    const int slot = (NT == 64 ? 0 : NT == 128 ? 1 : 2) * 2 + EPI;
+    if (dev < 64 && !g_gemm_smem_set[dev][slot]) {
+      LF_CUDA(cudaFuncSetAttribute(lf::lf_gemm_tc_kernel<NT, EPI>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)CF::SMEM_BYTES));
+      g_gemm_smem_set[dev][slot] = true;
     }
-    auto it = g_gemms.find(GemmKey{dev, M, N, K, y_bf16});
-    if (it != g_gemms.end()) gp = &it->second;
   }
-  if (gp == nullptr) {
-    GemmPlan p;
-    LF_LT(cublasLtMatmulDescCreate(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F));
-    const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-    LF_LT(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)));
-    LF_LT(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)));
-    LF_LT(cublasLtMatrixLayoutCreate(&p.a, CUDA_R_16BF, K, N, K));
-    LF_LT(cublasLtMatrixLayoutCreate(&p.b, CUDA_R_16BF, K, M, K));
-    LF_LT(cublasLtMatrixLayoutCreate(&p.c, y_bf16 ? CUDA_R_16BF : CUDA_R_32F, N, M, N));
-    cublasLtMatmulPreference_t pref = nullptr;
-    LF_LT(cublasLtMatmulPreferenceCreate(&pref));
-    const size_t wsb = kGemmWorkspace;
-    LF_LT(cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                               &wsb, sizeof(wsb)));
-    cublasLtMatmulHeuristicResult_t res{};
-    int n = 0;
-    const cublasStatus_t st =
-        cublasLtMatmulAlgoGetHeuristic(h, p.op, p.a, p.b, p.c, p.c, pref, 1, &res, &n);
-    cublasLtMatmulPreferenceDestroy(pref);
-    if (st != CUBLAS_STATUS_SUCCESS || n < 1)
-      return fail(LF_ERR_UNSUPPORTED, "no cuBLASLt algorithm for a %lld x %d x %d GEMM", M, N, K);
-    p.algo = res.algo;
-    std::lock_guard<std::mutex> lk(g_mu);
-    gp = &(g_gemms[GemmKey{dev, M, N, K, y_bf16}] = p);
+  cudaLaunchConfig_t cfg = {};
+  const long long row_tiles = (EPI == 0)
+                                  ? (long long)P.B * ((P.L + lf::kGemmBM - 1) / lf::kGemmBM)
+                                  : (M + lf::kGemmBM - 1) / lf::kGemmBM;
+  cfg.gridDim = dim3((unsigned)(N / NT), (unsigned)row_tiles, 1);
+  cfg.blockDim = dim3(CF::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = CF::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (EPI == 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
-  const float alpha = 1.f, beta = 0.f;
-  LF_LT(cublasLtMatmul(h, gp->op, &alpha, W, gp->a, X, gp->b, &beta, Y, gp->c, Y, gp->c,
-                       &gp->algo, ws, kGemmWorkspace, stream));
+  cudaError_t e = cudaSuccess;
+  traced(name, stream, [&] { e = cudaLaunchKernelEx(&cfg, lf::lf_gemm_tc_kernel<NT, EPI>, P); });
+  if (e != cudaSuccess) return fail(LF_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(e));
   return LF_OK;
 }
 
@@ -1264,43 +1269,52 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
   if ((s = get_dev(&ds, &dev)) != LF_OK) return s;
 
   const long long M = (long long)B * L;
+  if (M > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "B*L=%lld tokens is too many", M);
+  const FfShape ff = ff_shape(hidden);
+  if (ff.nt == 0) return fail(LF_ERR_UNSUPPORTED, "hidden=%d", hidden);
   const size_t act = (size_t)M * hidden;   // elements of one [B, L, hidden] activation
   size_t off = 0;
-  const size_t off_y = off;                // bf16 Y [M, 3*hidden], later fp32 F [M, hidden]
-  off += align_up(act * 3 * 2, 256);
   const size_t off_qkv = off;              // bf16 3 x [B, H, L, D]
   off += align_up(act * 3 * 2, 256);
   const size_t off_a = off;                // bf16 [B, H, L, D]
   off += align_up(act * 2, 256);
   const size_t off_x1 = off;               // bf16 [M, hidden]
   off += align_up(act * 2, 256);
-  const size_t off_gw = off;               // GEMM workspace
-  off += kGemmWorkspace;
   uint8_t* ws = nullptr;
   if ((s = get_layer_workspace(dev, stream, off, &ws)) != LF_OK) return s;
-  void* y = ws + off_y;
   uint16_t* qkv = reinterpret_cast<uint16_t*>(ws + off_qkv);
   uint16_t* a = reinterpret_cast<uint16_t*>(ws + off_a);
   uint16_t* x1 = reinterpret_cast<uint16_t*>(ws + off_x1);
-  void* gws = ws + off_gw;
 
-  lf_status gs = LF_OK;
-  traced("layer_gemm_qkv", stream,
-         [&] { gs = gemm_xwt(dev, x, w_qkv, y, true, M, 3 * hidden, hidden, gws, stream); });
-  if (gs != LF_OK) return gs;
-  if (M > INT32_MAX) return fail(LF_ERR_UNSUPPORTED, "B*L=%lld tokens is too many", M);
-  traced("layer_split_qkv", stream, [&] {
-    lf::lf_layer_split_qkv_kernel<<<(unsigned)((M + lf::kSplitRows - 1) / lf::kSplitRows),
-                                    3 * hidden / 8, 0, stream>>>(
-        reinterpret_cast<const uint4*>(y), reinterpret_cast<const float4*>(b_qkv),
-        reinterpret_cast<uint4*>(qkv), B, H, L, D);
-  });
+  // q, k, v = bf16(x W_qkv^T + b_qkv), written per head
+  {
+    lf::GemmParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.hidden = hidden;
+    P.bias = b_qkv;
+    P.qkv = qkv;
+    P.B = B;
+    P.H = H;
+    P.L = L;
+    P.D = D;
+    for (int part = 0; part < 3; ++part) {
+      const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L, (uint64_t)B * H};
+      const uint64_t st[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * L};
+      const uint32_t box[3] = {64, (uint32_t)lf::kGemmBM, 1};
+      if ((s = encode(ds, &P.tmO[part], qkv + part * act, 3, dims, st, box)) != LF_OK) return s;
+    }
+    if ((3 * hidden) % 128 == 0)
+      s = gemm_tc<128, 0>(ds, dev, P, x, w_qkv, M, 3 * hidden, hidden, 1, stream, "layer_gemm_qkv");
+    else
+      s = gemm_tc<64, 0>(ds, dev, P, x, w_qkv, M, 3 * hidden, hidden, 1, stream, "layer_gemm_qkv");
+    if (s != LF_OK) return s;
+  }
   if ((s = fwd_impl(qkv, qkv + act, qkv + 2 * act, a, false, B, H, L, D, w, dilation, gidx, n_g,
                     scale, stream)) != LF_OK)
     return s;
-  // the LayerNorm kernels, one warp per row, four rows per CTA (small CTAs
-  // pack into the register file with less of a tail wave), with the widest
-  // vector (VW columns, NJ steps per lane) the width allows
+  // x1 = bf16(LN1(x + merge(a))): one warp per row, four rows per CTA (small
+  // CTAs pack into the register file with less of a tail wave), with the
+  // widest vector (VW columns, NJ steps per lane) the width allows
   const int threads = 128;
   const unsigned rows_blocks = (unsigned)((M + threads / 32 - 1) / (threads / 32));
   auto launch_ln1 = [&](auto vw, auto nj) {
@@ -1310,32 +1324,45 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
           static_cast<const uint16_t*>(x), a, ln1, x1, B, H, L, D, eps);
     });
   };
-  auto launch_ln2 = [&](auto vw, auto nj) {
-    constexpr int VW = decltype(vw)::value, NJ = decltype(nj)::value;
-    traced("layer_ln2", stream, [&] {
-      lf::lf_layer_ln2_kernel<VW, NJ><<<rows_blocks, threads, 0, stream>>>(
-          x1, static_cast<const float*>(y), b_ff, ln2, static_cast<uint16_t*>(out), M, eps);
-    });
-  };
-  auto with_width = [&](auto&& f) {
+  {
     using I = std::integral_constant<int, 1>;
     switch (hidden) {
-      case 64: f(std::integral_constant<int, 2>{}, I{}); break;
-      case 128: f(std::integral_constant<int, 4>{}, I{}); break;
-      case 256: f(std::integral_constant<int, 8>{}, I{}); break;
-      case 384: f(std::integral_constant<int, 4>{}, std::integral_constant<int, 3>{}); break;
-      case 512: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 2>{}); break;
-      case 768: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 3>{}); break;
-      case 1024: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 4>{}); break;
-      case 1536: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 6>{}); break;
-      default: f(std::integral_constant<int, 8>{}, std::integral_constant<int, 8>{}); break;
+      case 64: launch_ln1(std::integral_constant<int, 2>{}, I{}); break;
+      case 128: launch_ln1(std::integral_constant<int, 4>{}, I{}); break;
+      case 256: launch_ln1(std::integral_constant<int, 8>{}, I{}); break;
+      case 384: launch_ln1(std::integral_constant<int, 4>{}, std::integral_constant<int, 3>{}); break;
+      case 512: launch_ln1(std::integral_constant<int, 8>{}, std::integral_constant<int, 2>{}); break;
+      case 768: launch_ln1(std::integral_constant<int, 8>{}, std::integral_constant<int, 3>{}); break;
+      case 1024: launch_ln1(std::integral_constant<int, 8>{}, std::integral_constant<int, 4>{}); break;
+      case 1536: launch_ln1(std::integral_constant<int, 8>{}, std::integral_constant<int, 6>{}); break;
+      default: launch_ln1(std::integral_constant<int, 8>{}, std::integral_constant<int, 8>{}); break;
     }
-  };
-  with_width(launch_ln1);
-  traced("layer_gemm_ff", stream,
-         [&] { gs = gemm_xwt(dev, x1, w_ff, y, false, M, hidden, hidden, gws, stream); });
-  if (gs != LF_OK) return gs;
-  with_width(launch_ln2);
+  }
+  // y = bf16(LN2(x1 + x1 W_ff^T + b_ff))
+  {
+    lf::GemmParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.hidden = hidden;
+    P.bias = b_ff;
+    P.resid = x1;
+    P.ln = ln2;
+    P.out = static_cast<uint16_t*>(out);
+    P.eps = eps;
+    P.L = L;
+    {
+      const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)M};
+      const uint64_t st[1] = {(uint64_t)hidden * 2};
+      const uint32_t box[2] = {64, (uint32_t)lf::kGemmBM};
+      if ((s = encode(ds, &P.tmO[0], out, 2, dims, st, box)) != LF_OK) return s;
+    }
+    if (ff.nt == 64)
+      s = gemm_tc<64, 1>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
+    else if (ff.nt == 128)
+      s = gemm_tc<128, 1>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
+    else
+      s = gemm_tc<256, 1>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
+    if (s != LF_OK) return s;
+  }
   LF_CUDA(cudaGetLastError());
   return LF_OK;
 }
@@ -1943,13 +1970,6 @@ void lf_plan_cache_clear(void) {
   g_bias_ws.clear();
   for (auto& kv : g_bwd_plans) cudaFree(kv.second.d_tiles);
   g_bwd_plans.clear();
-  for (auto& kv : g_gemms) {
-    cublasLtMatmulDescDestroy(kv.second.op);
-    cublasLtMatrixLayoutDestroy(kv.second.a);
-    cublasLtMatrixLayoutDestroy(kv.second.b);
-    cublasLtMatrixLayoutDestroy(kv.second.c);
-  }
-  g_gemms.clear();
   for (auto& kv : g_plans)
     if (kv.second->d_items) cudaFree(kv.second->d_items);
   g_plans.clear();

@@ -152,8 +152,10 @@ struct BtcCfg {
       STG_OWN ? OFF_STG + STG_BYTES : OFF_DS + (DS_TILE > STG_BYTES ? DS_TILE : STG_BYTES);
   static constexpr uint32_t OFF_BAR = OFF_ST + NQB * QB * 16;
   // barriers
+  // B_ST: the dQ read-out threads' staging writes (D arrivals per block)
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQB, B_SP = B_QE + NQB, B_PD = B_SP + 1,
-                       B_DQ = B_PD + 1, B_DF = B_DQ + 1, B_DR = B_DF + 1, NBAR = B_DR + 1;
+                       B_DQ = B_PD + 1, B_DF = B_DQ + 1, B_DR = B_DF + 1, B_ST = B_DR + 1,
+                       NBAR = B_ST + 1;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
   // TMEM columns
   static constexpr uint32_t TM_S = 0, TM_DP = QB, TM_DV = 2 * QB, TM_DK = 2 * QB + D;
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
     mbar_init(BAR(C::B_DQ), 1);
     mbar_init(BAR(C::B_DF), 128);
     mbar_init(BAR(C::B_DR), 1);
+    mbar_init(BAR(C::B_ST), D);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -455,20 +458,22 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
           }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, D);
+        // every read-out thread arrives once per block; a thread that issues
+        // reduce-adds waits (bounded) for all the staging writes
+        mbar_arrive(BAR(C::B_ST));
         const uint32_t stg_a = smem_u32(stg);
         if (!gblock) {
           // the block's query rows are one box of the residue (or natural)
           // view of dq; rows without pairs of the block's class hold zeros,
           // rows past the end are skipped
-          if (row == 0) {
+          if (row == 0 && bwait(BAR(C::B_ST), j & 1, W)) {
 #pragma unroll
             for (int hh = 0; hh < C::NH; ++hh)
               tma_reduce_add_4d(stg_a + hh * (C::QB * 64 * 4), gkeys ? &p.tmDQn : &p.tmDQ[slot],
                                 64 * hh, gkeys ? 0 : r, qs, bh);
             bulk_commit_group();
           }
-        } else if ((qv[row >> 5] >> (row & 31)) & 1u) {
+        } else if (bwait(BAR(C::B_ST), j & 1, W) && ((qv[row >> 5] >> (row & 31)) & 1u)) {
           // gathered global rows: one reduce-add per 64 elements of the row
           const int i = __ldg(p.gidx + gq + row);
 #pragma unroll

@@ -1,13 +1,10 @@
-// Kernels of the Longformer layer forward around the attention kernel
+// The first residual + LayerNorm of the Longformer layer forward
 // ("基于Block-Sparse Attention的Longformer" (block-sparse Longformer), §6
-// "Longformer的整体架构": q, k, v linear maps of x, the attention, residual +
-// LayerNorm, a linear feed-forward map, residual + LayerNorm).  The two linear
-// maps are plain GEMMs (cuBLASLt: bf16 Y for q/k/v, fp32 F for the
-// feed-forward map); these kernels do the memory-bound steps between them,
-// each reading and writing its tensors once:
-//   split_qkv   q, k, v = bf16(Y + b) split into heads [B, H, L, D]
+// "Longformer的整体架构"), between the attention and the feed-forward map:
 //   merge_ln1   x1 = bf16(LN1(x + merge_heads(a)))
-//   ln2         y  = bf16(LN2(x1 + F + b_f))
+// reading and writing its tensors once.  (The q, k, v maps and the
+// feed-forward map with its residual + LayerNorm are tcgen05 GEMMs with fused
+// epilogues, lf_gemm_kernel.cuh.)
 // LayerNorm (over the hidden axis, biased variance):
 //   LN(v) = (v - mean(v)) / sqrt(var(v) + eps) * gamma + beta.
 #pragma once
@@ -20,45 +17,6 @@ namespace lf {
 __device__ __forceinline__ uint32_t layer_pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&t);
-}
-
-// Y: bf16 [M = B*L, 3*hidden] (row = token, columns q | k | v features, head
-// h of each at h*D .. h*D + D-1); bias fp32 [3*hidden].  qkv: bf16, three
-// consecutive [B, H, L, D] tensors: qkv = bf16(Y + bias).  One thread per 8
-// consecutive columns (16 bytes in, 16 bytes out) of ROWS consecutive token
-// rows per CTA: the ROWS loads are issued before the first store, so that
-// each thread keeps several 16-byte reads in flight.
-constexpr int kSplitRows = 4;
-__global__ void lf_layer_split_qkv_kernel(const uint4* __restrict__ Y,
-                                          const float4* __restrict__ bias,
-                                          uint4* __restrict__ qkv, int B, int H, int L, int D) {
-  const int hidden = H * D;
-  const int c8 = threadIdx.x;                    // column group: columns 8*c8 .. 8*c8+7
-  if (c8 >= 3 * hidden / 8) return;
-  const long long M = (long long)B * L;
-  const long long row0 = (long long)blockIdx.x * kSplitRows;
-  uint4 y[kSplitRows];
-#pragma unroll
-  for (int r = 0; r < kSplitRows; ++r)
-    if (row0 + r < M) y[r] = Y[(row0 + r) * (3 * hidden / 8) + c8];
-  const int c = 8 * c8;
-  const int s = c / hidden, hc = c - s * hidden;
-  const int h = hc / D, e = hc - h * D;
-  const float4 b0 = bias[2 * c8], b1 = bias[2 * c8 + 1];
-  auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
-  auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
-#pragma unroll
-  for (int r = 0; r < kSplitRows; ++r) {
-    const long long row = row0 + r;              // token b*L + l
-    if (row >= M) break;
-    const int b = (int)(row / L), l = (int)(row % L);
-    const uint4 o = make_uint4(layer_pack_bf16x2(lo(y[r].x) + b0.x, hi(y[r].x) + b0.y),
-                               layer_pack_bf16x2(lo(y[r].y) + b0.z, hi(y[r].y) + b0.w),
-                               layer_pack_bf16x2(lo(y[r].z) + b1.x, hi(y[r].z) + b1.y),
-                               layer_pack_bf16x2(lo(y[r].w) + b1.z, hi(y[r].w) + b1.w));
-    const size_t dst = ((((size_t)s * B + b) * H + h) * L + l) * D + e;
-    qkv[dst / 8] = o;
-  }
 }
 
 // bf16 <-> fp32 vectors of VW elements (VW = 2, 4 or 8: 4, 8 or 16 bytes)
@@ -182,30 +140,6 @@ __global__ void lf_layer_merge_ln1_kernel(const uint16_t* __restrict__ x,
     for (int i = 0; i < VW; ++i) v[j][i] = xa[i] + aa[i];
   }
   layer_norm_row<VW, NJ>(v, eps, ln1, ln1 + hidden, lane, x1 + (size_t)row * hidden);
-}
-
-// y = bf16(LN2(x1 + F + b_f)), F: fp32 [M, hidden] (the feed-forward GEMM),
-// b_f fp32 [hidden], ln2: gamma then beta.  One warp per row.
-template <int VW, int NJ>
-__global__ void lf_layer_ln2_kernel(const uint16_t* __restrict__ x1, const float* __restrict__ F,
-                                    const float* __restrict__ bf, const float* __restrict__ ln2,
-                                    uint16_t* __restrict__ y, long long M, float eps) {
-  constexpr int hidden = 32 * VW * NJ;
-  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (row >= M) return;
-  float v[NJ][VW];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int c = VW * lane + 32 * VW * j;
-    float xa[VW], fa[VW], ba[VW];
-    layer_load_bf16<VW>(x1 + (size_t)row * hidden + c, xa);
-    layer_load_f32<VW>(F + (size_t)row * hidden + c, fa);
-    layer_load_f32<VW>(bf + c, ba);
-#pragma unroll
-    for (int i = 0; i < VW; ++i) v[j][i] = xa[i] + fa[i] + ba[i];
-  }
-  layer_norm_row<VW, NJ>(v, eps, ln2, ln2 + hidden, lane, y + (size_t)row * hidden);
 }
 
 }  // namespace lf

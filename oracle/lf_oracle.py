@@ -373,10 +373,10 @@ def longformer_layer(x: np.ndarray, w_qkv: np.ndarray, b_qkv: np.ndarray,
     x: [B, L, hidden]; w_qkv: [3*hidden, hidden] (q rows, then k, then v;
     out = x W^T + b as for nn.Linear); b_qkv: [3*hidden]; w_ff: [hidden,
     hidden]; b_ff: [hidden]; ln1, ln2: [2, hidden] or [2*hidden] (gamma, then
-    beta).  With store_bf16 (the library's storage), the q/k/v product x
-    W_qkv^T (before its bias is added), q, k, v, the attention output, x1
-    and the result are rounded to bf16 where the layer stores them;
-    everything else is float64.  ``rows`` (token positions shared by
+    beta).  With store_bf16 (the library's storage), q, k, v (the product
+    x W_qkv^T plus its bias, rounded once), the attention output, x1 and the
+    result are rounded to bf16 where the layer stores them; everything else
+    is float64.  ``rows`` (token positions shared by
     the batch) limits the attention and everything after it to those rows;
     the result is then [B, len(rows), hidden].
     """
@@ -386,7 +386,7 @@ def longformer_layer(x: np.ndarray, w_qkv: np.ndarray, b_qkv: np.ndarray,
     D = hidden // H
     ln1 = np.asarray(ln1, np.float64).reshape(2, hidden)
     ln2 = np.asarray(ln2, np.float64).reshape(2, hidden)
-    y = rnd(rnd(x @ np.asarray(w_qkv, np.float64).T) + np.asarray(b_qkv, np.float64))
+    y = rnd(x @ np.asarray(w_qkv, np.float64).T + np.asarray(b_qkv, np.float64))
     # [B, L, 3, H, D] -> three [B, H, L, D]
     y = y.reshape(B, L, 3, H, D).transpose(2, 0, 3, 1, 4)
     a = attention(y[0], y[1], y[2], w, dilation, G, scale, rows=rows)   # [B, H, R, D]

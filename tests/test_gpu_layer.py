@@ -2,10 +2,10 @@
 
 Primary check: the plain float64 layer (oracle.longformer_layer with
 store_bf16=False), which is pinned to a dense torch layer by the CPU tests.
-The GPU path stores the q/k/v product, q, k, v, the attention output, x1 and
-the result in bf16 (the storage points its header documents) and accumulates
-its products in fp32.  Tolerance against float64, derived from those points
-(bf16 unit roundoff u = 2^-8):
+The GPU path stores q, k, v (product plus bias, rounded once), the attention
+output, x1 and the result in bf16 (the storage points its header documents)
+and accumulates its products in fp32.  Tolerance against float64, derived
+from those points (bf16 unit roundoff u = 2^-8):
   - the final bf16 store: u * |y| per element, allowed on top of the bound;
   - upstream, to first order: the q/k/v roundings (2u relative) move the
     attention output by about 1e-3 rms, the stored attention output and x1

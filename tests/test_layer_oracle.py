@@ -133,6 +133,6 @@ def test_stored_bf16_layer_stays_close_to_float64_layer():
     exact = O.longformer_layer(*args, store_bf16=False, **kw)
     stored = O.longformer_layer(*args, store_bf16=True, **kw)
     assert np.all(O.bf16_round(stored) == stored)
-    # five bf16 stores of values of size ~1 (relative step 2^-8) move the
+    # four bf16 stores of values of size ~1 (relative step 2^-8) move the
     # result by well under 0.1
     assert np.abs(stored - exact).max() < 0.1
