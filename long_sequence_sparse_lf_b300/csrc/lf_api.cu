@@ -231,12 +231,20 @@ struct Pattern {
   int32_t* d_dil = nullptr;
   std::vector<uint8_t> isg;
   std::vector<int32_t> gcnt;   // [L + 1] number of global positions below x
+  // G is a run of consecutive positions G[0] .. G[0] + n_g - 1: the forward
+  // then reads the global rows of q, k, v in place, without a gathered copy
+  bool g_contig = false;
 };
 
 // Global-position tables of a pattern: the flag per position and the prefix
 // count, so that the globals inside any window [a, b) are G[gcnt[a] ..
 // gcnt[b]) without a search.
 void fill_global_tables(Pattern& pt) {
+  // (and at least one query tile of rows from G[0] on, so that no box is
+  // taller than its tensor)
+  pt.g_contig = !pt.G.empty() && pt.L - pt.G[0] >= lf::kBM;
+  for (size_t g = 1; g < pt.G.size(); ++g)
+    if (pt.G[g] != pt.G[0] + (int32_t)g) pt.g_contig = false;
   pt.isg.assign(pt.L, 0);
   for (int g : pt.G) pt.isg[g] = 1;
   pt.gcnt.assign(pt.L + 1, 0);
@@ -633,11 +641,12 @@ lf_status map_residue_f32(DevState* ds, CUtensorMap* m, const void* base, int D,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// 3-D view {D, rows, BH} with a box of `box_rows` rows
+// 3-D view {D, rows, BH} with a box of `box_rows` rows; consecutive bh lie
+// `bh_rows` rows apart (default: rows)
 lf_status map_rows(DevState* ds, CUtensorMap* m, const void* base, int D, int rows, int BH,
-                   int box_rows) {
+                   int box_rows, int bh_rows = 0) {
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)rows, (uint64_t)BH};
-  const uint64_t st[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * rows};
+  const uint64_t st[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * (bh_rows > 0 ? bh_rows : rows)};
   const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
   return encode(ds, m, base, 3, dims, st, box);
 }
@@ -742,9 +751,23 @@ lf_status build_params(DevState* ds, const Plan& plan, const Pattern& pattern, c
   if (n_g > 0) {
     if ((s = map_rows(ds, &P.tmKp, kb, D, L, BH, lf::kBN)) != LF_OK) return s;
     if ((s = map_rows(ds, &P.tmVp, vb, D, L, BH, lf::kBN)) != LF_OK) return s;
-    if ((s = map_rows(ds, &P.tmQg, qg, D, pl->NGQ, BH, lf::kBM)) != LF_OK) return s;
-    if ((s = map_rows(ds, &P.tmKg, kg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
-    if ((s = map_rows(ds, &P.tmVg, vg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+    if (pat->g_contig) {
+      // the global rows in place: rows G[0].. of each head (past n_g the
+      // kernel masks the keys and drops the query rows; past L the loads
+      // read zeros)
+      const size_t g0 = (size_t)pat->G[0] * D;
+      const int rows = L - pat->G[0];
+      const uint16_t* q0 = static_cast<const uint16_t*>(qb) + g0;
+      const uint16_t* k0 = static_cast<const uint16_t*>(kb) + g0;
+      const uint16_t* v0 = static_cast<const uint16_t*>(vb) + g0;
+      if ((s = map_rows(ds, &P.tmQg, q0, D, rows, BH, lf::kBM, L)) != LF_OK) return s;
+      if ((s = map_rows(ds, &P.tmKg, k0, D, rows, BH, pl->NGB, L)) != LF_OK) return s;
+      if ((s = map_rows(ds, &P.tmVg, v0, D, rows, BH, pl->NGB, L)) != LF_OK) return s;
+    } else {
+      if ((s = map_rows(ds, &P.tmQg, qg, D, pl->NGQ, BH, lf::kBM)) != LF_OK) return s;
+      if ((s = map_rows(ds, &P.tmKg, kg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+      if ((s = map_rows(ds, &P.tmVg, vg, D, pl->NGQ, BH, pl->NGB)) != LF_OK) return s;
+    }
   }
   P.items = pl->d_items;
   P.cta_begin = pl->d_cta;
@@ -863,7 +886,7 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
   }
   const MainParams& prm = *cached;
 
-  if (n_g > 0) {
+  if (n_g > 0 && !pat->g_contig) {
     const size_t total = (size_t)BH * pl->NGQ * (D / 8);
     const int threads = 256;
     const int blocks = (int)std::max<size_t>(1, std::min<size_t>((total + threads - 1) / threads,
