@@ -280,8 +280,7 @@ LF_API lf_status lf_attn_fwd_host(const void* q, const void* k, const void* v, v
  * without global tokens need only the work list and the global flags.
  *
  *   - The first call on a device looks up the array's device address there
- *     (one cudaGetSymbolAddress); make that first call before any stream
- *     capture.
+ *     (one cudaGetSymbolAddress).
  *   - Every call uses the same array and overwrites what the previous call
  *     left in it; nothing in it needs to start at zero.  Calls whose work
  *     overlaps on the GPU (other streams, other threads) race on it: order
