@@ -63,9 +63,12 @@ __global__ void lf_gather_globals_kernel(const uint4* __restrict__ q, const uint
 // One warp per (bh, g < n_g): merges the key-chunk partials of a global row,
 //   m = max_c m_c,  l = sum_c l_c 2^(m_c - m),  o = sum_c o_c 2^(m_c - m) / l
 // (m in log2 units), and writes the row of the output at position G[g] (and
-// its log-sum-exp (m + log2 l) ln 2, if lse is given).  Lane c reads chunk c's (m_c, l_c) (32 chunks at a time), the weights are
-// shared by shuffles, and every O load of the chunk loop is independent of
-// the others, so the warp has all its loads in flight at once.
+// its log-sum-exp (m + log2 l) ln 2, if lse is given).  The chunks go in
+// groups of up to 32: lane c of a group reads chunk c's (m_c, l_c), and the
+// group's O rows (D / 32 values per lane and chunk, up to kCombineBatch
+// chunks at a time) are loaded before any of the arithmetic, so that the
+// warp waits for memory once per batch rather than once per step.
+constexpr int kCombineBatch = 16;
 template <int D>
 __global__ void lf_combine_globals_kernel(const float* __restrict__ part_o,
                                           const float* __restrict__ part_ml,
@@ -74,6 +77,7 @@ __global__ void lf_combine_globals_kernel(const float* __restrict__ part_o,
                                           float* __restrict__ lse) {
   constexpr int PER = D / 32;
   const float NEG_INF = -__int_as_float(0x7f800000);
+  const unsigned FULL = 0xffffffffu;
   const int warps_per_block = blockDim.x / 32;
   const long long wid = (long long)blockIdx.x * warps_per_block + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -81,38 +85,65 @@ __global__ void lf_combine_globals_kernel(const float* __restrict__ part_o,
   const int g = (int)(wid % n_g);
   const long long bh = wid / n_g;
   const size_t base = ((size_t)bh * NGQ + g) * n_chunks;
-  float m = NEG_INF;
-  for (int c0 = 0; c0 < n_chunks; c0 += 32)
-    if (c0 + lane < n_chunks) m = fmaxf(m, part_ml[(base + c0 + lane) * 2]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float l = 0.f;
+  const int grow = __ldg(gidx + g);
+  // running (m, l, o) of the row over the groups merged so far
+  float m = NEG_INF, l = 0.f;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-    // this lane's chunk: its weight 2^(m_c - m) (0 for an empty chunk)
-    float wgt = 0.f, lc = 0.f;
-    if (c0 + lane < n_chunks) {
-      const float mc = part_ml[(base + c0 + lane) * 2];
-      lc = part_ml[(base + c0 + lane) * 2 + 1];
-      wgt = (mc == m) ? 1.f : exp2f(mc - m);
-    }
-    l += wgt * lc;
     const int nc = min(32, n_chunks - c0);
-#pragma unroll 4
-    for (int c = 0; c < nc; ++c) {
-      const float wc = __shfl_sync(0xffffffffu, wgt, c);
-      const float* src = part_o + (base + c0 + c) * D;
+    // this group: each lane's chunk statistics, and the first batch of O rows
+    float mc = NEG_INF, lc = 0.f;
+    if (lane < nc) {
+      const float2 ml = *reinterpret_cast<const float2*>(part_ml + (base + c0 + lane) * 2);
+      mc = ml.x;
+      lc = ml.y;
+    }
+    float ob[kCombineBatch][PER];
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = fmaf(src[lane + 32 * e], wc, acc[e]);
+    for (int c = 0; c < kCombineBatch; ++c)
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        ob[c][e] = c < nc ? part_o[(base + c0 + c) * D + lane + 32 * e] : 0.f;
+    float mg = mc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(FULL, mg, o));
+    const float mn = fmaxf(m, mg);
+    // rescale what has been merged so far, then add this group
+    const float sc = (m == NEG_INF) ? 0.f : ((m == mn) ? 1.f : exp2f(m - mn));
+    l *= sc;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] *= sc;
+    m = mn;
+    const float wgt = (lane < nc && mc != NEG_INF) ? ((mc == m) ? 1.f : exp2f(mc - m)) : 0.f;
+    float lw = wgt * lc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
+    l += lw;
+#pragma unroll
+    for (int c = 0; c < kCombineBatch; ++c) {
+      const float wc = __shfl_sync(FULL, wgt, c);
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(ob[c][e], wc, acc[e]);
+    }
+    for (int cb = kCombineBatch; cb < nc; cb += kCombineBatch) {
+#pragma unroll
+      for (int c = 0; c < kCombineBatch; ++c)
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          ob[c][e] = cb + c < nc ? part_o[(base + c0 + cb + c) * D + lane + 32 * e] : 0.f;
+#pragma unroll
+      for (int c = 0; c < kCombineBatch; ++c) {
+        const float wc = __shfl_sync(FULL, wgt, (cb + c) & 31);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(ob[c][e], cb + c < nc ? wc : 0.f, acc[e]);
+      }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  const size_t orow = ((size_t)bh * L + gidx[g]) * D;
-  if (lse != nullptr && lane == 0) lse[(size_t)bh * L + gidx[g]] = (m + __log2f(l)) * 0.69314718f;
+  const size_t orow = ((size_t)bh * L + grow) * D;
+  if (lse != nullptr && lane == 0) lse[(size_t)bh * L + grow] = (m + __log2f(l)) * 0.69314718f;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
     const float val = acc[e] * inv;
