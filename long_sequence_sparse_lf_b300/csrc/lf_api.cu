@@ -1504,7 +1504,14 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   const size_t off_sn = off_sg + align_up((size_t)BH * NGQ * 16 + 16, 256);
   const size_t off_g = off_sn + align_up((size_t)BH * (L + lf::kBtcQPad) * 16, 256);
   const size_t g_elems = (size_t)BH * NGQ * D;
-  const size_t need = off_g + align_up(4 * g_elems * 2 + 16, 256);
+  // few global tokens: the prep kernel does the global-key pairs and sets
+  // dq; their dk, dv sums go to dkg, dvg [BH][n_g][D] fp32
+  // (and L at least one warp run of rows, so that a block's rows span at
+  // most two heads)
+  const bool fused_gk = n_g <= lf::kBwdPrepGlobals && L >= 16;
+  const size_t gk_elems = fused_gk ? (size_t)BH * n_g * D : 0;
+  const size_t off_gk = off_g + align_up(4 * g_elems * 2 + 16, 256);
+  const size_t need = off_gk + align_up(2 * gk_elems * 4 + 16, 256);
   uint8_t* ws = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1525,10 +1532,18 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
   uint16_t* og = qg + g_elems;
   uint16_t* kg = og + g_elems;
   uint16_t* vg = kg + g_elems;
+  float* dkg = reinterpret_cast<float*>(ws + off_gk);
+  float* dvg = dkg + gk_elems;
   const size_t grad_bytes = (size_t)rows * D * 4;
-  // dq is accumulated by every tile; dk and dv are stored by the band tiles
-  // (every key row has one) before the global-key tiles add to them
-  LF_CUDA(cudaMemsetAsync(dq, 0, grad_bytes, stream));
+  // dq is accumulated by every tile: zeroed first, or set by the prep kernel
+  // (fused_gk); dk and dv are stored by the band tiles (every key row has
+  // one), with the global-key pairs' sums added either there (fused_gk) or
+  // by the global-key tiles afterwards
+  if (fused_gk) {
+    if (gk_elems > 0) LF_CUDA(cudaMemsetAsync(dkg, 0, 2 * gk_elems * 4, stream));
+  } else {
+    LF_CUDA(cudaMemsetAsync(dq, 0, grad_bytes, stream));
+  }
 
   // kernel parameters: residue views of k, v, q, dout per dilation value,
   // undilated views of q and dout, and the gathered global rows
@@ -1553,6 +1568,12 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     if ((s = map_rows(ds, &T.tmVg, vg, D, NGQ, BH, lf::kBtcKeys)) != LF_OK) return s;
   }
   T.tiles = bp->d_tiles;
+  if (fused_gk && n_g > 0) {
+    T.dkg = dkg;
+    T.dvg = dvg;
+    T.is_glob = pat->d_isg;
+    T.gcnt = pat->d_gcnt;
+  }
   T.stats = stats;
   T.stats_bh = stats_bh;
   T.stats_g = stats_g;
@@ -1590,16 +1611,35 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
         return (int)std::max<long long>(
             1, std::min<long long>((units + pthreads - 1) / pthreads, (long long)ds->num_sms * 16));
       };
-      const int nb0 = nblk(rows * (DD / 8)), nb1 = nblk((long long)BH * NGQ * (DD / 8));
+      // the rows: per thread (plain), or per run of 4 steps a warp
+      // (fused_gk)
+      // fused_gk: a contiguous range of rows per block, at most L (two
+      // heads), a multiple of the warps' 4-step runs
+      const long long run_rows = 4 * (32 / (DD / 8));
+      const long long rpb = std::max<long long>(
+          run_rows, std::min<long long>(ceil_div(rows, (long long)ds->num_sms * 2), L) / run_rows *
+                        run_rows);
+      const int nb0 = fused_gk ? (int)ceil_div(rows, rpb) : nblk(rows * (DD / 8));
+      const int nb1 = nblk((long long)BH * NGQ * (DD / 8));
       const int nb2 = nblk((long long)BH * 2 * lf::kBtcQPad);
       traced("bwd_prep", stream, [&] {
-        lf::lf_bwd_tc_prep_kernel<DD><<<nb0 + nb1 + nb2, pthreads, 0, stream>>>(
-            reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
-            reinterpret_cast<const uint4*>(v), reinterpret_cast<const uint4*>(out),
-            reinterpret_cast<const uint4*>(dout), lse, pat->d_isg, pat->d_dil, pat->d_G, n_g,
-            NGQ, H, L, stats_bh, BH, stats, stats_n, stats_g, reinterpret_cast<uint4*>(qg),
-            reinterpret_cast<uint4*>(og), reinterpret_cast<uint4*>(kg),
-            reinterpret_cast<uint4*>(vg), nb0, nb1);
+        auto args = [&](auto kern) {
+          kern<<<nb0 + nb1 + nb2, pthreads, 0, stream>>>(
+              reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
+              reinterpret_cast<const uint4*>(v), reinterpret_cast<const uint4*>(out),
+              reinterpret_cast<const uint4*>(dout), lse, pat->d_isg, pat->d_dil, pat->d_G, n_g,
+              NGQ, H, L, stats_bh, BH, stats, stats_n, stats_g, reinterpret_cast<uint4*>(qg),
+              reinterpret_cast<uint4*>(og), reinterpret_cast<uint4*>(kg),
+              reinterpret_cast<uint4*>(vg), nb0, nb1, dq, dkg, dvg, w, scale, (int)rpb);
+        };
+        if (!fused_gk)
+          args(lf::lf_bwd_tc_prep_kernel<DD, 0>);
+        else if (n_g <= 1)
+          args(lf::lf_bwd_tc_prep_kernel<DD, 1>);
+        else if (n_g <= 2)
+          args(lf::lf_bwd_tc_prep_kernel<DD, 2>);
+        else
+          args(lf::lf_bwd_tc_prep_kernel<DD, 4>);
       });
     }
     if (bp->n_band > 0)
@@ -1607,7 +1647,7 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
         lf::lf_bwd_band_tc_kernel<DD><<<(unsigned)bp->n_band, CF::THREADS, CF::SMEM_BYTES,
                                         stream>>>(T);
       });
-    if (bp->n_gkey > 0) {
+    if (bp->n_gkey > 0 && !fused_gk) {
       lf::BwdTcParams T2 = T;
       T2.tiles = bp->d_tiles + bp->n_band;
       traced("bwd_tc_global_keys", stream, [&] {

@@ -73,6 +73,9 @@
 namespace lf {
 
 constexpr int kBtcKeys = 128;   // keys per tile (TMEM lanes)
+// Global tokens up to which the prep kernel does the global-key pairs (on the
+// CUDA cores, fp32), and the rows a warp takes at a time there
+constexpr int kBwdPrepGlobals = 4;
 constexpr int kBtcQPad = 128;   // padding of each residue class of the statistics
 
 // A unit of the backward kernel.
@@ -106,7 +109,14 @@ struct BwdTcParams {
   const float4* stats_n;           // [B*H][L + 128]: natural order
   const int32_t* gidx;             // [n_g] sorted global positions
   int n_g, NGQ;
-  float* dq;                       // [B*H, L, D] fp32, accumulated (zeroed first)
+  float* dq;                       // [B*H, L, D] fp32, accumulated (zeroed or set first)
+  // global-key pairs done by the prep kernel (few global tokens): their dk,
+  // dv sums [B*H][n_g][D], which the band tiles add to the global keys' rows;
+  // null when global-key tiles run instead
+  const float* dkg;
+  const float* dvg;
+  const uint8_t* is_glob;          // [L]
+  const int32_t* gcnt;             // [L + 1] global positions below x
   float* dk;                       // [B*H, L, D] fp32, stored
   float* dv;
   int L, w;
@@ -503,6 +513,15 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
         tmem_ld32(tl + C::TM_DV + c0, vr);
         tmem_ld32(tl + C::TM_DK + c0, kr);
         if (kvalid && !gkeys) {
+          if (p.dkg != nullptr && p.is_glob[kpos]) {
+            // a global key: add its global-key pairs' sums (prep kernel)
+            const size_t gb = (static_cast<size_t>(bh) * p.n_g + p.gcnt[kpos]) * D + c0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              vr[e] = __float_as_uint(__uint_as_float(vr[e]) + p.dvg[gb + e]);
+              kr[e] = __float_as_uint(__uint_as_float(kr[e]) + p.dkg[gb + e] / p.scale);
+            }
+          }
           float4* dvp = reinterpret_cast<float4*>(p.dv + base + c0);
           float4* dkp = reinterpret_cast<float4*>(p.dk + base + c0);
 #pragma unroll
@@ -545,7 +564,24 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
 // with delta_i = dout_i . out_i (bf16 rows, fp32 sum).  A row is read by
 // D / 8 threads, 16 bytes each.  The first nb0 blocks take the rows, the next
 // nb1 the gathered global rows, the rest the padding entries.
-template <int D>
+//
+// GK (at most kBwdPrepGlobals global tokens): the global-key pairs (j in G,
+// i not global, j not in band(i)) are done here too, in fp32 on the CUDA
+// cores, instead of by global-key tiles:
+//   s = q_i.k_j, p = 2^(s scale log2e - lse_i log2e), ds = p (dout_i.v_j - delta_i)
+//   dq_i  = scale sum_j ds k_j          (written: dq's initial value, so dq
+//                                         needs no zeroing; the band tiles add)
+//   dkg_j += scale ds q_i, dvg_j += p dout_i   (fp32 [B*H][n_g][D], zeroed
+//                                         first; the band tiles add them to the
+//                                         global keys' dk, dv rows)
+// A block then takes a contiguous range of rows (`rows_per_block`, at most L,
+// so at most two heads), its warps runs of 4 steps of 32 / (D / 8)
+// consecutive rows whose loads they issue together.  A row group keeps
+// partial dkg, dvg sums in registers and adds them to the block's two head
+// slots in shared memory when its head changes; the block adds its slots to
+// dkg, dvg at the end.  GKN: the register arrays' size in global keys
+// (n_g <= GKN), 0 for the plain pass.
+template <int D, int GKN = 0>
 __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
                                       const uint4* __restrict__ v, const uint4* __restrict__ out,
                                       const uint4* __restrict__ dout,
@@ -557,7 +593,11 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
                                       float4* __restrict__ stats, float4* __restrict__ stats_n,
                                       float4* __restrict__ stats_g, uint4* __restrict__ qg,
                                       uint4* __restrict__ og, uint4* __restrict__ kg,
-                                      uint4* __restrict__ vg, int nb0, int nb1) {
+                                      uint4* __restrict__ vg, int nb0, int nb1,
+                                      float* __restrict__ dq = nullptr,
+                                      float* __restrict__ dkg = nullptr,
+                                      float* __restrict__ dvg = nullptr, int w = 0,
+                                      float scale = 0.f, int rows_per_block = 0) {
   constexpr int G = D / 8;   // threads per row (a divisor of 32)
   const float INF = __int_as_float(0x7f800000);
   const float LOG2E = 1.4426950408889634f;
@@ -585,7 +625,8 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
     for (int o = G / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     return s;
   };
-  if (part == 0) {
+  constexpr bool GK = GKN > 0;
+  if (part == 0 && !GK) {
     // B*H*L < 2^31 (the entry point checks it): 32-bit row arithmetic
     const int rows = (int)(BH * L);
     for (long long w0 = warp0; w0 * (32 / G) < rows; w0 += wstride) {
@@ -601,6 +642,150 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
                                     : make_float4(-lse[row] * LOG2E, -dl, 0.f, 0.f);
         stats[(long long)bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
         stats_n[(long long)bh * (L + kBtcQPad) + i] = o;
+      }
+    }
+  } else if (part == 0) {
+    constexpr int NGM = GK ? GKN : 1;
+    constexpr int RPI = 32 / G;                      // rows per warp step
+    constexpr int NS = 4;                            // steps per run
+    constexpr int RUN = NS * RPI;
+    const int rows = (int)(BH * L);
+    const float sl2 = scale * LOG2E;
+    // this lane's 8 elements (of D) of each global key row, per head: loaded
+    // when the group's head changes
+    float kj[NGM][8], vj[NGM][8], dkp[NGM][8], dvp[NGM][8];
+    int cur_bh = -1;
+    // the block's rows and its head slots [2][NGM][2][D]
+    const int r_begin = pb * rows_per_block;
+    const int r_end = min(rows, r_begin + rows_per_block);
+    const int bh_first = r_begin / L;
+    __shared__ float acc_s[2 * NGM * 2 * D];
+    for (int x = threadIdx.x; x < 2 * NGM * 2 * D; x += blockDim.x) acc_s[x] = 0.f;
+    __syncthreads();
+    auto flush = [&]() {
+      if (cur_bh < 0) return;
+      float* slot = acc_s + (cur_bh - bh_first) * (NGM * 2 * D);
+#pragma unroll
+      for (int j = 0; j < NGM; ++j) {
+        if (j >= n_g) break;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          atomicAdd(slot + (j * 2 + 0) * D + 8 * sub + e, dkp[j][e]);
+          atomicAdd(slot + (j * 2 + 1) * D + 8 * sub + e, dvp[j][e]);
+        }
+      }
+    };
+    auto unpack8 = [](const uint4 u, float (&f)[8]) {
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        f[2 * e] = __uint_as_float(w4[e] << 16);
+        f[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+      }
+    };
+    const int wib = threadIdx.x / 32, nwb = blockDim.x / 32;
+    for (int run0 = r_begin + wib * RUN; run0 < r_end; run0 += nwb * RUN) {
+      // the run's loads first, all in flight together
+      uint4 ou[NS], du[NS], qu[NS];
+#pragma unroll
+      for (int st = 0; st < NS; ++st) {
+        const int row = run0 + st * RPI + lane / G;
+        const bool ok = row < r_end;
+        ou[st] = ok ? out[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
+        du[st] = ok ? dout[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
+        qu[st] = ok ? q[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int st = 0; st < NS; ++st) {
+        const int row = run0 + st * RPI + lane / G;
+        const bool ok = row < r_end;
+        const int rr = ok ? row : 0;
+        const int bh = rr / L, i = rr - bh * L;
+        // all lanes take part in the group reductions below
+        float of[8], df[8], qf[8];
+        unpack8(ou[st], of);
+        unpack8(du[st], df);
+        unpack8(qu[st], qf);
+        float dl = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dl = fmaf(of[e], df[e], dl);
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+        if (ok && bh != cur_bh) {
+          flush();
+          cur_bh = bh;
+#pragma unroll
+          for (int j = 0; j < NGM; ++j) {
+            const size_t gr = (static_cast<size_t>(bh) * L + (j < n_g ? gidx[j] : 0)) * G + sub;
+            float t8[8];
+            unpack8(j < n_g ? k[gr] : make_uint4(0, 0, 0, 0), t8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kj[j][e] = t8[e];
+            unpack8(j < n_g ? v[gr] : make_uint4(0, 0, 0, 0), t8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              vj[j][e] = t8[e];
+              dkp[j][e] = 0.f;
+              dvp[j][e] = 0.f;
+            }
+          }
+        }
+        const bool glob = ok && is_glob[i];
+        const int d = head_dil[bh % H];
+        const float nl = ok ? -lse[rr] * LOG2E : 0.f;
+        float dqa[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dqa[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NGM; ++j) {
+          if (j >= n_g) break;
+          float sd = 0.f, pd = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sd = fmaf(qf[e], kj[j][e], sd);
+            pd = fmaf(df[e], vj[j][e], pd);
+          }
+#pragma unroll
+          for (int o = G / 2; o > 0; o >>= 1) {
+            sd += __shfl_xor_sync(0xffffffffu, sd, o);
+            pd += __shfl_xor_sync(0xffffffffu, pd, o);
+          }
+          const int diff = gidx[j] - i;
+          const bool in_band = (diff <= d * w && diff >= -d * w && diff % d == 0);
+          if (ok && !glob && !in_band) {
+            const float pp = ex2_approx(fmaf(sd, sl2, nl));
+            const float ds = pp * (pd - dl);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              dqa[e] = fmaf(scale * ds, kj[j][e], dqa[e]);
+              dkp[j][e] = fmaf(scale * ds, qf[e], dkp[j][e]);
+              dvp[j][e] = fmaf(pp, df[e], dvp[j][e]);
+            }
+          }
+        }
+        if (ok) {
+          float4* dqr = reinterpret_cast<float4*>(dq + (size_t)rr * D + 8 * sub);
+          dqr[0] = make_float4(dqa[0], dqa[1], dqa[2], dqa[3]);
+          dqr[1] = make_float4(dqa[4], dqa[5], dqa[6], dqa[7]);
+          if (sub == 0) {
+            const int r = i % d, t = i / d;
+            const float4 o = glob ? make_float4(-INF, 0.f, 0.f, 0.f) : make_float4(nl, -dl, 0.f, 0.f);
+            stats[(long long)bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
+            stats_n[(long long)bh * (L + kBtcQPad) + i] = o;
+          }
+        }
+      }
+    }
+    flush();
+    __syncthreads();
+    // the block's head slots to dkg, dvg
+    for (int x = threadIdx.x; x < 2 * NGM * 2 * D; x += blockDim.x) {
+      const int sl = x / (NGM * 2 * D), rem = x - sl * (NGM * 2 * D);
+      const int j = rem / (2 * D), kv = (rem / D) & 1, e = rem % D;
+      const int bh = bh_first + sl;
+      if (j < n_g && bh < BH && bh * L < r_end) {
+        float* dst = (kv == 0 ? dkg : dvg) + (static_cast<size_t>(bh) * n_g + j) * D + e;
+        atomicAdd(dst, acc_s[x]);
       }
     }
   } else if (part == 1) {
