@@ -1201,21 +1201,21 @@ FfShape ff_shape(int hidden) {
   return {};
 }
 
-bool g_gemm_smem_set[64][6] = {};
+bool g_gemm_smem_set[64][8] = {};
 
 // C = A B^T through lf_gemm_tc_kernel<NT, EPI>: A [M, K], B [N, K] bf16
 // row-major (the caller sets P's output maps); grid (N / NT, row tiles):
 // B * ceil(L / 128) tiles of one batch element each for EPI 0, ceil(M / 128)
 // for EPI 1, with clusters of `cluster` CTAs along the columns.
-template <int NT, int EPI>
+template <int NT, int EPI, int MH = 1>
 lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const void* Bw,
                   long long M, int N, int K, int cluster, cudaStream_t stream, const char* name) {
-  using CF = lf::GemmCfg<NT>;
+  using CF = lf::GemmCfg<NT, MH>;
   lf_status s;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t st[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {(uint32_t)lf::kGemmBK, (uint32_t)lf::kGemmBM};
+    const uint32_t box[2] = {(uint32_t)lf::kGemmBK, (uint32_t)CF::BM};
     if ((s = encode(ds, &P.tmA, A, 2, dims, st, box)) != LF_OK) return s;
   }
   {
@@ -1230,9 +1230,9 @@ lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const
   P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    const int slot = (NT == 64 ? 0 : NT == 128 ? 1 : 2) * 2 + EPI;
+    const int slot = MH == 2 ? 6 : (NT == 64 ? 0 : NT == 128 ? 1 : 2) * 2 + EPI;
     if (dev < 64 && !g_gemm_smem_set[dev][slot]) {
-      LF_CUDA(cudaFuncSetAttribute(lf::lf_gemm_tc_kernel<NT, EPI>,
+      LF_CUDA(cudaFuncSetAttribute(lf::lf_gemm_tc_kernel<NT, EPI, MH>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)CF::SMEM_BYTES));
       g_gemm_smem_set[dev][slot] = true;
@@ -1240,8 +1240,8 @@ lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const
   }
   cudaLaunchConfig_t cfg = {};
   const long long row_tiles = (EPI == 0)
-                                  ? (long long)P.B * ((P.L + lf::kGemmBM - 1) / lf::kGemmBM)
-                                  : (M + lf::kGemmBM - 1) / lf::kGemmBM;
+                                  ? (long long)P.B * ((P.L + CF::BM - 1) / CF::BM)
+                                  : (M + CF::BM - 1) / CF::BM;
   cfg.gridDim = dim3((unsigned)(N / NT), (unsigned)row_tiles, 1);
   cfg.blockDim = dim3(CF::THREADS, 1, 1);
   cfg.dynamicSmemBytes = CF::SMEM_BYTES;
@@ -1256,7 +1256,7 @@ lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const
     cfg.numAttrs = 1;
   }
   cudaError_t e = cudaSuccess;
-  traced(name, stream, [&] { e = cudaLaunchKernelEx(&cfg, lf::lf_gemm_tc_kernel<NT, EPI>, P); });
+  traced(name, stream, [&] { e = cudaLaunchKernelEx(&cfg, lf::lf_gemm_tc_kernel<NT, EPI, MH>, P); });
   if (e != cudaSuccess) return fail(LF_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(e));
   return LF_OK;
 }
@@ -1320,13 +1320,19 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
     P.H = H;
     P.L = L;
     P.D = D;
+    // 256 x 256 tiles (two accumulators) where the width allows: half the
+    // L2 traffic per product of 128 x 128 tiles
+    const bool wide = (3 * hidden) % 256 == 0;
     for (int part = 0; part < 3; ++part) {
       const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L, (uint64_t)B * H};
       const uint64_t st[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * L};
-      const uint32_t box[3] = {64, (uint32_t)lf::kGemmBM, 1};
+      const uint32_t box[3] = {64, (uint32_t)(wide ? 2 * lf::kGemmBM : lf::kGemmBM), 1};
       if ((s = encode(ds, &P.tmO[part], qkv + part * act, 3, dims, st, box)) != LF_OK) return s;
     }
-    if ((3 * hidden) % 128 == 0)
+    if (wide)
+      s = gemm_tc<256, 0, 2>(ds, dev, P, x, w_qkv, M, 3 * hidden, hidden, 1, stream,
+                             "layer_gemm_qkv");
+    else if ((3 * hidden) % 128 == 0)
       s = gemm_tc<128, 0>(ds, dev, P, x, w_qkv, M, 3 * hidden, hidden, 1, stream, "layer_gemm_qkv");
     else
       s = gemm_tc<64, 0>(ds, dev, P, x, w_qkv, M, 3 * hidden, hidden, 1, stream, "layer_gemm_qkv");

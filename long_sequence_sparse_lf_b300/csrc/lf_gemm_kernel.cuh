@@ -40,11 +40,15 @@ constexpr int kGemmBM = 128;          // rows per tile (TMEM lanes)
 constexpr int kGemmBK = 64;           // K per stage: one 128-byte swizzle atom of bf16
 constexpr int kGemmMaxCluster = 8;    // CTAs sharing a row in the LayerNorm epilogue
 
-template <int NT>
+// NT: columns per tile; MH: 128-row halves per tile (MH = 2: two M = 128
+// accumulators side by side in TMEM, sharing each B k-block)
+template <int NT, int MH = 1>
 struct GemmCfg {
   static_assert(NT == 64 || NT == 128 || NT == 256, "tile width");
-  static constexpr int STAGES = (NT == 256) ? 4 : (NT == 128 ? 3 : 4);
-  static constexpr uint32_t A_BYTES = kGemmBM * 128;   // 128 rows x 64 bf16
+  static_assert(MH == 1 || MH == 2, "tile height");
+  static constexpr int BM = kGemmBM * MH;              // rows per tile
+  static constexpr int STAGES = (MH == 2) ? 3 : ((NT == 256) ? 4 : (NT == 128 ? 3 : 4));
+  static constexpr uint32_t A_BYTES = BM * 128;        // BM rows x 64 bf16
   static constexpr uint32_t B_BYTES = NT * 128;        // NT rows x 64 bf16
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr uint32_t OFF_RED = STAGES * STAGE;  // [2][kGemmMaxCluster][128] fp32
@@ -55,10 +59,10 @@ struct GemmCfg {
   static constexpr int B_FULL = 0, B_EMPTY = STAGES, B_ACC = 2 * STAGES, B_DR = B_ACC + 1,
                        B_VEC = B_DR + 1, B_STG = B_VEC + 1, NBAR = B_STG + 1;
   // the output staging rows ([128][NT] bf16) fit in the consumed stages
-  static_assert(kGemmBM * NT * 2 <= STAGES * STAGE, "staging rows");
+  static_assert(BM * NT * 2 <= STAGES * STAGE, "staging rows");
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
   static constexpr int CTAS = (2 * SMEM_BYTES <= 228u * 1024u) ? 2 : 1;
-  static constexpr uint32_t TM_COLS = NT;              // a power of two >= 32
+  static constexpr uint32_t TM_COLS = NT * MH;         // a power of two >= 32
   static constexpr int THREADS = 192;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory of one CTA");
 };
@@ -131,10 +135,12 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t ran
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-template <int NT, int EPI>
-__global__ void __launch_bounds__(192, GemmCfg<NT>::CTAS)
+template <int NT, int EPI, int MH = 1>
+__global__ void __launch_bounds__(192, GemmCfg<NT, MH>::CTAS)
     lf_gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<NT>;
+  using C = GemmCfg<NT, MH>;
+  static_assert(EPI == 0 || MH == 1, "the LayerNorm epilogue takes 128-row tiles");
+  constexpr int BM = C::BM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -151,12 +157,12 @@ __global__ void __launch_bounds__(192, GemmCfg<NT>::CTAS)
   // EPI 0: row tiles per batch element (tile = 128 positions l0.. of one b,
   // so that its rows are one box of the [B, H, L, D] outputs); EPI 1: rows
   // m0.. of [M, hidden]
-  const int tiles_b = (p.L + kGemmBM - 1) / kGemmBM;
+  const int tiles_b = (p.L + BM - 1) / BM;
   const int b_t = (EPI == 0) ? static_cast<int>(blockIdx.y) / tiles_b : 0;
-  const int l0 = (EPI == 0) ? (static_cast<int>(blockIdx.y) - b_t * tiles_b) * kGemmBM : 0;
-  const int m0 = (EPI == 0) ? b_t * p.L + l0 : static_cast<int>(blockIdx.y) * kGemmBM;
+  const int l0 = (EPI == 0) ? (static_cast<int>(blockIdx.y) - b_t * tiles_b) * BM : 0;
+  const int m0 = (EPI == 0) ? b_t * p.L + l0 : static_cast<int>(blockIdx.y) * BM;
   // rows of the tile that are outputs
-  const int rows_out = (EPI == 0) ? min(kGemmBM, p.L - l0) : min(kGemmBM, p.M - m0);
+  const int rows_out = (EPI == 0) ? min(BM, p.L - l0) : min(BM, p.M - m0);
   const int KB = p.K / kGemmBK;
 
   if (threadIdx.x == 0) {
@@ -220,9 +226,11 @@ __global__ void __launch_bounds__(192, GemmCfg<NT>::CTAS)
         const uint32_t st = sb + s * C::STAGE;
 #pragma unroll
         for (int kk = 0; kk < kGemmBK / 16; ++kk)
-          mma_ss(tmem, sdesc_sw128(st + kk * 32u, 16, 1024),
-                 sdesc_sw128(st + C::A_BYTES + kk * 32u, 16, 1024), idesc,
-                 (kb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int h = 0; h < MH; ++h)
+            mma_ss(tmem + h * NT, sdesc_sw128(st + h * (kGemmBM * 128) + kk * 32u, 16, 1024),
+                   sdesc_sw128(st + C::A_BYTES + kk * 32u, 16, 1024), idesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
         mma_commit(BAR(C::B_EMPTY + s));
       }
       if (iok) {
@@ -262,9 +270,10 @@ __global__ void __launch_bounds__(192, GemmCfg<NT>::CTAS)
       // row r at chunk c ^ (r & 7) (the tensor maps' 128-byte swizzle)
       uint8_t* stg = smem;
 #pragma unroll 1
-      for (int c0 = 0; c0 < (ok ? NT : 0); c0 += 32) {
+      for (int hc = 0; hc < (ok ? MH * NT : 0); hc += 32) {
+        const int h = hc / NT, c0 = hc - h * NT;   // row half, column
         uint32_t r[32];
-        tmem_ld32(tl + c0, r);
+        tmem_ld32(tl + hc, r);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -273,11 +282,12 @@ __global__ void __launch_bounds__(192, GemmCfg<NT>::CTAS)
           pk[e / 2 + 1] =
               pack_bf16x2(__uint_as_float(r[e + 2]) + bv.z, __uint_as_float(r[e + 3]) + bv.w);
         }
-        uint8_t* rowp = stg + (c0 / 64) * (kGemmBM * 128) + row * 128;
+        const int rh = row + kGemmBM * h;
+        uint8_t* rowp = stg + (c0 / 64) * (BM * 128) + rh * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int chunk = (c0 & 63) / 8 + q;
-          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (rh & 7)) << 4)) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(192, GemmCfg<NT>::CTAS)
           const int n = n0 + 64 * cb;
           const int part = n / p.hidden, hc = n - part * p.hidden;
           const int hh = hc / p.D, dcol = hc - hh * p.D;
-          tma_store_3d(&p.tmO[part], smem_u32(stg) + cb * (kGemmBM * 128), dcol, l0,
+          tma_store_3d(&p.tmO[part], smem_u32(stg) + cb * (BM * 128), dcol, l0,
                        b_t * p.H + hh);
         }
         bulk_commit_group();
