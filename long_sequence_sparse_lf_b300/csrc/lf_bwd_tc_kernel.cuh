@@ -695,12 +695,23 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
         du[st] = ok ? dout[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
         qu[st] = ok ? q[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
       }
+      // the group's first row of the run: head and position (then stepped,
+      // RPI <= L rows at a time)
+      int bh = (run0 + lane / G) / L, i = run0 + lane / G - bh * L;
+      int d = head_dil[min(bh, (int)BH - 1) % H];
 #pragma unroll
       for (int st = 0; st < NS; ++st) {
         const int row = run0 + st * RPI + lane / G;
         const bool ok = row < r_end;
         const int rr = ok ? row : 0;
-        const int bh = rr / L, i = rr - bh * L;
+        if (st > 0) {
+          i += RPI;
+          if (i >= L) {
+            i -= L;
+            ++bh;
+            d = head_dil[min(bh, (int)BH - 1) % H];
+          }
+        }
         // all lanes take part in the group reductions below
         float of[8], df[8], qf[8];
         unpack8(ou[st], of);
@@ -731,7 +742,6 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
           }
         }
         const bool glob = ok && is_glob[i];
-        const int d = head_dil[bh % H];
         const float nl = ok ? -lse[rr] * LOG2E : 0.f;
         float dqa[8];
 #pragma unroll
@@ -751,7 +761,7 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
             pd += __shfl_xor_sync(0xffffffffu, pd, o);
           }
           const int diff = gidx[j] - i;
-          const bool in_band = (diff <= d * w && diff >= -d * w && diff % d == 0);
+          const bool in_band = (diff <= d * w && diff >= -d * w && (d == 1 || diff % d == 0));
           if (ok && !glob && !in_band) {
             const float pp = ex2_approx(fmaf(sd, sl2, nl));
             const float ds = pp * (pd - dl);
@@ -768,7 +778,7 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
           dqr[0] = make_float4(dqa[0], dqa[1], dqa[2], dqa[3]);
           dqr[1] = make_float4(dqa[4], dqa[5], dqa[6], dqa[7]);
           if (sub == 0) {
-            const int r = i % d, t = i / d;
+            const int t = d == 1 ? i : i / d, r = i - t * d;
             const float4 o = glob ? make_float4(-INF, 0.f, 0.f, 0.f) : make_float4(nl, -dl, 0.f, 0.f);
             stats[(long long)bh * stats_bh + (long long)r * btc_class_len(L, d) + t] = o;
             stats_n[(long long)bh * (L + kBtcQPad) + i] = o;
