@@ -85,6 +85,14 @@ __device__ __forceinline__ void layer_norm_row(float (&v)[NJ][VW], float eps,
                                                const float* __restrict__ beta, int lane,
                                                uint16_t* __restrict__ out_row) {
   constexpr int hidden = 32 * VW * NJ;
+  // gamma and beta first: their loads overlap the reductions
+  float g[NJ][VW], bt[NJ][VW];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int c = VW * lane + 32 * VW * j;
+    layer_load_f32<VW>(gamma + c, g[j]);
+    layer_load_f32<VW>(beta + c, bt[j]);
+  }
   float s = 0.f;
 #pragma unroll
   for (int j = 0; j < NJ; ++j)
@@ -107,11 +115,9 @@ __device__ __forceinline__ void layer_norm_row(float (&v)[NJ][VW], float eps,
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int c = VW * lane + 32 * VW * j;
-    float g[VW], bt[VW], y[VW];
-    layer_load_f32<VW>(gamma + c, g);
-    layer_load_f32<VW>(beta + c, bt);
+    float y[VW];
 #pragma unroll
-    for (int e = 0; e < VW; ++e) y[e] = (v[j][e] - mean) * rstd * g[e] + bt[e];
+    for (int e = 0; e < VW; ++e) y[e] = (v[j][e] - mean) * rstd * g[j][e] + bt[j][e];
     layer_store_bf16<VW>(out_row + c, y);
   }
 }
