@@ -48,6 +48,12 @@ CASES = [
     (1, 2, 640, 128, 20, (2, 1), tuple(range(5, 640, 4))),
     # L not a multiple of the query block, globals at both ends
     (1, 3, 333, 64, 50, (1, 1, 1), (0, 332)),
+    # the prep kernel's global-key pass at its limit (4 global tokens) and
+    # the global-key tiles just past it (5), D = 128 with dilation
+    (2, 2, 512, 64, 30, (1, 2), (10, 11, 200, 511)),
+    (1, 2, 512, 128, 30, (2, 1), (0, 64, 65, 300, 400)),
+    # one query tile per head
+    (1, 2, 128, 64, 4, (1, 1), (3,)),
 ]
 
 

@@ -80,6 +80,12 @@ SMALL = [
     W.LAYER_CONFIGS["layer-tiny"],
     W.LayerWorkload("d128-dilated", 1, 768, 2, 128, 40, (1, 2), (0, 100, 767), 12),
     W.LayerWorkload("h4-ragged", 2, 1000, 4, 64, 70, (1, 1, 2, 1), (3, 500), 13),
+    # hidden 64: 64-column q/k/v and feed-forward tiles; hidden 384: 128-wide
+    # q/k/v tiles and a cluster of three feed-forward CTAs; hidden 2048:
+    # 256-column feed-forward tiles in clusters of eight
+    W.LayerWorkload("h1-narrow", 1, 300, 1, 64, 20, (1,), (0,), 15),
+    W.LayerWorkload("h6-cluster3", 1, 512, 6, 64, 30, (1, 2, 1, 1, 2, 1), (7, 8, 9), 16),
+    W.LayerWorkload("h16-wide", 1, 256, 16, 128, 16, (1,) * 16, (0,), 17),
 ]
 
 
