@@ -1207,10 +1207,10 @@ bool g_gemm_smem_set[64][8] = {};
 // row-major (the caller sets P's output maps); grid (N / NT, row tiles):
 // B * ceil(L / 128) tiles of one batch element each for EPI 0, ceil(M / 128)
 // for EPI 1, with clusters of `cluster` CTAs along the columns.
-template <int NT, int EPI, int MH = 1>
+template <int NT, int EPI, int MH = 1, int ST = 0>
 lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const void* Bw,
                   long long M, int N, int K, int cluster, cudaStream_t stream, const char* name) {
-  using CF = lf::GemmCfg<NT, MH>;
+  using CF = lf::GemmCfg<NT, MH, ST>;
   lf_status s;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
@@ -1230,9 +1230,9 @@ lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const
   P.wait_iters = lf::wait_iters_for(wait_timeout_ns());
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    const int slot = MH == 2 ? 6 : (NT == 64 ? 0 : NT == 128 ? 1 : 2) * 2 + EPI;
+    const int slot = ST > 0 ? 7 : (MH == 2 ? 6 : (NT == 64 ? 0 : NT == 128 ? 1 : 2) * 2 + EPI);
     if (dev < 64 && !g_gemm_smem_set[dev][slot]) {
-      LF_CUDA(cudaFuncSetAttribute(lf::lf_gemm_tc_kernel<NT, EPI, MH>,
+      LF_CUDA(cudaFuncSetAttribute(lf::lf_gemm_tc_kernel<NT, EPI, MH, ST>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)CF::SMEM_BYTES));
       g_gemm_smem_set[dev][slot] = true;
@@ -1256,7 +1256,7 @@ lf_status gemm_tc(DevState* ds, int dev, lf::GemmParams& P, const void* A, const
     cfg.numAttrs = 1;
   }
   cudaError_t e = cudaSuccess;
-  traced(name, stream, [&] { e = cudaLaunchKernelEx(&cfg, lf::lf_gemm_tc_kernel<NT, EPI, MH>, P); });
+  traced(name, stream, [&] { e = cudaLaunchKernelEx(&cfg, lf::lf_gemm_tc_kernel<NT, EPI, MH, ST>, P); });
   if (e != cudaSuccess) return fail(LF_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(e));
   return LF_OK;
 }
@@ -1386,8 +1386,8 @@ lf_status layer_impl(const void* x, const void* w_qkv, const float* b_qkv, const
     }
     if (ff.nt == 64)
       s = gemm_tc<64, 1>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
-    else if (ff.nt == 128)
-      s = gemm_tc<128, 1>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
+    else if (ff.nt == 128)   // two stages: three CTAs per SM, one wave for layer-base
+      s = gemm_tc<128, 1, 1, 2>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
     else
       s = gemm_tc<256, 1>(ds, dev, P, x1, w_ff, M, hidden, hidden, ff.cluster, stream, "layer_gemm_ff_ln2");
     if (s != LF_OK) return s;

@@ -41,13 +41,16 @@ constexpr int kGemmBK = 64;           // K per stage: one 128-byte swizzle atom 
 constexpr int kGemmMaxCluster = 8;    // CTAs sharing a row in the LayerNorm epilogue
 
 // NT: columns per tile; MH: 128-row halves per tile (MH = 2: two M = 128
-// accumulators side by side in TMEM, sharing each B k-block)
-template <int NT, int MH = 1>
+// accumulators side by side in TMEM, sharing each B k-block); ST: pipeline
+// stages (0: the default for the shape).  Three CTAs fit an SM when their
+// shared memory allows (the feed-forward map's two-stage build).
+template <int NT, int MH = 1, int ST = 0>
 struct GemmCfg {
   static_assert(NT == 64 || NT == 128 || NT == 256, "tile width");
   static_assert(MH == 1 || MH == 2, "tile height");
   static constexpr int BM = kGemmBM * MH;              // rows per tile
-  static constexpr int STAGES = (MH == 2) ? 3 : ((NT == 256) ? 4 : (NT == 128 ? 3 : 4));
+  static constexpr int STAGES =
+      ST > 0 ? ST : ((MH == 2) ? 3 : ((NT == 256) ? 4 : (NT == 128 ? 3 : 4)));
   static constexpr uint32_t A_BYTES = BM * 128;        // BM rows x 64 bf16
   static constexpr uint32_t B_BYTES = NT * 128;        // NT rows x 64 bf16
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
@@ -61,7 +64,8 @@ struct GemmCfg {
   // the output staging rows ([128][NT] bf16) fit in the consumed stages
   static_assert(BM * NT * 2 <= STAGES * STAGE, "staging rows");
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
-  static constexpr int CTAS = (2 * SMEM_BYTES <= 228u * 1024u) ? 2 : 1;
+  static constexpr int CTAS =
+      (3 * (SMEM_BYTES + 1024) <= 228u * 1024u) ? 3 : ((2 * SMEM_BYTES <= 228u * 1024u) ? 2 : 1);
   static constexpr uint32_t TM_COLS = NT * MH;         // a power of two >= 32
   static constexpr int THREADS = 192;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory of one CTA");
@@ -135,10 +139,10 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t ran
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-template <int NT, int EPI, int MH = 1>
-__global__ void __launch_bounds__(192, GemmCfg<NT, MH>::CTAS)
+template <int NT, int EPI, int MH = 1, int ST = 0>
+__global__ void __launch_bounds__(192, GemmCfg<NT, MH, ST>::CTAS)
     lf_gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<NT, MH>;
+  using C = GemmCfg<NT, MH, ST>;
   static_assert(EPI == 0 || MH == 1, "the LayerNorm epilogue takes 128-row tiles");
   constexpr int BM = C::BM;
   extern __shared__ uint8_t smem_raw[];
@@ -253,7 +257,9 @@ __global__ void __launch_bounds__(192, GemmCfg<NT, MH>::CTAS)
       }
     }
     mbar_arrive(BAR(C::B_VEC));
-    constexpr int XPF = (EPI == 1) ? (NT <= 128 ? NT / 8 : 16) : 1;   // prefetched uint4
+    // prefetched uint4 of the row of x1 (fewer with three CTAs per SM, for
+    // their register budget)
+    constexpr int XPF = (EPI == 1) ? (C::CTAS >= 3 ? 4 : (NT <= 128 ? NT / 8 : 16)) : 1;
     uint4 xpf[XPF];
     const uint16_t* xr = p.resid + static_cast<size_t>(valid ? m : 0) * p.hidden + n0;
     if (EPI == 1) {
