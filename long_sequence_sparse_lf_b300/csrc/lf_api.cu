@@ -1617,13 +1617,13 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
         return (int)std::max<long long>(
             1, std::min<long long>((units + pthreads - 1) / pthreads, (long long)ds->num_sms * 16));
       };
-      // the rows: per thread (plain), or per run of 4 steps a warp
+      // the rows: per thread (plain), or per run of 2 steps a warp
       // (fused_gk)
       // fused_gk: a contiguous range of rows per block, at most L (two
-      // heads), a multiple of the warps' 4-step runs
-      const long long run_rows = 4 * (32 / (DD / 8));
+      // heads), a multiple of the warps' 2-step runs, three blocks per SM
+      const long long run_rows = 2 * (32 / (DD / 8));
       const long long rpb = std::max<long long>(
-          run_rows, std::min<long long>(ceil_div(rows, (long long)ds->num_sms * 2), L) / run_rows *
+          run_rows, std::min<long long>(ceil_div(rows, (long long)ds->num_sms * 3), L) / run_rows *
                         run_rows);
       const int nb0 = fused_gk ? (int)ceil_div(rows, rpb) : nblk(rows * (DD / 8));
       const int nb1 = nblk((long long)BH * NGQ * (DD / 8));

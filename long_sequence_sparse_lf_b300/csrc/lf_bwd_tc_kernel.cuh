@@ -575,14 +575,16 @@ __global__ void __launch_bounds__(192, BtcCfg<D>::CTAS)
 //                                         first; the band tiles add them to the
 //                                         global keys' dk, dv rows)
 // A block then takes a contiguous range of rows (`rows_per_block`, at most L,
-// so at most two heads), its warps runs of 4 steps of 32 / (D / 8)
-// consecutive rows whose loads they issue together.  A row group keeps
+// so at most two heads), its warps runs of 2 steps of 32 / (D / 8)
+// consecutive rows whose loads they issue together (two steps keep the
+// registers low enough for three blocks per SM with one global token: the
+// pass is bound by latency, not bandwidth).  A row group keeps
 // partial dkg, dvg sums in registers and adds them to the block's two head
 // slots in shared memory when its head changes; the block adds its slots to
 // dkg, dvg at the end.  GKN: the register arrays' size in global keys
 // (n_g <= GKN), 0 for the plain pass.
 template <int D, int GKN = 0>
-__global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
+__global__ void __launch_bounds__(256, GKN == 1 ? 3 : 2) lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
                                       const uint4* __restrict__ v, const uint4* __restrict__ out,
                                       const uint4* __restrict__ dout,
                                       const float* __restrict__ lse,
@@ -647,7 +649,7 @@ __global__ void lf_bwd_tc_prep_kernel(const uint4* __restrict__ q, const uint4* 
   } else if (part == 0) {
     constexpr int NGM = GK ? GKN : 1;
     constexpr int RPI = 32 / G;                      // rows per warp step
-    constexpr int NS = 4;                            // steps per run
+    constexpr int NS = 2;                            // steps per run
     constexpr int RUN = NS * RPI;
     const int rows = (int)(BH * L);
     const float sl2 = scale * LOG2E;
