@@ -1419,6 +1419,9 @@ bool g_bwd_smem_set[64] = {false};
 // kBwdGkeyMinBlocks .. kBwdGkeyBlocks blocks, so that a few global keys still
 // spread over the GPU
 constexpr int kBwdGkeyBlocks = 8, kBwdGkeyMinBlocks = 2;
+// resident blocks per SM of the fused prep kernel, per (device, D, global-key
+// build); 0 until queried
+int g_prep_occ[384] = {};
 
 lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
                    const void* dout, float* dq, float* dk, float* dv, int B, int H, int L, int D,
@@ -1619,15 +1622,42 @@ lf_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
       };
       // the rows: per thread (plain), or per run of 2 steps a warp
       // (fused_gk)
+      int nb1 = nblk((long long)BH * NGQ * (DD / 8));
+      int nb2 = nblk((long long)BH * 2 * lf::kBtcQPad);
       // fused_gk: a contiguous range of rows per block, at most L (two
-      // heads), a multiple of the warps' 2-step runs, three blocks per SM
+      // heads), a multiple of the warps' 2-step runs.  The blocks of all
+      // three parts are sized to be resident at once (one wave): the row
+      // blocks all take about the same time, and a second wave of a few of
+      // them would double the launch.  The gathered rows and the padding,
+      // a few row-slices per thread, take a quarter of their one-pass blocks.
       const long long run_rows = 2 * (32 / (DD / 8));
-      const long long rpb = std::max<long long>(
-          run_rows, std::min<long long>(ceil_div(rows, (long long)ds->num_sms * 3), L) / run_rows *
-                        run_rows);
+      long long rpb = run_rows;
+      if (fused_gk) {
+        nb1 = std::max(1, (nb1 + 3) / 4);
+        nb2 = std::max(1, (nb2 + 3) / 4);
+        const int gkn = n_g <= 1 ? 0 : n_g <= 2 ? 1 : 2;
+        int per_sm = 0;
+        {
+          std::lock_guard<std::mutex> lk(g_mu);
+          const int slot = (dev * 2 + (DD == 128 ? 1 : 0)) * 3 + gkn;
+          if (slot < 384 && g_prep_occ[slot] > 0) per_sm = g_prep_occ[slot];
+        }
+        if (per_sm == 0) {
+          const void* fn = gkn == 0   ? (const void*)lf::lf_bwd_tc_prep_kernel<DD, 1>
+                           : gkn == 1 ? (const void*)lf::lf_bwd_tc_prep_kernel<DD, 2>
+                                      : (const void*)lf::lf_bwd_tc_prep_kernel<DD, 4>;
+          LF_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pthreads, 0));
+          per_sm = std::max(per_sm, 1);
+          std::lock_guard<std::mutex> lk(g_mu);
+          const int slot = (dev * 2 + (DD == 128 ? 1 : 0)) * 3 + gkn;
+          if (slot < 384) g_prep_occ[slot] = per_sm;
+        }
+        const long long cap = (long long)ds->num_sms * per_sm;
+        const long long target = std::max(cap - nb1 - nb2, std::max(cap / 2, 1LL));
+        const long long want = ceil_div(ceil_div(rows, target), run_rows) * run_rows;
+        rpb = std::max<long long>(run_rows, std::min<long long>(want, L) / run_rows * run_rows);
+      }
       const int nb0 = fused_gk ? (int)ceil_div(rows, rpb) : nblk(rows * (DD / 8));
-      const int nb1 = nblk((long long)BH * NGQ * (DD / 8));
-      const int nb2 = nblk((long long)BH * 2 * lf::kBtcQPad);
       traced("bwd_prep", stream, [&] {
         auto args = [&](auto kern) {
           kern<<<nb0 + nb1 + nb2, pthreads, 0, stream>>>(

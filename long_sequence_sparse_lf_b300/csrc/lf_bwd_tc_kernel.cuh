@@ -689,6 +689,7 @@ __global__ void __launch_bounds__(256, GKN == 1 ? 3 : 2) lf_bwd_tc_prep_kernel(c
     for (int run0 = r_begin + wib * RUN; run0 < r_end; run0 += nwb * RUN) {
       // the run's loads first, all in flight together
       uint4 ou[NS], du[NS], qu[NS];
+      float lsv[NS];
 #pragma unroll
       for (int st = 0; st < NS; ++st) {
         const int row = run0 + st * RPI + lane / G;
@@ -696,6 +697,7 @@ __global__ void __launch_bounds__(256, GKN == 1 ? 3 : 2) lf_bwd_tc_prep_kernel(c
         ou[st] = ok ? out[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
         du[st] = ok ? dout[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
         qu[st] = ok ? q[(size_t)row * G + sub] : make_uint4(0, 0, 0, 0);
+        lsv[st] = ok ? lse[row] : 0.f;
       }
       // the group's first row of the run: head and position (then stepped,
       // RPI <= L rows at a time)
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(256, GKN == 1 ? 3 : 2) lf_bwd_tc_prep_kernel(c
           }
         }
         const bool glob = ok && is_glob[i];
-        const float nl = ok ? -lse[rr] * LOG2E : 0.f;
+        const float nl = ok ? -lsv[st] * LOG2E : 0.f;
         float dqa[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) dqa[e] = 0.f;
