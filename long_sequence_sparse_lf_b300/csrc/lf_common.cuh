@@ -117,34 +117,11 @@ struct SlotBlocks {
   }
 };
 
-// Blocks of item `wi` used by tile slot X.
-__host__ __device__ __forceinline__ bool blk_uses(const WorkItem& wi, int X, int j) {
-  if (wi.kind == 0) {
-    const bool present = wi.jlo[X] <= wi.jhi[X];
-    return present && (j >= wi.nkb || (j >= wi.jlo[X] && j <= wi.jhi[X]));
-  }
-  return j < wi.nkb && (j & 1) == X;
-}
-
+// Number of blocks of item `wi` that tile slot X uses (band and gathered
+// global blocks; extra blocks are counted apart).
 __host__ __device__ __forceinline__ int blk_count(const WorkItem& wi, int X) {
   if (wi.kind == 0) return wi.jlo[X] <= wi.jhi[X] ? wi.jhi[X] - wi.jlo[X] + 1 + wi.ngb : 0;
   return wi.nkb > X ? (wi.nkb - X + 1) / 2 : 0;
-}
-
-// first block used by slot X, or -1
-__host__ __device__ __forceinline__ int blk_first(const WorkItem& wi, int X) {
-  if (wi.kind == 0) return wi.jlo[X] <= wi.jhi[X] ? wi.jlo[X] : -1;
-  return wi.nkb > X ? X : -1;
-}
-
-// next block used by slot X after block j, or -1
-__host__ __device__ __forceinline__ int blk_next(const WorkItem& wi, int X, int j) {
-  if (wi.kind == 0) {
-    if (j < wi.jhi[X]) return j + 1;
-    if (j < wi.nkb) return wi.ngb > 0 ? wi.nkb : -1;
-    return j + 1 < wi.nkb + wi.ngb ? j + 1 : -1;
-  }
-  return j + 2 < wi.nkb ? j + 2 : -1;
 }
 
 struct MainParams {
@@ -195,16 +172,6 @@ __host__ __device__ __forceinline__ bool in_band_abs(int i, int j, int d, int w)
   int diff = j - i;
   int ad = diff < 0 ? -diff : diff;
   return ad <= d * w && (diff % d) == 0;
-}
-
-// Number of entries of the sorted array G[0..n) that are < x.
-__host__ __device__ __forceinline__ int sorted_lower(const int32_t* G, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (G[mid] < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
 }
 
 // Bits of the columns base .. base+31 that lie in [lo, hi) (bit c - base),
