@@ -852,13 +852,11 @@ lf_status fwd_impl(const void* q, const void* k, const void* v, void* out, bool 
     const size_t n4 = elems / 4;
     const int threads = 256;
     const int blocks = (int)std::min<size_t>((n4 + threads - 1) / threads, (size_t)ds->num_sms * 8);
-    const void* src[3] = {q, k, v};
-    for (int x = 0; x < 3; ++x) {
-      traced("cast_f32_bf16", stream, [&] {
-        lf::lf_cast_f32_bf16_kernel<<<blocks, threads, 0, stream>>>(
-            reinterpret_cast<const float4*>(src[x]), reinterpret_cast<uint2*>(cq + x * elems), n4);
-      });
-    }
+    traced("cast_f32_bf16", stream, [&] {
+      lf::lf_cast_f32_bf16_kernel<<<blocks, threads, 0, stream>>>(
+          reinterpret_cast<const float4*>(q), reinterpret_cast<const float4*>(k),
+          reinterpret_cast<const float4*>(v), reinterpret_cast<uint2*>(cq), n4);
+    });
     qb = cq;
     kb = cq + elems;
     vb = cq + 2 * elems;

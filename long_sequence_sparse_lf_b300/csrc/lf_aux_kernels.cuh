@@ -11,18 +11,26 @@
 namespace lf {
 
 // ---------------------------------------------------------------- cast
-// out[i] = bf16_rn(in[i]); n4 = number of float4 groups
-__global__ void lf_cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
+// q, k, v rounded to bf16 in one launch: out[x * n4 + i] = bf16_rn(in_x[i])
+// for x = 0, 1, 2 (in_0 = q, in_1 = k, in_2 = v); n4 = float4 groups of one
+// tensor.
+__global__ void lf_cast_f32_bf16_kernel(const float4* __restrict__ q, const float4* __restrict__ k,
+                                        const float4* __restrict__ v, uint2* __restrict__ out,
                                         size_t n4) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = in[i];
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t*>(&a);
-    o.y = *reinterpret_cast<uint32_t*>(&b);
-    out[i] = o;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+#pragma unroll 1
+  for (int x = 0; x < 3; ++x) {
+    const float4* __restrict__ in = x == 0 ? q : (x == 1 ? k : v);
+    uint2* __restrict__ dst = out + x * n4;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
+      const float4 f = in[i];
+      __nv_bfloat162 a = __floats2bfloat162_rn(f.x, f.y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f.z, f.w);
+      uint2 o;
+      o.x = *reinterpret_cast<uint32_t*>(&a);
+      o.y = *reinterpret_cast<uint32_t*>(&b);
+      dst[i] = o;
+    }
   }
 }
 
