@@ -11,7 +11,11 @@ Each check compares against something computed another way:
     layer with an explicit boolean mask built from oracle.key_set (the
     brute-force per-query key lists);
   - a zero feed-forward map: LN2 of an already normalised row (gamma 1,
-    beta 0) returns the row.
+    beta 0) returns the row;
+  - the stored (bf16) form against the masked torch layer rounding with
+    torch's own bf16 conversion at the same four storage points, element for
+    element, and not equal to a form that also rounds the q/k/v product
+    before its bias.
 The layer follows "基于Block-Sparse Attention的Longformer" §6.
 """
 import numpy as np
@@ -35,21 +39,32 @@ def _rng_layer(B, L, H, D, seed):
     return x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2
 
 
-def _torch_layer(x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, H, scale, eps, mask=None):
+def _torch_bf16(t):
+    """torch's own round-to-nearest-even conversion to bfloat16, back in float64."""
+    return t.to(torch.bfloat16).to(torch.float64)
+
+
+def _torch_layer(x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2, H, scale, eps, mask=None,
+                 store=lambda t: t, store_product=False):
     """Dense reference with torch library routines, float64.  mask: bool
-    [H, L, L] (True = attended) or None for full attention."""
+    [H, L, L] (True = attended) or None for full attention.  store: applied
+    where the layer stores a tensor (q, k, v; the attention output; x1; the
+    result); store_product also applies it to x W_qkv^T before the bias."""
     t = lambda a: torch.as_tensor(np.asarray(a), dtype=torch.float64)
     x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2 = map(t, (x, w_qkv, b_qkv, w_ff, b_ff, ln1, ln2))
     B, L, h = x.shape
     D = h // H
-    y = F.linear(x, w_qkv, b_qkv)                                   # [B, L, 3h]
+    if store_product:
+        y = store(store(F.linear(x, w_qkv)) + b_qkv)
+    else:
+        y = store(F.linear(x, w_qkv, b_qkv))                        # [B, L, 3h]
     q, k, v = (y[..., s * h:(s + 1) * h].reshape(B, L, H, D).transpose(1, 2) for s in range(3))
     am = None if mask is None else torch.as_tensor(mask)[None]     # [1, H, L, L]
     a = F.scaled_dot_product_attention(q, k, v, attn_mask=am, scale=scale)
-    a = a.transpose(1, 2).reshape(B, L, h)
-    x1 = F.layer_norm(x + a, (h,), ln1[:h], ln1[h:], eps)
+    a = store(a.transpose(1, 2).reshape(B, L, h))
+    x1 = store(F.layer_norm(x + a, (h,), ln1[:h], ln1[h:], eps))
     f = F.linear(x1, w_ff, b_ff)
-    return F.layer_norm(x1 + f, (h,), ln2[:h], ln2[h:], eps).numpy()
+    return store(F.layer_norm(x1 + f, (h,), ln2[:h], ln2[h:], eps)).numpy()
 
 
 def test_bf16_round_matches_torch_conversion():
@@ -136,3 +151,27 @@ def test_stored_bf16_layer_stays_close_to_float64_layer():
     # four bf16 stores of values of size ~1 (relative step 2^-8) move the
     # result by well under 0.1
     assert np.abs(stored - exact).max() < 0.1
+
+
+def test_stored_bf16_layer_against_torch_bf16_storage():
+    """The stored form against the masked dense torch layer that rounds with
+    torch's own bf16 conversion at the same four points (q, k, v after the
+    bias; the attention output; x1; the result).  The pre-rounding values of
+    the two agree to float64 rounding, so every element must match; rounding
+    the q/k/v product once more before its bias (a different storage
+    reading) must not."""
+    B, L, H, D, w = 2, 48, 2, 32, 4
+    dil, G = [1, 2], [0, 17, 30]
+    args = _rng_layer(B, L, H, D, 7)
+    scale = 1 / np.sqrt(D)
+    mask = np.zeros((H, L, L), dtype=bool)
+    for h in range(H):
+        for i in range(L):
+            mask[h, i, O.key_set(i, L, w, dil[h], G)] = True
+    got = O.longformer_layer(*args, H=H, w=w, dilation=dil, G=G, scale=scale, eps=1e-5,
+                             store_bf16=True)
+    want = _torch_layer(*args, H=H, scale=scale, eps=1e-5, mask=mask, store=_torch_bf16)
+    assert np.array_equal(got, want), np.abs(got - want).max()
+    other = _torch_layer(*args, H=H, scale=scale, eps=1e-5, mask=mask, store=_torch_bf16,
+                         store_product=True)
+    assert not np.array_equal(got, other)
